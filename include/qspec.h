@@ -1,0 +1,212 @@
+/*
+ * qspec.h -- C ABI of the QSPEC hot-path library (libqspec.so, sm_103a).
+ *
+ * QSPEC (speculative decoding with complementary quantisation schemes) drafts
+ * tokens with a W4A4 pass and verifies them with a W4A16 pass over ONE shared
+ * set of 4-bit weights, then overwrites the draft KV-cache entries of accepted
+ * tokens with the verify pass's.  This library holds the data-parallel steps of
+ * one such round.
+ *
+ * Sources, cited by page title and section:
+ *   [QS-bg]     "QSPEC: Speculative Decoding with Complementary Quantization
+ *               Schemes" summary page (molayo1419.me), background terms.
+ *   [QS-design] same page, "QSPEC structure".
+ *
+ * Conventions for every call
+ *   - Every pointer argument is a DEVICE pointer, owned by the caller, unless
+ *     stated otherwise.  The library allocates no device memory and keeps no
+ *     state between calls.  Outputs are written in place.
+ *   - bf16 and fp16 values travel as uint16_t bit patterns.
+ *   - Calls are enqueued on `stream` and return right after launch; results
+ *     and *dev_status are valid once the stream has synchronised.
+ *   - The return value reports what the host can check before launch
+ *     (QSPEC_ERR_NULL, _SHAPE, _ALIGN, _WORKSPACE, _UNSUPPORTED) and launch
+ *     failures (QSPEC_ERR_LAUNCH; see qspec_last_cuda_error()).  Nothing is
+ *     launched when it is not QSPEC_OK.
+ *   - dev_status (nullable) is a device int32 the caller zeroes.  Kernels that
+ *     detect a data error (QSPEC_ERR_RANGE, _ZERO_POINT, _NONFINITE) store its
+ *     code there if it still holds 0 (first error wins) and carry on; the
+ *     outputs that depend on the bad data are then unspecified.  No kernel
+ *     traps or spins without a bound.
+ *   - K is a multiple of the quantisation group, 128.  G = K / 128.
+ */
+#ifndef QSPEC_H
+#define QSPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so this header needs no CUDA
+ * header.  NULL is the legacy default stream. */
+typedef struct CUstream_st *qspec_stream_t;
+
+enum qspec_status {
+    QSPEC_OK = 0,
+    QSPEC_ERR_NULL = 1,        /* a required pointer is NULL */
+    QSPEC_ERR_SHAPE = 2,       /* a size is out of range (K % 128, gamma, ...) */
+    QSPEC_ERR_ALIGN = 3,       /* a pointer or leading dimension is misaligned */
+    QSPEC_ERR_LAUNCH = 4,      /* the CUDA launch failed */
+    QSPEC_ERR_WORKSPACE = 5,   /* the workspace is smaller than required */
+    QSPEC_ERR_RANGE = 6,       /* device: an index or code is out of range */
+    QSPEC_ERR_ZERO_POINT = 7,  /* device: a zero point is not an integer 0..15 */
+    QSPEC_ERR_NONFINITE = 8,   /* device: NaN / +inf input, or a row with no mass */
+    QSPEC_ERR_TIMEOUT = 9,     /* device: a bounded wait expired */
+    QSPEC_ERR_UNSUPPORTED = 10 /* the current device is not sm_103 */
+};
+
+#define QSPEC_GROUP 128
+#define QSPEC_MAX_GAMMA 16
+
+/* Library version as major*10000 + minor*100 + patch. */
+int qspec_version(void);
+
+/* Static string naming a status code. */
+const char *qspec_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char *qspec_last_cuda_error(void);
+
+/*
+ * a1. Pack INT4 weights.  [QS-bg] dequantisation W^ = s (W_INT4 - z);
+ * [QS-design] one 4-bit weight set serves both the W4A4 draft and the W4A16
+ * verify kernels, so this is the only weight format either reads.
+ *
+ *   codes  uint8  [N][K]   values 0..15 (output channel n, input index k)
+ *   s_fp16 uint16 [N][G]   fp16 scale of group g = k / 128 of row n
+ *   z_fp16 uint16 [N][G]   fp16 zero point; must be an integer 0..15
+ *   packed uint8  [N][K/2] out: byte j = code[2j] | code[2j+1] << 4
+ *   sz     uint32 [N][G]   out: fp16 bits of s | fp16 bits of z << 16
+ * Device errors: QSPEC_ERR_RANGE (a code > 15), QSPEC_ERR_ZERO_POINT,
+ * QSPEC_ERR_NONFINITE (a scale is inf/NaN).  codes, packed: 16-byte aligned.
+ */
+int qspec_pack_weights(const uint8_t *codes, const uint16_t *s_fp16, const uint16_t *z_fp16,
+                       int N, int K, uint8_t *packed, uint32_t *sz, int32_t *dev_status,
+                       qspec_stream_t stream);
+
+/*
+ * a2. Quantise activations to symmetric INT4 per token and 128-group.
+ * [QS-bg] W4A4 quantises activations as well as weights to 4 bits.
+ * Per row m and group g: amax = max |x|, sx = amax / 7 (fp32, IEEE
+ * division), q = clamp(rint(x / sx), -7, 7) (q = 0 when sx == 0), qs = sum q.
+ *
+ *   x_bf16 uint16 [M][ldx]  input rows (ldx >= K, ldx % 4 == 0, 8-byte aligned)
+ *   xq     uint8  [M][K/2]  out: two's-complement nibbles, byte j = q[2j] | q[2j+1] << 4
+ *   sx     float  [M][G]    out: scales
+ *   qs     int32  [M][G]    out: group sums of q
+ * Device errors: QSPEC_ERR_NONFINITE (a NaN or inf input).
+ */
+int qspec_quant_act_int4(const uint16_t *x_bf16, int M, int K, int ldx, uint8_t *xq, float *sx,
+                         int32_t *qs, int32_t *dev_status, qspec_stream_t stream);
+
+/*
+ * a3. W4A4 linear (draft).  [QS-bg] 4-bit activations times 4-bit weights,
+ * products accumulated in INT32, then scaled to 16 bits; [QS-design] the
+ * draft pass.  Bit-exact definition:
+ *   I[m][n][g] = sum_{k in g} q[m][k] * (W[n][k] - z[n][g])        (exact int)
+ *   acc = 0; for g = 0..G-1: acc = fmaf((float)I, sx[m][g] * s[n][g], acc)
+ *   y[m][n] = bf16 round-to-nearest-even(acc)
+ *
+ *   xq, sx, qs      from qspec_quant_act_int4 (qs must be its output)
+ *   packed, sz      from qspec_pack_weights, N rows
+ *   y_bf16 uint16 [M][ldy]  out (ldy >= N)
+ *   dbg_I  int32 [M][N][G]  nullable: out, the group integers I
+ * Any M >= 1; large M runs on the tensor cores (FP8 E4M3 operands holding the
+ * small integers exactly, fp32 accumulation of integer partial sums below 2^24
+ * -- exact -- drained per group).
+ */
+int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32_t *qs,
+                      const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
+                      uint16_t *y_bf16, int ldy, int32_t *dbg_I, int32_t *dev_status,
+                      qspec_stream_t stream);
+
+/*
+ * a4. W4A16 linear (verify).  [QS-bg] Y = X W^, W^ = s (W_INT4 - z),
+ * 16-bit activations; [QS-design] the verify pass over the gamma+1 rows of
+ * every sequence (M = B (gamma + 1)).  fp32 accumulation, bf16 output,
+ * within 1e-2 (1 + |ref|) of the fp64 value of the same definition.
+ *
+ *   x_bf16 uint16 [M][ldx]  (ldx >= K, ldx % 8 == 0, 16-byte aligned)
+ *   packed, sz              from qspec_pack_weights, N rows
+ *   y_bf16 uint16 [M][ldy]  out (ldy >= N)
+ */
+int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t *packed, const uint32_t *sz,
+                       int M, int N, int K, uint16_t *y_bf16, int ldy, int32_t *dev_status,
+                       qspec_stream_t stream);
+
+/* Bytes of workspace the verification calls need for (B, gamma, V). */
+size_t qspec_verify_workspace_bytes(int B, int gamma, int V);
+
+/*
+ * a5. Greedy verification.  [QS-bg] under greedy decoding a draft token is
+ * accepted when it is the target's top-1 token; nothing after the first
+ * rejection is kept; the target supplies one more token (the correction at
+ * the first mismatch, or a bonus token when all gamma drafts are accepted).
+ *
+ *   p_logits uint16 [B][gamma+1][V]  target (W4A16) logits, bf16
+ *   draft    int32  [B][gamma]       draft tokens
+ *   n_acc    int32  [B]              out: accepted drafts A_b (0..gamma)
+ *   out      int32  [B][gamma+1]     out: drafts 1..A_b, then the target's
+ *                                    argmax of row A_b (lowest id on ties);
+ *                                    entries after A_b are -1
+ *   workspace, ws_bytes              device scratch of
+ *                                    qspec_verify_workspace_bytes(B, gamma, V)
+ * 1 <= gamma <= 16.  Device errors: QSPEC_ERR_NONFINITE (NaN logit),
+ * QSPEC_ERR_RANGE (draft id outside [0, V)).
+ */
+int qspec_verify_greedy(const uint16_t *p_logits, const int32_t *draft, int B, int gamma, int V,
+                        int32_t *n_acc, int32_t *out, void *workspace, size_t ws_bytes,
+                        int32_t *dev_status, qspec_stream_t stream);
+
+/*
+ * a6. Sampled verification (speculative sampling).  [QS-bg] accept draft x
+ * with probability min(1, p(x|h) / q(x|h)); stop at the first rejection;
+ * replace it with a token drawn from the normalised residual max(0, p - q),
+ * or draw a bonus token from the last target row when all are accepted.
+ * Every decision is made in integers so that it is reproducible bit for bit:
+ *   E_v = rint(qexp(l_v - max_row) * 2^32) (own exp: Cody-Waite reduction and
+ *   a degree-7 Taylor polynomial in fp32), S = sum_v E_v;
+ *   accept iff U_i * Eq_t * Sp < 2^24 * Ep_t * Sq, U_i a 24-bit uniform;
+ *   residual R_v = max(0, Ep_v * Sq - Eq_v * Sp) (the target row if all zero);
+ *   draw v* = min{v : sum_{u<=v} w_u > floor(U' * sum w / 2^24)}.
+ * Uniforms: Philox4x32-10 (Salmon et al., SC'11), key = seed, counter =
+ * (slot, b, round lo, round hi), U = word0 >> 8; slot i-1 for draft i, slot
+ * gamma for the correction / bonus draw.
+ *
+ *   p_logits uint16 [B][gamma+1][V], q_logits uint16 [B][gamma][V] (bf16)
+ *   draft, n_acc, out, workspace: as in qspec_verify_greedy
+ * Device errors: QSPEC_ERR_NONFINITE (NaN or +inf logit, or a row that is all
+ * -inf), QSPEC_ERR_RANGE (draft id outside [0, V)).
+ */
+int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_logits, const int32_t *draft,
+                        int B, int gamma, int V, uint64_t seed, uint64_t round, int32_t *n_acc,
+                        int32_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                        qspec_stream_t stream);
+
+/*
+ * a7. KV overwrite.  [QS-design] for accepted tokens the low-precision (W4A4)
+ * KV-cache entries are replaced with the W4A16 ones, so later steps read the
+ * high-precision context from the one shared cache.  For each sequence b and
+ * r = 0..n_acc[b] (the last confirmed token and the accepted drafts):
+ *   cache[l][b][h][base_pos[b] + r][:] = new[l][b][r][h][:]   (K and V)
+ *
+ *   k_cache, v_cache uint16 [L][B][H][T][D]         bf16, updated in place
+ *   k_new, v_new     uint16 [L][B][gamma+1][H][D]   bf16 verify-pass rows
+ *   base_pos, n_acc  int32  [B]
+ * D % 8 == 0, all four tensors 16-byte aligned.  Device errors:
+ * QSPEC_ERR_RANGE when base_pos < 0, n_acc outside [0, gamma] or
+ * base_pos + n_acc >= T (that sequence is left untouched).
+ */
+int qspec_kv_overwrite(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+                       const uint16_t *v_new, const int32_t *base_pos, const int32_t *n_acc,
+                       int L, int B, int H, int T, int D, int gamma, int32_t *dev_status,
+                       qspec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSPEC_H */
