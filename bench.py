@@ -1,0 +1,585 @@
+#!/usr/bin/env python
+"""Benchmark of one QSPEC decoding round on the GB300 path.
+
+Workload (default): a Llama-3-8B-shaped model -- 32 layers, each with its
+seven linears stacked as qkv (4096 -> 6144), o (4096 -> 4096), gate/up
+(4096 -> 28672) and down (14336 -> 4096), plus the 4096 x 128256 LM head --
+with random INT4 weights (codes U{0..15}, fp16 scales U(0.005, 0.02), zero
+points U{0..15}, group 128), batch B = 1, gamma = 4 drafts.  One step is one
+round of the hot path:
+  gamma draft passes: per layer and linear, INT4 activation quantisation and
+      the W4A4 linear at M = B; then the W4A4 LM head;
+  one verify pass: every linear and the LM head in W4A16 at M = B (gamma + 1);
+  sampled verification of the gamma drafts over the 128256-token vocabulary;
+  the KV overwrite of the accepted rows in a 32-layer x 8-head x 4096 x 128
+  bf16 cache.
+Activations are bf16 N(0, 1) with 1 % outlier channels x20; target logits
+N(0, 3^2), draft logits = target + N(0, 0.5^2); drafts drawn from the draft
+rows.  Attention, norms and embeddings are not on this path and are not run;
+the verification reads its synthetic logits.  Weights (3.9 GB) exceed L2, so
+no flush is needed between steps.
+
+value    accepted tokens per second, sum_b (A_b + 1) / step time, with every
+         input resident in HBM (CUDA graphs, CUDA events around K steps).
+e2e      the same through host buffers: per step, pinned host -> device copy
+         of that step's inputs, the round, device -> host read of its tokens.
+roofline the dominant kernel (the W4A4 small-M linear), its algorithmic bytes
+         over its CUDA-event time, against the measured HBM copy bandwidth.
+
+--impl reference runs the CPU oracle (plain C, all host cores) on a bounded
+sample of the same round each step and extrapolates the round time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from quantized_speculative_decoding_shared_gb300 import synthetic as syn  # noqa: E402
+
+GROUP = 128
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "llama3-8b-decode-b1-g4": dict(shape=syn.LLAMA3_8B, B=1, gamma=4, outliers=0.01,
+                                   T=4096, p_std=3.0, q_noise=0.5, seed=1),
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3-8b-decode-b1-g4")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rounds", type=int, default=16, help="distinct captured rounds (RNG round ids)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (per launch) of the HBM-bound steps
+# ---------------------------------------------------------------------------
+def bytes_w4a16(M, N, K):
+    return K * N // 2 + 4 * N * K // GROUP + 2 * M * K + 2 * M * N
+
+
+def bytes_w4a4(M, N, K):
+    return K * N // 2 + 4 * N * K // GROUP + M * K // 2 + 8 * M * K // GROUP + 2 * M * N
+
+
+def bytes_quant(M, K):
+    return 2 * M * K + M * K // 2 + 8 * M * K // GROUP
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(name):
+    p = os.path.join(ROOT, "quantized_speculative_decoding_shared_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_file):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        d = json.load(open(p))
+        e = d[kernel_file]
+        if e.get("source_sha256_16") == kernel_source_hash(kernel_file):
+            return e
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            t = [v.strip() for v in line.split(",")]
+            if len(t) >= 9:
+                rows.append(t)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the round on the GPU
+# ---------------------------------------------------------------------------
+class GpuRound:
+    def __init__(self, wl, dev):
+        from quantized_speculative_decoding_shared_gb300 import binding as q
+        self.q = q
+        self.dev = dev
+        sh = wl["shape"]
+        self.B, self.gamma, self.T = wl["B"], wl["gamma"], wl["T"]
+        self.L, self.hidden, self.V = sh["layers"], sh["hidden"], sh["vocab"]
+        self.H, self.D = sh["kv_heads"], sh["head_dim"]
+        self.linears = syn.fused_layer_linears(sh)
+        seed = wl["seed"]
+        B, g, L = self.B, self.gamma, self.L
+        Mv = B * (g + 1)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # weights: one packed INT4 set per linear, shared by both passes
+        self.w = []
+        for l in range(L):
+            lw = {}
+            for j, (name, N, K) in enumerate(self.linears):
+                codes, s, z = syn.weights(N, K, seed * 100003 + l * 8 + j, device=dev)
+                lw[name] = q.pack_weights(codes, s, z, dev_status=self.status)
+                del codes, s, z
+            self.w.append(lw)
+        codes, s, z = syn.weights(self.V, self.hidden, seed * 100003 + 7777, device=dev)
+        self.lm = q.pack_weights(codes, s, z, dev_status=self.status)
+        del codes, s, z
+        # inputs: draft activations [gamma][L][B][K] per linear, verify [L][Mv][K]
+        self.xd, self.xv = {}, {}
+        for j, (name, N, K) in enumerate(self.linears):
+            self.xd[name] = syn.activations(g * L * B, K, seed * 7 + j, device=dev,
+                                            outlier_frac=wl["outliers"]).view(g, L, B, K)
+            self.xv[name] = syn.activations(L * Mv, K, seed * 11 + j, device=dev,
+                                            outlier_frac=wl["outliers"]).view(L, Mv, K)
+        self.xd_lm = syn.activations(g * B, self.hidden, seed * 13, device=dev,
+                                     outlier_frac=wl["outliers"]).view(g, B, self.hidden)
+        self.xv_lm = syn.activations(Mv, self.hidden, seed * 17, device=dev,
+                                     outlier_frac=wl["outliers"])
+        P, Q, d = syn.logits_noisy_draft(B, g, self.V, seed * 19, device=dev,
+                                         p_std=wl["p_std"], q_noise=wl["q_noise"])
+        self.P, self.Q, self.drafts = P, Q, d
+        self.kc, self.vc = syn.kv_cache(L, B, self.H, self.T, self.D, seed * 23, device=dev)
+        self.kn, self.vn = syn.kv_new(L, B, g, self.H, self.D, seed * 29, device=dev)
+        self.base = syn.base_positions(B, self.T, g, seed * 31, device=dev)
+        # scratch and outputs
+        Ks = sorted({K for _, _, K in self.linears} | {self.hidden})
+        self.qbuf = {K: (torch.empty((B, K // 2), dtype=torch.uint8, device=dev),
+                         torch.empty((B, K // GROUP), dtype=torch.float32, device=dev),
+                         torch.empty((B, K // GROUP), dtype=torch.int32, device=dev)) for K in Ks}
+        self.yd = {name: torch.empty((B, N), dtype=torch.bfloat16, device=dev)
+                   for name, N, _ in self.linears}
+        self.yv = {name: torch.empty((Mv, N), dtype=torch.bfloat16, device=dev)
+                   for name, N, _ in self.linears}
+        self.yd_lm = torch.empty((B, self.V), dtype=torch.bfloat16, device=dev)
+        self.yv_lm = torch.empty((Mv, self.V), dtype=torch.bfloat16, device=dev)
+        self.ws = q.verify_workspace(B, g, self.V, dev)
+        self.n_acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.out = torch.zeros((B, g + 1), dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+
+    # kernel launches of the library per step (for gpu_launches)
+    def launches_per_round(self):
+        n_lin = len(self.linears)
+        draft = self.gamma * (self.L * n_lin * 2 + 2)
+        verify = self.L * n_lin + 1
+        return draft + verify + 4 + 1
+
+    def _check(self, rc, what):
+        if rc != 0:
+            raise RuntimeError("%s returned %s" % (what, self.q.STATUS.get(rc, rc)))
+
+    def _w4a4(self, x, pk, N, K, y):
+        q = self.q
+        xq, sx, qs = self.qbuf[K]
+        M = x.shape[0]
+        self._check(q.qspec_quant_act_int4(x, M, K, K, xq, sx, qs, self.status), "quant")
+        self._check(q.qspec_linear_w4a4(xq, sx, qs, pk[0], pk[1], M, N, K, y, N, None,
+                                        self.status), "w4a4")
+
+    def draft_linears_only(self, j=0):
+        """One draft step's W4A4 launches without the quantiser (kernel timing)."""
+        q = self.q
+        for l in range(self.L):
+            for name, N, K in self.linears:
+                xq, sx, qs = self.qbuf[K]
+                self._check(q.qspec_linear_w4a4(xq, sx, qs, self.w[l][name][0], self.w[l][name][1],
+                                                self.B, N, K, self.yd[name], N, None, self.status),
+                            "w4a4")
+        xq, sx, qs = self.qbuf[self.hidden]
+        self._check(q.qspec_linear_w4a4(xq, sx, qs, self.lm[0], self.lm[1], self.B, self.V,
+                                        self.hidden, self.yd_lm, self.V, None, self.status), "w4a4")
+
+    def verify_linears_only(self):
+        q = self.q
+        Mv = self.B * (self.gamma + 1)
+        for l in range(self.L):
+            for name, N, K in self.linears:
+                self._check(q.qspec_linear_w4a16(self.xv[name][l], K, self.w[l][name][0],
+                                                 self.w[l][name][1], Mv, N, K, self.yv[name], N,
+                                                 self.status), "w4a16")
+        self._check(q.qspec_linear_w4a16(self.xv_lm, self.hidden, self.lm[0], self.lm[1], Mv,
+                                         self.V, self.hidden, self.yv_lm, self.V, self.status),
+                    "w4a16")
+
+    def bytes_draft_linears(self):
+        b = sum(bytes_w4a4(self.B, N, K) for _, N, K in self.linears) * self.L
+        return b + bytes_w4a4(self.B, self.V, self.hidden)
+
+    def bytes_verify_linears(self):
+        Mv = self.B * (self.gamma + 1)
+        b = sum(bytes_w4a16(Mv, N, K) for _, N, K in self.linears) * self.L
+        return b + bytes_w4a16(Mv, self.V, self.hidden)
+
+    def run(self, rnd, acc_slot=None):
+        q = self.q
+        for j in range(self.gamma):
+            for l in range(self.L):
+                for name, N, K in self.linears:
+                    self._w4a4(self.xd[name][j, l], self.w[l][name], N, K, self.yd[name])
+            self._w4a4(self.xd_lm[j], self.lm, self.V, self.hidden, self.yd_lm)
+        self.verify_linears_only()
+        self._check(q.qspec_verify_sample(self.P, self.Q, self.drafts, self.B, self.gamma, self.V,
+                                          1234, rnd, self.n_acc, self.out, self.ws,
+                                          self.ws.numel(), self.status), "verify_sample")
+        self._check(q.qspec_kv_overwrite(self.kc, self.vc, self.kn, self.vn, self.base, self.n_acc,
+                                         self.L, self.B, self.H, self.T, self.D, self.gamma,
+                                         self.status), "kv_overwrite")
+        if acc_slot is not None:
+            acc_slot.copy_(self.n_acc, non_blocking=True)
+
+    def host_inputs(self):
+        """The tensors a step reads from outside: all activations, logits,
+        drafts and cache positions (weights and the cache stay resident)."""
+        t = [self.xd[n] for n, _, _ in self.linears] + [self.xv[n] for n, _, _ in self.linears]
+        return t + [self.xd_lm, self.xv_lm, self.P, self.Q, self.drafts, self.base]
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_graph(g, reps, stream):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        torch.cuda.synchronize()
+        s.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) / reps
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: a bounded sample of the same round, extrapolated
+# ---------------------------------------------------------------------------
+class OracleRound:
+    """One layer of each pass, an LM-head row slice and the full verification
+    are run by the oracle; the round time is extrapolated to all layers and
+    rows (layers are identical in shape, rows of a linear are independent)."""
+
+    def __init__(self, wl, lm_rows=2048):
+        import oracle
+        self.o = oracle
+        self.wl = wl
+        sh = wl["shape"]
+        self.B, self.gamma, self.L, self.V = wl["B"], wl["gamma"], sh["layers"], sh["vocab"]
+        self.hidden = sh["hidden"]
+        self.linears = syn.fused_layer_linears(sh)
+        self.lm_rows = lm_rows
+        seed = wl["seed"]
+        self.packs = {}
+        for j, (name, N, K) in enumerate(self.linears):
+            codes, s, z = syn.weights(N, K, seed * 100003 + j)
+            st, p, szz = oracle.pack_weights(codes.numpy(), syn.bits16(s), syn.bits16(z))
+            self.packs[name] = (p, szz)
+        codes, s, z = syn.weights(lm_rows, self.hidden, seed * 100003 + 7777)
+        st, p, szz = oracle.pack_weights(codes.numpy(), syn.bits16(s), syn.bits16(z))
+        self.lm = (p, szz)
+        Mv = self.B * (self.gamma + 1)
+        self.xd = {n: syn.bits16(syn.activations(self.B, K, seed * 7 + j, outlier_frac=wl["outliers"]))
+                   for j, (n, _, K) in enumerate(self.linears)}
+        self.xv = {n: syn.bits16(syn.activations(Mv, K, seed * 11 + j, outlier_frac=wl["outliers"]))
+                   for j, (n, _, K) in enumerate(self.linears)}
+        self.xd_lm = syn.bits16(syn.activations(self.B, self.hidden, seed * 13))
+        self.xv_lm = syn.bits16(syn.activations(Mv, self.hidden, seed * 17))
+        P, Q, d = syn.logits_noisy_draft(self.B, self.gamma, self.V, seed * 19,
+                                         p_std=wl["p_std"], q_noise=wl["q_noise"])
+        self.P, self.Q, self.d = syn.bits16(P), syn.bits16(Q), d.numpy()
+        H, D, T = sh["kv_heads"], sh["head_dim"], wl["T"]
+        kc, vc = syn.kv_cache(1, self.B, H, T, D, seed * 23)
+        kn, vn = syn.kv_new(1, self.B, self.gamma, H, D, seed * 29)
+        self.kc, self.vc = syn.bits16(kc).copy(), syn.bits16(vc).copy()
+        self.kn, self.vn = syn.bits16(kn), syn.bits16(vn)
+        self.base = syn.base_positions(self.B, T, self.gamma, seed * 31).numpy()
+
+    def step(self, rnd):
+        o, t0 = self.o, time.perf_counter
+        a = t0()
+        for name, N, K in self.linears:                       # one layer, one draft step
+            st, xq, sx, qs = o.quant_act_int4(self.xd[name])
+            o.linear_w4a4(xq, sx, *self.packs[name])
+        b = t0()
+        st, xq, sx, qs = o.quant_act_int4(self.xd_lm)
+        o.linear_w4a4(xq, sx, *self.lm)                       # LM-head row slice
+        c = t0()
+        for name, N, K in self.linears:                       # one layer, verify pass
+            o.linear_w4a16(self.xv[name], *self.packs[name])
+        d = t0()
+        o.linear_w4a16(self.xv_lm, *self.lm)
+        e = t0()
+        st, n_acc, out = o.verify_sample(self.P, self.Q, self.d, 1234, rnd)
+        f = t0()
+        o.kv_overwrite(self.kc, self.vc, self.kn, self.vn, self.base, n_acc, self.gamma)
+        g = t0()
+        scale = self.V / self.lm_rows
+        t_round = (self.gamma * (self.L * (b - a) + (c - b) * scale) + self.L * (d - c)
+                   + (e - d) * scale + (f - e) + self.L * (g - f))
+        sampled = (b - a) + (c - b) + (d - c) + (e - d) + (f - e) + (g - f)
+        return int((n_acc + 1).sum()), t_round, sampled
+
+
+def cpu_baseline(wl, steps=3):
+    import oracle
+    orc = OracleRound(wl)
+    orc.step(0)
+    tok = tsum = sampled = 0.0
+    for r in range(steps):
+        k, t, s = orc.step(r)
+        tok, tsum, sampled = tok + k, tsum + t, sampled + s
+    return {"value": tok / tsum, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": ("%d rounds; per round 1 of %d layers (draft and verify linears), LM head "
+                       "%d of %d rows, full verification and 1-layer KV overwrite, extrapolated "
+                       "to the full round; %.1f s of oracle time measured"
+                       % (steps, orc.L, orc.lm_rows, orc.V, sampled))}
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    wl = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = {"workload": args.workload, "model_shape": "llama3-8b (32 layers, 4096 hidden, "
+           "128256 vocab)", "batch": wl["B"], "gamma": wl["gamma"],
+           "l2": "inputs larger than L2 (3.9 GB of weights per step)",
+           "parallelism": "replicas x%d" % args.gpus}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        orc = OracleRound(wl)
+        for r in range(args.warmup):
+            orc.step(r)
+        tok = tsum = sampled = 0.0
+        for r in range(args.steps):
+            k, t, s = orc.step(args.warmup + r)
+            tok, tsum, sampled = tok + k, tsum + t, sampled + s
+        v = tok / tsum
+        line = {"impl": "reference", "metric": "accepted tokens/s", "value": v, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * tsum / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights; u64/u128 sums",
+                "data": "synthetic", "config": cfg,
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(),
+                                 "kind": "oracle",
+                                 "sample": "per step 1 of %d layers, LM head %d of %d rows, full "
+                                           "verification; %.1f s of oracle time in total"
+                                           % (orc.L, orc.lm_rows, orc.V, sampled)},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from quantized_speculative_decoding_shared_gb300 import build as qbuild
+    if not os.path.exists(os.path.join(ROOT, "quantized_speculative_decoding_shared_gb300", "_lib",
+                                       "libqspec.so")):
+        qbuild.build()
+    rnd_obj = GpuRound(wl, dev)
+    stream = torch.cuda.Stream(device=dev)
+    R = max(1, args.rounds)
+    acc_log = torch.zeros((R, wl["B"]), dtype=torch.int32, device=dev)
+    # eager round first: sets kernel attributes outside capture, checks status
+    with torch.cuda.stream(stream):
+        rnd_obj.run(0)
+    torch.cuda.synchronize()
+    if int(rnd_obj.status.item()) != 0:
+        raise RuntimeError("device status %d after the eager round" % int(rnd_obj.status.item()))
+    graphs = [capture(lambda r=r: rnd_obj.run(r, acc_log[r]), stream) for r in range(R)]
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up, then K timed steps
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % R].replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % R].replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    acc = acc_log.cpu().numpy()
+    tokens = int(sum((acc[i % R] + 1).sum() for i in range(args.steps)))
+    if int(rnd_obj.status.item()) != 0:
+        raise RuntimeError("device status %d" % int(rnd_obj.status.item()))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, float(tokens)], dtype=torch.float64, device=dev)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        ms, tokens = float(mx[0]), int(t[1])
+    value = tokens / (ms / 1e3)
+
+    # dominant kernel: one draft step's W4A4 linears, graph-replayed alone
+    g4 = capture(rnd_obj.draft_linears_only, stream)
+    g16 = capture(rnd_obj.verify_linears_only, stream)
+    reps = 10
+    t4 = time_graph(g4, reps, stream)
+    t16 = time_graph(g16, reps, stream)
+    n4 = rnd_obj.L * len(rnd_obj.linears) + 1
+    peak, peak_kind = measured_peaks()
+    ach4 = rnd_obj.bytes_draft_linears() / (t4 / 1e3) / 1e9
+    ach16 = rnd_obj.bytes_verify_linears() / (t16 / 1e3) / 1e9
+    traffic = recorded_traffic("w4a4.cu")
+    roofline = {"bound": "hbm", "kernel": "w4a4_gemv_kernel<1> (W4A4 linear, M = 1)",
+                "achieved": round(ach4, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach4 / peak, 4), "peak_source": peak_kind,
+                "bytes_per_launch": rnd_obj.bytes_draft_linears() / n4,
+                "launch_us": 1e3 * t4 / n4,
+                "traffic": traffic["dram_bytes_per_launch"] if traffic else None}
+
+    # e2e: host buffers, copies inside the timed region
+    host_in = [t.cpu().pin_memory() for t in rnd_obj.host_inputs()]
+    dev_in = rnd_obj.host_inputs()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    out_host = torch.empty_like(rnd_obj.out, device="cpu").pin_memory()
+    nacc_host = torch.empty_like(rnd_obj.n_acc, device="cpu").pin_memory()
+    d2h = out_host.numel() * 4 + nacc_host.numel() * 4
+    e2e_tokens = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            for hsrc, ddst in zip(host_in, dev_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            graphs[i % R].replay()
+            out_host.copy_(rnd_obj.out, non_blocking=True)
+            nacc_host.copy_(rnd_obj.n_acc, non_blocking=True)
+            stream.synchronize()
+            e2e_tokens += int((nacc_host + 1).sum())
+    t_e2e = time.perf_counter() - t0
+    e2e_ms = [t_e2e * 1e3]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_e2e, float(e2e_tokens)], dtype=torch.float64, device=dev)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        t_e2e, e2e_tokens = float(mx[0]), int(t[1])
+
+    if rank != 0:
+        return
+    line = {"metric": "accepted tokens/s", "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4 w; int32 acc (W4A4) / bf16 x "
+            "fp32 acc (W4A16); u64/u128 integer verification", "data": "synthetic",
+            "config": cfg, "tokens_per_step": tokens / args.steps / world,
+            "e2e": {"value": round(e2e_tokens / t_e2e, 2), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "roofline": roofline,
+            "kernels": {"w4a4_draft_linears": {"GB/s": round(ach4, 1), "frac_hbm": round(ach4 / peak, 4),
+                                               "ms_per_draft_step": round(t4, 4), "M": wl["B"]},
+                        "w4a16_verify_linears": {"GB/s": round(ach16, 1),
+                                                 "frac_hbm": round(ach16 / peak, 4),
+                                                 "ms_per_verify_pass": round(t16, 4),
+                                                 "M": wl["B"] * (wl["gamma"] + 1)}},
+            "gpu_launches": rnd_obj.launches_per_round() * args.steps,
+            "clocks": clk}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

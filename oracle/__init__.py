@@ -101,8 +101,15 @@ def _load():
         lib.orc_kv_overwrite.argtypes = [_P(u16), _P(u16), _P(u16), _P(u16), _P(i32), _P(i32),
                                          I, I, I, I, I, I]
         lib.orc_kv_overwrite.restype = I
+        lib.orc_num_threads.argtypes = []
+        lib.orc_num_threads.restype = I
         _lib = lib
         return lib
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use (its CPU-baseline core count)."""
+    return int(_load().orc_num_threads())
 
 
 def _ptr(a: np.ndarray, ctype):

@@ -46,6 +46,7 @@
  * explicit fmaf and every other operation is rounded on its own.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -61,6 +62,9 @@ enum {
 };
 
 #define GROUP 128
+
+/* threads an OpenMP region of the oracle uses */
+int orc_num_threads(void) { return omp_get_max_threads(); }
 
 /* ------------------------------------------------------------------ */
 /* number formats                                                       */

@@ -1,0 +1,101 @@
+// abi.cu -- version, status strings, error text, device checks.
+#include <cstdio>
+#include <cstring>
+
+#include "qspec_host.h"
+
+namespace qspec {
+
+static thread_local char g_last_error[256] = "";
+
+void set_last_error(const char *where, cudaError_t e) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+             cudaGetErrorString(e));
+}
+
+static constexpr int kMaxDevices = 64;
+static int g_device_ok[kMaxDevices];   // 0 unknown, 1 ok, -1 unsupported
+static int g_sm_count[kMaxDevices];
+
+int check_device() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_last_error("cudaGetDevice", e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return QSPEC_ERR_UNSUPPORTED;
+    if (g_device_ok[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = sms;
+        g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_device_ok[dev] == 1 ? QSPEC_OK : QSPEC_ERR_UNSUPPORTED;
+}
+
+int sm_count() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices || g_sm_count[dev] <= 0) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev] = sms;
+        return sms > 0 ? sms : 1;
+    }
+    return g_sm_count[dev];
+}
+
+static unsigned char g_smem_set[kMaxDevices][64];
+
+int smem_limit_once(const void *func, int slot, int bytes) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= 64) return QSPEC_ERR_UNSUPPORTED;
+    if (g_smem_set[dev][slot]) return QSPEC_OK;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) {
+        set_last_error("cudaFuncSetAttribute", e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    g_smem_set[dev][slot] = 1;
+    return QSPEC_OK;
+}
+
+int check_launch(const char *where) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_last_error(where, e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    return QSPEC_OK;
+}
+
+}  // namespace qspec
+
+extern "C" {
+
+int qspec_version(void) { return 100; }   // 0.1.0
+
+const char *qspec_status_string(int status) {
+    switch (status) {
+        case QSPEC_OK: return "QSPEC_OK";
+        case QSPEC_ERR_NULL: return "QSPEC_ERR_NULL";
+        case QSPEC_ERR_SHAPE: return "QSPEC_ERR_SHAPE";
+        case QSPEC_ERR_ALIGN: return "QSPEC_ERR_ALIGN";
+        case QSPEC_ERR_LAUNCH: return "QSPEC_ERR_LAUNCH";
+        case QSPEC_ERR_WORKSPACE: return "QSPEC_ERR_WORKSPACE";
+        case QSPEC_ERR_RANGE: return "QSPEC_ERR_RANGE";
+        case QSPEC_ERR_ZERO_POINT: return "QSPEC_ERR_ZERO_POINT";
+        case QSPEC_ERR_NONFINITE: return "QSPEC_ERR_NONFINITE";
+        case QSPEC_ERR_TIMEOUT: return "QSPEC_ERR_TIMEOUT";
+        case QSPEC_ERR_UNSUPPORTED: return "QSPEC_ERR_UNSUPPORTED";
+        default: return "QSPEC_ERR_UNKNOWN";
+    }
+}
+
+const char *qspec_last_cuda_error(void) { return qspec::g_last_error; }
+
+}  // extern "C"

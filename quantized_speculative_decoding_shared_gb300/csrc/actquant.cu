@@ -1,0 +1,92 @@
+// actquant.cu -- a2: symmetric INT4 quantisation of bf16 activations per token
+// and 128-group (QSPEC summary page, background terms: W4A4 quantises the
+// activations to 4 bits as well as the weights).
+//
+// Per (m, g): amax = max |x|, sx = amax / 7 (IEEE fp32 division),
+// q = clamp(rint(x / sx), -7, 7) (0 when sx == 0), qs = sum q.
+// Half a warp per group: 16 lanes x 8 bf16 (one 16-byte load each), amax and
+// qs by shuffles over the half warp.  HBM-bound: 2 bytes read and ~0.53
+// bytes written per element.
+#include "qspec_device.cuh"
+#include "qspec_host.h"
+
+namespace qspec {
+
+__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restrict__ x, int M, int K,
+                                                       int ldx, uint8_t *__restrict__ xq,
+                                                       float *__restrict__ sx,
+                                                       int32_t *__restrict__ qs, int32_t *st) {
+    const int G = K / kGroup;
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4, hl = lane & 15;
+    const long long pairs_per_row = (G + 1) / 2;
+    long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
+    bool bad = false;
+    for (; warp < (long long)M * pairs_per_row; warp += n_warps) {
+        int m = (int)(warp / pairs_per_row);
+        int g = (int)(warp % pairs_per_row) * 2 + half;
+        bool active = g < G;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (active)
+            v = __ldcs(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup) + hl);
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            bad |= !isfinite(f[i]);
+            amax = fmaxf(amax, fabsf(f[i]));
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        float scale = __fdiv_rn(amax, 7.0f);
+        int sum = 0;
+        uint32_t nib = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int q = 0;
+            if (scale != 0.0f) {
+                q = __float2int_rn(__fdiv_rn(f[i], scale));
+                q = max(-7, min(7, q));
+            }
+            sum += q;
+            nib |= (uint32_t)(q & 15) << (4 * i);
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (active) {
+            reinterpret_cast<uint32_t *>(xq + (size_t)m * (K / 2) + (size_t)g * (kGroup / 2))[hl] = nib;
+            if (hl == 0) {
+                sx[(size_t)m * G + g] = scale;
+                qs[(size_t)m * G + g] = sum;
+            }
+        }
+    }
+    if (bad) flag(st, QSPEC_ERR_NONFINITE);
+}
+
+}  // namespace qspec
+
+using namespace qspec;
+
+extern "C" int qspec_quant_act_int4(const uint16_t *x_bf16, int M, int K, int ldx, uint8_t *xq,
+                                    float *sx, int32_t *qs, int32_t *dev_status,
+                                    qspec_stream_t stream) {
+    if (!x_bf16 || !xq || !sx || !qs) return QSPEC_ERR_NULL;
+    if (M < 1 || K < kGroup || K % kGroup || ldx < K) return QSPEC_ERR_SHAPE;
+    if (!aligned(x_bf16, 16) || ldx % 8 || !aligned(xq, 4) || !aligned(sx, 4) || !aligned(qs, 4))
+        return QSPEC_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    long long warps = (long long)M * ((K / kGroup + 1) / 2);
+    long long blocks = (warps * 32 + 255) / 256;
+    unsigned grid = (unsigned)std::min<long long>(blocks, (long long)sm_count() * 16);
+    quant_act_kernel<<<grid, 256, 0, as_cuda(stream)>>>(x_bf16, M, K, ldx, xq, sx, qs, dev_status);
+    return check_launch("qspec_quant_act_int4");
+}

@@ -1,0 +1,108 @@
+// qspec_device.cuh -- device helpers shared by the library's kernels.
+//
+// Nothing here is shared with the CPU oracle: the Philox generator and the
+// fixed-point exp are written separately on each side from their published
+// definitions.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "qspec.h"
+
+namespace qspec {
+
+constexpr int kGroup = QSPEC_GROUP;
+
+// First data error wins: later codes never overwrite an earlier one.
+__device__ __forceinline__ void flag(int32_t *st, int code) {
+    if (st != nullptr && code != QSPEC_OK) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
+    return __uint_as_float(b << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even (the bf16 intrinsic).
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// Monotone map of fp32 onto uint32: a < b (as floats, no NaN) iff enc(a) < enc(b).
+// enc(x) > 0 for every x, so 0 works as a "minus infinity" start value.
+__device__ __forceinline__ uint32_t ordered_bits(float x) {
+    uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered_bits(uint32_t e) {
+    uint32_t u = (e & 0x80000000u) ? (e & 0x7fffffffu) : ~e;
+    return __uint_as_float(u);
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies with the
+// published multipliers, key bumped by the published Weyl constants.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
+        uint32_t hi0 = __umulhi(m0, c0), lo0 = m0 * c0;
+        uint32_t hi1 = __umulhi(m1, c2), lo1 = m1 * c2;
+        uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c0;
+}
+
+// 24-bit uniform for draw `slot` of sequence b in verification round `round`.
+__device__ __forceinline__ uint32_t uniform24(uint64_t seed, uint64_t round, uint32_t slot,
+                                              uint32_t b) {
+    return philox_word0(slot, b, (uint32_t)round, (uint32_t)(round >> 32), (uint32_t)seed,
+                        (uint32_t)(seed >> 32)) >> 8;
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-point softmax weight E = rint(e^(l - m) * 2^32), l <= m.
+// e^x for x in [-32, 0]: Cody-Waite reduction x = n ln2 + r (ln2 split into a
+// 12-significant-bit head and a tail), degree-7 Taylor polynomial of e^r in
+// Horner form, exact scaling by 2^n.  Every step is one fp32 operation,
+// rounded to nearest; the fused steps are explicit fmas.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float qexp(float x) {
+    if (x < -32.0f) return 0.0f;
+    const float log2e = __uint_as_float(0x3FB8AA3Bu);
+    const float ln2_hi = __uint_as_float(0x3F317200u);
+    const float ln2_lo = __uint_as_float(0x35BFBE8Eu);
+    float n = rintf(__fmul_rn(x, log2e));
+    float r = __fmaf_rn(-n, ln2_hi, x);
+    r = __fmaf_rn(-n, ln2_lo, r);
+    float p = __uint_as_float(0x39500D01u);            // 1/7!
+    p = __fmaf_rn(p, r, __uint_as_float(0x3AB60B61u)); // 1/6!
+    p = __fmaf_rn(p, r, __uint_as_float(0x3C088889u)); // 1/5!
+    p = __fmaf_rn(p, r, __uint_as_float(0x3D2AAAABu)); // 1/4!
+    p = __fmaf_rn(p, r, __uint_as_float(0x3E2AAAABu)); // 1/3!
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    int e = (int)n;                                     // -47 <= e <= 0
+    return __fmul_rn(p, __int_as_float((e + 127) << 23));
+}
+
+__device__ __forceinline__ uint64_t fixed_weight(float l, float m) {
+    float e = qexp(__fsub_rn(l, m));
+    return __float2ull_rn(__fmul_rn(e, 4294967296.0f));
+}
+
+typedef unsigned __int128 u128;
+
+}  // namespace qspec

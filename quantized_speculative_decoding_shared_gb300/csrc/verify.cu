@@ -1,0 +1,559 @@
+// verify.cu -- a5 greedy and a6 sampled verification of gamma draft tokens.
+//
+// QSPEC summary page, background terms: speculative sampling accepts a draft
+// x with probability min(1, p(x|h) / q(x|h)); greedy decoding accepts it when
+// it is the target's top-1 token; nothing after the first rejection is kept;
+// the target then supplies one more token (a correction drawn from the
+// normalised residual max(0, p - q), or a bonus token from the last target
+// row when every draft is accepted), so L = A + 1 tokens are emitted.
+// "QSPEC structure": the verify pass yields gamma + 1 target distributions.
+//
+// All decisions are integer so they are reproducible bit for bit:
+//   E_v = rint(qexp(l_v - row max) * 2^32), S = sum_v E_v (exact in uint64);
+//   accept draft i iff U_i * Eq_t * Sp < 2^24 * Ep_t * Sq (128-bit);
+//   residual R_v = max(0, Ep_v Sq - Eq_v Sp) (128-bit; the target row's E if
+//   every R_v is 0); draw v* = min{v : sum_{u<=v} w_u > floor(U' sum w / 2^24)}.
+// Integer sums are associative, so rows are split into chunks processed by
+// many CTAs and combined with atomics without changing a single bit.
+//
+// Launch sequence (one stream, no host synchronisation):
+//   greedy : memset, argmax (chunk x row), finalize (per sequence)
+//   sampled: memset, row max (chunk x row), row sums (chunk x row),
+//            decisions + residual chunk sums (chunk x sequence),
+//            draw (per sequence)
+// HBM traffic: one read of every logit (B (2 gamma + 1) V bf16) plus L2
+// re-reads of the rows a later phase needs.
+#include <algorithm>
+
+#include "qspec_device.cuh"
+#include "qspec_host.h"
+
+namespace qspec {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSub = kThreads * 8;    // elements one CTA covers per pass (8 per thread)
+constexpr int kMaxChunks = 256;
+
+struct Layout {
+    int chunk;        // elements per chunk (multiple of kSub)
+    int n_chunks;     // <= kMaxChunks
+    size_t off_key, off_max, off_sum, off_rsum, off_esum, off_acc, total;
+};
+
+inline size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+Layout make_layout(int B, int gamma, int V) {
+    Layout L;
+    int subs = (V + kSub - 1) / kSub;
+    int per = (subs + kMaxChunks - 1) / kMaxChunks;
+    L.chunk = per * kSub;
+    L.n_chunks = (V + L.chunk - 1) / L.chunk;
+    size_t rows_g = (size_t)B * (gamma + 1), rows_s = (size_t)B * (2 * gamma + 1);
+    size_t o = 0;
+    L.off_key = o;  o = align16(o + rows_g * 8);                 // greedy argmax keys
+    L.off_max = o;  o = align16(o + rows_s * 4);                 // row max, ordered bits
+    L.off_sum = o;  o = align16(o + rows_s * 8);                 // row sums S
+    L.off_rsum = o; o = align16(o + (size_t)B * L.n_chunks * 16); // residual chunk sums
+    L.off_esum = o; o = align16(o + (size_t)B * L.n_chunks * 8);  // target-row chunk sums
+    L.off_acc = o;  o = align16(o + (size_t)B * 4);              // A_b
+    L.total = o;
+    return L;
+}
+
+// -------------------------------------------------------------------------
+// helpers: load 8 logits of a row starting at element v0 (V % 8 == 0 path,
+// else element-wise); missing elements read as -inf.
+// -------------------------------------------------------------------------
+template <bool VEC>
+__device__ __forceinline__ void load8(const uint16_t *row, int v0, int V, float f[8]) {
+    if (VEC) {
+        if (v0 + 8 <= V) {
+            uint4 u = __ldg(reinterpret_cast<const uint4 *>(row + v0));
+            uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+            return;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = (v0 + i < V) ? bf16_bits_to_float(row[v0 + i]) : -INFINITY;
+}
+
+template <typename T>
+__device__ __forceinline__ T block_reduce_max(T v, T *sh) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        T u = __shfl_xor_sync(0xffffffffu, v, o);
+        v = u > v ? u : v;
+    }
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        v = threadIdx.x < kThreads / 32 ? sh[threadIdx.x] : sh[0];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            T u = __shfl_xor_sync(0xffffffffu, v, o);
+            v = u > v ? u : v;
+        }
+    }
+    __syncthreads();
+    return v;   // valid in thread 0
+}
+
+__device__ __forceinline__ unsigned long long block_reduce_sum(unsigned long long v,
+                                                               unsigned long long *sh) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        v = threadIdx.x < kThreads / 32 ? sh[threadIdx.x] : 0ull;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    }
+    __syncthreads();
+    return v;
+}
+
+// inclusive block scan of u128 values (kThreads entries in shared memory)
+__device__ __forceinline__ u128 block_scan_u128(u128 v, u128 *buf) {
+    buf[threadIdx.x] = v;
+    __syncthreads();
+    for (int off = 1; off < kThreads; off <<= 1) {
+        u128 add = threadIdx.x >= off ? buf[threadIdx.x - off] : (u128)0;
+        __syncthreads();
+        buf[threadIdx.x] += add;
+        __syncthreads();
+    }
+    return buf[threadIdx.x];
+}
+
+// -------------------------------------------------------------------------
+// greedy
+// -------------------------------------------------------------------------
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) greedy_argmax_kernel(const uint16_t *__restrict__ P, int V,
+                                                                int chunk,
+                                                                unsigned long long *__restrict__ keys,
+                                                                int32_t *st) {
+    __shared__ unsigned long long sh[kThreads / 32];
+    const int row = blockIdx.y;
+    const uint16_t *rp = P + (size_t)row * V;
+    const int c0 = blockIdx.x * chunk, c1 = min(V, c0 + chunk);
+    unsigned long long best = 0;
+    bool bad = false;
+    for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
+        float f[8];
+        load8<VEC>(rp, v0, c1, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (v0 + i >= c1) break;
+            bad |= isnan(f[i]);
+            unsigned long long key = ((unsigned long long)ordered_bits(f[i]) << 32) |
+                                     (0xFFFFFFFFu - (uint32_t)(v0 + i));
+            best = key > best ? key : best;
+        }
+    }
+    if (bad) flag(st, QSPEC_ERR_NONFINITE);
+    best = block_reduce_max(best, sh);
+    if (threadIdx.x == 0) atomicMax(keys + row, best);
+}
+
+__global__ void greedy_finalize_kernel(const unsigned long long *__restrict__ keys,
+                                       const int32_t *__restrict__ draft, int B, int gamma, int V,
+                                       int32_t *__restrict__ n_acc, int32_t *__restrict__ out,
+                                       int32_t *st) {
+    int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const unsigned long long *k = keys + (size_t)b * (gamma + 1);
+    const int32_t *d = draft + (size_t)b * gamma;
+    int A = gamma;
+    bool bad = false;
+    for (int i = 0; i < gamma; ++i) {
+        int t = d[i];
+        bad |= (t < 0 || t >= V);
+        int arg = (int)(0xFFFFFFFFu - (uint32_t)(k[i] & 0xFFFFFFFFull));
+        if (A == gamma && t != arg) A = i;
+    }
+    if (bad) flag(st, QSPEC_ERR_RANGE);
+    int32_t *o = out + (size_t)b * (gamma + 1);
+    for (int i = 0; i <= gamma; ++i) o[i] = i < A ? d[i] : -1;
+    o[A] = (int)(0xFFFFFFFFu - (uint32_t)(k[A] & 0xFFFFFFFFull));
+    n_acc[b] = A;
+}
+
+// -------------------------------------------------------------------------
+// sampled: rows 0 .. B(gamma+1)-1 are P[b][i], then B gamma rows of Q[b][i]
+// -------------------------------------------------------------------------
+__device__ __forceinline__ const uint16_t *row_ptr(const uint16_t *P, const uint16_t *Q, int B,
+                                                   int gamma, int V, int row) {
+    int np = B * (gamma + 1);
+    return row < np ? P + (size_t)row * V : Q + (size_t)(row - np) * V;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) sample_rowmax_kernel(const uint16_t *__restrict__ P,
+                                                                const uint16_t *__restrict__ Q, int B,
+                                                                int gamma, int V, int chunk,
+                                                                uint32_t *__restrict__ maxenc,
+                                                                int32_t *st) {
+    __shared__ uint32_t sh[kThreads / 32];
+    const int row = blockIdx.y;
+    const uint16_t *rp = row_ptr(P, Q, B, gamma, V, row);
+    const int c0 = blockIdx.x * chunk, c1 = min(V, c0 + chunk);
+    float m = -INFINITY;
+    bool bad = false;
+    for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
+        float f[8];
+        load8<VEC>(rp, v0, c1, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            bad |= isnan(f[i]) || f[i] == INFINITY;
+            m = fmaxf(m, f[i]);
+        }
+    }
+    if (bad) flag(st, QSPEC_ERR_NONFINITE);
+    uint32_t e = block_reduce_max(ordered_bits(m), sh);
+    if (threadIdx.x == 0) atomicMax(maxenc + row, e);
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) sample_rowsum_kernel(const uint16_t *__restrict__ P,
+                                                                const uint16_t *__restrict__ Q, int B,
+                                                                int gamma, int V, int chunk,
+                                                                const uint32_t *__restrict__ maxenc,
+                                                                unsigned long long *__restrict__ sums,
+                                                                int32_t *st) {
+    __shared__ unsigned long long sh[kThreads / 32];
+    const int row = blockIdx.y;
+    const uint16_t *rp = row_ptr(P, Q, B, gamma, V, row);
+    const float m = from_ordered_bits(maxenc[row]);
+    if (m == -INFINITY) {                      // a row without any mass
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag(st, QSPEC_ERR_NONFINITE);
+        return;
+    }
+    const int c0 = blockIdx.x * chunk, c1 = min(V, c0 + chunk);
+    unsigned long long s = 0;
+    for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
+        float f[8];
+        load8<VEC>(rp, v0, c1, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s += fixed_weight(f[i], m);
+    }
+    s = block_reduce_sum(s, sh);
+    if (threadIdx.x == 0 && s) atomicAdd(sums + row, s);
+}
+
+// decisions of sequence b: A_b (first rejected draft index, gamma if none)
+__device__ int decide(const uint16_t *P, const uint16_t *Q, const int32_t *draft, int B, int gamma,
+                      int V, int b, uint64_t seed, uint64_t round, const uint32_t *maxenc,
+                      const unsigned long long *sums, bool *range_bad) {
+    // thread i < gamma tests draft i; result combined with a ballot in warp 0
+    int reject = 0;
+    bool bad = false;
+    if (threadIdx.x < 32) {
+        int i = threadIdx.x;
+        if (i < gamma) {
+            int t = draft[(size_t)b * gamma + i];
+            bad = t < 0 || t >= V;
+            t = bad ? 0 : t;
+            int rp = b * (gamma + 1) + i;
+            int rq = B * (gamma + 1) + b * gamma + i;
+            float mp = from_ordered_bits(maxenc[rp]), mq = from_ordered_bits(maxenc[rq]);
+            uint64_t Ep = fixed_weight(bf16_bits_to_float(P[(size_t)rp * V + t]), mp);
+            uint64_t Eq = fixed_weight(bf16_bits_to_float(Q[((size_t)b * gamma + i) * V + t]), mq);
+            uint64_t Sp = sums[rp], Sq = sums[rq];
+            uint32_t U = uniform24(seed, round, (uint32_t)i, (uint32_t)b);
+            u128 lhs = (u128)U * Sp * Eq;
+            u128 rhs = ((u128)Ep * Sq) << 24;
+            reject = !(lhs < rhs);
+        }
+        unsigned rj = __ballot_sync(0xffffffffu, reject);
+        unsigned bd = __ballot_sync(0xffffffffu, bad);
+        *range_bad = bd != 0;
+        return rj ? __ffs(rj) - 1 : gamma;
+    }
+    return -1;
+}
+
+// grid (chunk, b): decisions (recomputed by every chunk's CTA), then this
+// chunk's sums of the residual R_v and of the target row's E_v.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) sample_residual_kernel(
+    const uint16_t *__restrict__ P, const uint16_t *__restrict__ Q, const int32_t *__restrict__ draft,
+    int B, int gamma, int V, int chunk, uint64_t seed, uint64_t round,
+    const uint32_t *__restrict__ maxenc, const unsigned long long *__restrict__ sums,
+    u128 *__restrict__ rsum, unsigned long long *__restrict__ esum, int32_t *__restrict__ accbuf,
+    int32_t *__restrict__ n_acc, int32_t *__restrict__ out, int32_t *st) {
+    __shared__ int sA;
+    __shared__ u128 shr[kThreads / 32];
+    __shared__ unsigned long long she[kThreads / 32];
+    const int b = blockIdx.y;
+    bool range_bad = false;
+    int A = decide(P, Q, draft, B, gamma, V, b, seed, round, maxenc, sums, &range_bad);
+    if (threadIdx.x == 0) {
+        sA = A;
+        if (blockIdx.x == 0) {
+            if (range_bad) flag(st, QSPEC_ERR_RANGE);
+            accbuf[b] = A;
+            n_acc[b] = A;
+            int32_t *o = out + (size_t)b * (gamma + 1);
+            for (int i = 0; i <= gamma; ++i) o[i] = i < A ? draft[(size_t)b * gamma + i] : -1;
+        }
+    }
+    __syncthreads();
+    A = sA;
+    const int rp = b * (gamma + 1) + A;
+    const float mp = from_ordered_bits(maxenc[rp]);
+    const uint64_t Sp = sums[rp];
+    const bool residual = A < gamma;
+    const int rq = B * (gamma + 1) + b * gamma + (residual ? A : 0);
+    const float mq = from_ordered_bits(maxenc[rq]);
+    const uint64_t Sq = sums[rq];
+    const uint16_t *prow = P + (size_t)rp * V;
+    const uint16_t *qrow = Q + ((size_t)b * gamma + (residual ? A : 0)) * V;
+    const int c0 = blockIdx.x * chunk, c1 = min(V, c0 + chunk);
+    u128 r = 0;
+    unsigned long long e = 0;
+    for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
+        float fp[8], fq[8];
+        load8<VEC>(prow, v0, c1, fp);
+        if (residual) load8<VEC>(qrow, v0, c1, fq);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint64_t Ep = fixed_weight(fp[i], mp);
+            e += Ep;
+            if (residual) {
+                uint64_t Eq = fixed_weight(fq[i], mq);
+                u128 a = (u128)Ep * Sq, c = (u128)Eq * Sp;
+                r += a > c ? a - c : (u128)0;
+            }
+        }
+    }
+    // block sums (u128 via two halves with carry handled by the scan helper)
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        uint64_t lo = (uint64_t)r, hi = (uint64_t)(r >> 64);
+        uint64_t lo2 = __shfl_xor_sync(0xffffffffu, lo, o), hi2 = __shfl_xor_sync(0xffffffffu, hi, o);
+        r += ((u128)hi2 << 64) | lo2;
+        e += __shfl_xor_sync(0xffffffffu, e, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        shr[threadIdx.x >> 5] = r;
+        she[threadIdx.x >> 5] = e;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        u128 rt = 0;
+        unsigned long long et = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            rt += shr[w];
+            et += she[w];
+        }
+        rsum[(size_t)b * gridDim.x + blockIdx.x] = rt;
+        esum[(size_t)b * gridDim.x + blockIdx.x] = et;
+    }
+}
+
+// one CTA per sequence: pick the chunk holding the draw, then the element.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) sample_draw_kernel(
+    const uint16_t *__restrict__ P, const uint16_t *__restrict__ Q, int B, int gamma, int V,
+    int chunk, int n_chunks, uint64_t seed, uint64_t round, const uint32_t *__restrict__ maxenc,
+    const unsigned long long *__restrict__ sums, const u128 *__restrict__ rsum,
+    const unsigned long long *__restrict__ esum, const int32_t *__restrict__ accbuf,
+    int32_t *__restrict__ out) {
+    __shared__ u128 buf[kThreads];
+    __shared__ int s_chunk, s_mode;
+    __shared__ u128 s_base;
+    const int b = blockIdx.x;
+    const int A = accbuf[b];
+    const bool residual0 = A < gamma;
+    // chunk totals of the residual; fall back to the target row if all zero
+    u128 rv = (threadIdx.x < n_chunks && residual0) ? rsum[(size_t)b * n_chunks + threadIdx.x] : (u128)0;
+    u128 rinc = block_scan_u128(rv, buf);
+    u128 Wr = buf[kThreads - 1];
+    __syncthreads();
+    const bool residual = residual0 && Wr != 0;
+    u128 inc = rinc;
+    u128 W = Wr;
+    if (!residual) {
+        u128 ev = threadIdx.x < n_chunks ? (u128)esum[(size_t)b * n_chunks + threadIdx.x] : (u128)0;
+        inc = block_scan_u128(ev, buf);
+        W = buf[kThreads - 1];
+        __syncthreads();
+    }
+    const uint32_t U = uniform24(seed, round, (uint32_t)gamma, (uint32_t)b);
+    const u128 T = ((u128)U * W) >> 24;
+    // the first chunk whose inclusive prefix exceeds T
+    if (threadIdx.x == 0) s_chunk = n_chunks - 1;
+    __syncthreads();
+    {
+        u128 exc = inc - (threadIdx.x < n_chunks ? (residual ? rv
+                                                             : (u128)esum[(size_t)b * n_chunks + threadIdx.x])
+                                                 : (u128)0);
+        if (threadIdx.x < n_chunks && inc > T && exc <= T) {
+            s_chunk = threadIdx.x;
+            s_base = exc;
+        }
+    }
+    __syncthreads();
+    const int c = s_chunk;
+    const u128 base = c == 0 ? (u128)0 : s_base;
+    // walk chunk c: per-thread sums of 8 consecutive elements, scan, find
+    const int rp = b * (gamma + 1) + A;
+    const float mp = from_ordered_bits(maxenc[rp]);
+    const uint64_t Sp = sums[rp];
+    const int rq = B * (gamma + 1) + b * gamma + (residual ? A : 0);
+    const float mq = from_ordered_bits(maxenc[rq]);
+    const uint64_t Sq = sums[rq];
+    const uint16_t *prow = P + (size_t)rp * V;
+    const uint16_t *qrow = Q + ((size_t)b * gamma + (residual ? A : 0)) * V;
+    const int c0 = c * chunk, c1 = min(V, c0 + chunk);
+    u128 running = base;
+    if (threadIdx.x == 0) s_mode = -1;
+    for (int s0 = c0; s0 < c1; s0 += kSub) {
+        const int v0 = s0 + threadIdx.x * 8;
+        u128 w[8];
+        float fp[8], fq[8];
+        load8<VEC>(prow, v0, c1, fp);
+        if (residual) load8<VEC>(qrow, v0, c1, fq);
+        u128 tsum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint64_t Ep = fixed_weight(fp[i], mp);
+            if (residual) {
+                uint64_t Eq = fixed_weight(fq[i], mq);
+                u128 a = (u128)Ep * Sq, cc = (u128)Eq * Sp;
+                w[i] = a > cc ? a - cc : (u128)0;
+            } else {
+                w[i] = Ep;
+            }
+            tsum += w[i];
+        }
+        u128 tinc = block_scan_u128(tsum, buf);
+        u128 total = buf[kThreads - 1];
+        u128 texc = running + tinc - tsum;
+        if (running + tinc > T && texc <= T) {
+            u128 cum = texc;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cum += w[i];
+                if (cum > T) {
+                    s_mode = v0 + i;
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+        if (s_mode >= 0) break;
+        running += total;
+    }
+    if (threadIdx.x == 0) out[(size_t)b * (gamma + 1) + A] = s_mode >= 0 ? s_mode : c1 - 1;
+}
+
+}  // namespace
+
+}  // namespace qspec
+
+using namespace qspec;
+
+extern "C" size_t qspec_verify_workspace_bytes(int B, int gamma, int V) {
+    if (B < 1 || gamma < 1 || gamma > QSPEC_MAX_GAMMA || V < 1) return 0;
+    return make_layout(B, gamma, V).total;
+}
+
+static int verify_args(const void *p, const int32_t *draft, int B, int gamma, int V, const int32_t *n_acc,
+                       const int32_t *out, const void *ws, size_t ws_bytes) {
+    if (!p || !draft || !n_acc || !out || !ws) return QSPEC_ERR_NULL;
+    if (B < 1 || gamma < 1 || gamma > QSPEC_MAX_GAMMA || V < 1) return QSPEC_ERR_SHAPE;
+    if (!aligned(p, 2) || !aligned(draft, 4) || !aligned(n_acc, 4) || !aligned(out, 4) ||
+        !aligned(ws, 16))
+        return QSPEC_ERR_ALIGN;
+    if (ws_bytes < make_layout(B, gamma, V).total) return QSPEC_ERR_WORKSPACE;
+    return QSPEC_OK;
+}
+
+extern "C" int qspec_verify_greedy(const uint16_t *p_logits, const int32_t *draft, int B, int gamma,
+                                   int V, int32_t *n_acc, int32_t *out, void *workspace,
+                                   size_t ws_bytes, int32_t *dev_status, qspec_stream_t stream) {
+    int rc = verify_args(p_logits, draft, B, gamma, V, n_acc, out, workspace, ws_bytes);
+    if (rc) return rc;
+    rc = check_device();
+    if (rc) return rc;
+    cudaStream_t st = as_cuda(stream);
+    Layout L = make_layout(B, gamma, V);
+    char *ws = static_cast<char *>(workspace);
+    auto *keys = reinterpret_cast<unsigned long long *>(ws + L.off_key);
+    cudaError_t e = cudaMemsetAsync(keys, 0, (size_t)B * (gamma + 1) * 8, st);
+    if (e != cudaSuccess) {
+        set_last_error("qspec_verify_greedy memset", e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    dim3 grid((unsigned)L.n_chunks, (unsigned)(B * (gamma + 1)));
+    bool vec = (V % 8 == 0) && aligned(p_logits, 16);
+    if (vec)
+        greedy_argmax_kernel<true><<<grid, kThreads, 0, st>>>(p_logits, V, L.chunk, keys, dev_status);
+    else
+        greedy_argmax_kernel<false><<<grid, kThreads, 0, st>>>(p_logits, V, L.chunk, keys, dev_status);
+    greedy_finalize_kernel<<<(B + 127) / 128, 128, 0, st>>>(keys, draft, B, gamma, V, n_acc, out,
+                                                            dev_status);
+    return check_launch("qspec_verify_greedy");
+}
+
+template <bool VEC>
+static void launch_sample(const uint16_t *P, const uint16_t *Q, const int32_t *draft, int B, int gamma,
+                          int V, uint64_t seed, uint64_t round, int32_t *n_acc, int32_t *out,
+                          const Layout &L, char *ws, int32_t *dev_status, cudaStream_t st) {
+    auto *maxenc = reinterpret_cast<uint32_t *>(ws + L.off_max);
+    auto *sums = reinterpret_cast<unsigned long long *>(ws + L.off_sum);
+    auto *rsum = reinterpret_cast<u128 *>(ws + L.off_rsum);
+    auto *esum = reinterpret_cast<unsigned long long *>(ws + L.off_esum);
+    auto *accbuf = reinterpret_cast<int32_t *>(ws + L.off_acc);
+    const int rows = B * (2 * gamma + 1);
+    dim3 grid_rows((unsigned)L.n_chunks, (unsigned)rows);
+    sample_rowmax_kernel<VEC><<<grid_rows, kThreads, 0, st>>>(P, Q, B, gamma, V, L.chunk, maxenc,
+                                                              dev_status);
+    sample_rowsum_kernel<VEC><<<grid_rows, kThreads, 0, st>>>(P, Q, B, gamma, V, L.chunk, maxenc, sums,
+                                                              dev_status);
+    dim3 grid_seq((unsigned)L.n_chunks, (unsigned)B);
+    sample_residual_kernel<VEC><<<grid_seq, kThreads, 0, st>>>(P, Q, draft, B, gamma, V, L.chunk, seed,
+                                                               round, maxenc, sums, rsum, esum, accbuf,
+                                                               n_acc, out, dev_status);
+    sample_draw_kernel<VEC><<<B, kThreads, 0, st>>>(P, Q, B, gamma, V, L.chunk, L.n_chunks, seed, round,
+                                                    maxenc, sums, rsum, esum, accbuf, out);
+}
+
+extern "C" int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_logits,
+                                   const int32_t *draft, int B, int gamma, int V, uint64_t seed,
+                                   uint64_t round, int32_t *n_acc, int32_t *out, void *workspace,
+                                   size_t ws_bytes, int32_t *dev_status, qspec_stream_t stream) {
+    if (!q_logits) return QSPEC_ERR_NULL;
+    int rc = verify_args(p_logits, draft, B, gamma, V, n_acc, out, workspace, ws_bytes);
+    if (rc) return rc;
+    if (!aligned(q_logits, 2)) return QSPEC_ERR_ALIGN;
+    rc = check_device();
+    if (rc) return rc;
+    cudaStream_t st = as_cuda(stream);
+    Layout L = make_layout(B, gamma, V);
+    char *ws = static_cast<char *>(workspace);
+    // row maxima start at 0 (below every encoded value), row sums at 0
+    cudaError_t e = cudaMemsetAsync(ws + L.off_max, 0, L.off_rsum - L.off_max, st);
+    if (e != cudaSuccess) {
+        set_last_error("qspec_verify_sample memset", e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    bool vec = (V % 8 == 0) && aligned(p_logits, 16) && aligned(q_logits, 16);
+    if (vec)
+        launch_sample<true>(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, L, ws,
+                            dev_status, st);
+    else
+        launch_sample<false>(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, L, ws,
+                             dev_status, st);
+    return check_launch("qspec_verify_sample");
+}

@@ -1,0 +1,117 @@
+"""a3 W4A4 (bit-exact: outputs and INT32 group accumulators) and a4 W4A16
+(within 1e-2 (1 + |ref|) of fp64): CUDA path vs oracle on the same inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_speculative_decoding_shared_gb300 import binding as q, synthetic as syn
+from gpuhelp import assert_w4a16_close, bits, need_gpu, read_status, sample_points, status
+
+pytestmark = pytest.mark.gpu
+
+
+def make_layer(N, K, seed, dev):
+    codes, s, z = syn.weights(N, K, seed, device=dev)
+    packed, sz = q.pack_weights(codes, s, z)
+    rc, po, szo = oracle.pack_weights(codes.cpu().numpy(), bits(s), bits(z))
+    assert rc == 0
+    assert np.array_equal(packed.cpu().numpy(), po)
+    return packed, sz, po, szo
+
+
+def run_w4a4(x, packed, sz, dev, want_I=True):
+    st = status(dev)
+    xq, sx, qs = q.quant_act_int4(x.to(dev), dev_status=st)
+    out = q.linear_w4a4(xq, sx, qs, packed, sz, want_I=want_I, dev_status=st)
+    assert read_status(st) == 0
+    rc, xqo, sxo, qso = oracle.quant_act_int4(bits(x))
+    assert np.array_equal(xq.cpu().numpy(), xqo)
+    return out, xqo, sxo
+
+
+# ----------------------------------------------------------------- small, full compare
+@pytest.mark.parametrize("M,N,K,seed", [
+    (4, 512, 512, 0),                     # the single-layer case: K = N = 512, M = gamma + 1 = 4
+    (1, 16, 128, 1), (2, 100, 384, 2), (3, 1000, 1024, 3), (5, 48, 3072, 4),
+    (8, 33, 256, 5), (9, 64, 512, 6), (13, 17, 128, 7), (16, 256, 640, 8), (17, 40, 384, 9),
+    (33, 31, 1152, 10)])
+def test_small_full_compare(M, N, K, seed):
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100)
+    (y4, I), xqo, sxo = run_w4a4(x, packed, sz, dev)
+    y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert np.array_equal(I.cpu().numpy(), Io)
+    assert np.array_equal(bits(y4), y4o)
+    y16 = q.linear_w4a16(x.to(dev), packed, sz)
+    ref = oracle.linear_w4a16(bits(x), po, szo)
+    assert_w4a16_close(y16, ref, "w4a16 M=%d N=%d K=%d" % (M, N, K))
+
+
+def test_extreme_codes_and_unit_scales():
+    """codes and activations at the ends of their ranges: |I| reaches 128*7*15."""
+    dev = need_gpu()
+    M, N, K = 3, 64, 512
+    G = K // 128
+    rng = np.random.default_rng(0)
+    codes = torch.from_numpy(rng.choice([0, 15], (N, K)).astype(np.uint8))
+    z = torch.from_numpy(rng.choice([0.0, 15.0], (N, G))).to(torch.float16)
+    s = torch.ones((N, G), dtype=torch.float16)
+    packed, sz = q.pack_weights(codes.to(dev), s.to(dev), z.to(dev))
+    rc, po, szo = oracle.pack_weights(codes.numpy(), bits(s), bits(z))
+    x = torch.from_numpy(rng.choice([-7.0, 7.0], (M, K)).astype(np.float32)).to(torch.bfloat16)
+    (y4, I), xqo, sxo = run_w4a4(x, packed, sz, dev)
+    y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert np.abs(Io).max() == 128 * 7 * 15
+    assert np.array_equal(I.cpu().numpy(), Io) and np.array_equal(bits(y4), y4o)
+    y16 = q.linear_w4a16(x.to(dev), packed, sz)
+    assert_w4a16_close(y16, oracle.linear_w4a16(bits(x), po, szo), "extreme")
+
+
+# ----------------------------------------------------------------- full-size layer shapes
+LLAMA = syn.layer_linears(syn.LLAMA3_8B)
+QWEN = syn.layer_linears(syn.QWEN25_7B)
+
+
+def sampled_compare(M_list, shapes, seed, dev, outliers=0.0, w4a4=True, w4a16=True, points=384):
+    for idx, (name, N, K) in enumerate(shapes):
+        packed, sz, po, szo = make_layer(N, K, seed * 10 + idx, dev)
+        for M in M_list:
+            x = syn.activations(M, K, seed * 100 + idx, outlier_frac=outliers)
+            ms, ns = sample_points(M, N, points, seed + idx + M)
+            if w4a4:
+                y4, xqo, sxo = run_w4a4(x, packed, sz, dev, want_I=False)
+                y4o = oracle.linear_w4a4_points(xqo, sxo, po, szo, ms, ns)
+                assert np.array_equal(bits(y4)[ms, ns], y4o), (name, M)
+            if w4a16:
+                y16 = q.linear_w4a16(x.to(dev), packed, sz)
+                ref = oracle.linear_w4a16_points(bits(x), po, szo, ms, ns)
+                assert_w4a16_close(y16.float().cpu().numpy()[ms, ns], ref, "%s M=%d" % (name, M))
+
+
+def test_llama_decode_draft_m1_verify_m5():
+    """Llama-3-8B-shaped decode linears, 1 % outlier channels x20: W4A4 draft
+    at M = 1, W4A16 verify at M = gamma + 1 = 5."""
+    dev = need_gpu()
+    sampled_compare([1], LLAMA, 1, dev, outliers=0.01, w4a16=False)
+    sampled_compare([5], LLAMA, 1, dev, outliers=0.01, w4a4=False)
+
+
+def test_llama_batch16_verify_m80_with_lm_head():
+    dev = need_gpu()
+    sampled_compare([80], LLAMA + [("lm_head", 128256, 4096)], 2, dev, w4a4=False)
+
+
+@pytest.mark.parametrize("gamma", [2, 4, 8])
+def test_qwen_batch32(gamma):
+    dev = need_gpu()
+    shapes = QWEN if gamma == 4 else [QWEN[0], QWEN[6]]
+    sampled_compare([32], shapes, 3, dev, w4a16=False)
+    sampled_compare([32 * (gamma + 1)], shapes, 3, dev, w4a4=False)
+
+
+def test_prefill_m4096():
+    dev = need_gpu()
+    shapes = [("gate_proj", 14336, 4096), ("down_proj", 4096, 14336)]
+    sampled_compare([4096], shapes, 4, dev)
