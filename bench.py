@@ -67,7 +67,51 @@ def parse_args():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3-8b-decode-b1-g4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rounds", type=int, default=16, help="distinct captured rounds (RNG round ids)")
+    ap.add_argument("--profile-case", choices=["w4a4_m1", "w4a16_m5", "quant", "verify_sample",
+                                               "verify_greedy", "kv"],
+                    help="run one kernel a few times on a single LM-head-sized case (for ncu)")
+    ap.add_argument("--profile-reps", type=int, default=3)
     return ap.parse_args()
+
+
+def profile_case(name, reps):
+    """One kernel on one case larger than L2 (the 128256 x 4096 LM head: 263 MB
+    of packed weights), launched `reps` times; prints nothing measured."""
+    from quantized_speculative_decoding_shared_gb300 import binding as q
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, K = 128256, 4096
+    if name in ("w4a4_m1", "w4a16_m5", "quant"):
+        codes, s, z = syn.weights(N, K, 5, device=dev)
+        packed, sz = q.pack_weights(codes, s, z)
+        del codes
+        M = 1 if name != "w4a16_m5" else 5
+        x = syn.activations(M, K, 6, device=dev, outlier_frac=0.01)
+        xq, sx, qs = q.quant_act_int4(x)
+        for _ in range(reps):
+            if name == "w4a4_m1":
+                q.linear_w4a4(xq, sx, qs, packed, sz)
+            elif name == "w4a16_m5":
+                q.linear_w4a16(x, packed, sz)
+            else:
+                q.quant_act_int4(syn.activations(4096, 14336, 7, device=dev))
+    elif name in ("verify_sample", "verify_greedy"):
+        P, Q, d = syn.logits_noisy_draft(256, 4, 128256, 4, device=dev)
+        ws = q.verify_workspace(256, 4, 128256, dev)
+        for r in range(reps):
+            if name == "verify_sample":
+                q.verify_sample(P, Q, d, 1, r, workspace=ws)
+            else:
+                q.verify_greedy(P, d, workspace=ws)
+    else:
+        kc, vc = syn.kv_cache(32, 16, 8, 4096, 128, 2, device=dev)
+        kn, vn = syn.kv_new(32, 16, 4, 8, 128, 3, device=dev)
+        base = syn.base_positions(16, 4096, 4, 2, device=dev)
+        nacc = torch.full((16,), 4, dtype=torch.int32, device=dev)
+        for _ in range(reps):
+            q.kv_overwrite(kc, vc, kn, vn, base, nacc)
+    torch.cuda.synchronize()
+    print("profile case %s: %d launches done" % (name, reps))
 
 
 # ---------------------------------------------------------------------------
@@ -307,6 +351,19 @@ class GpuRound:
         return t + [self.xd_lm, self.xv_lm, self.P, self.Q, self.drafts, self.base]
 
 
+def aggregate_over_ranks(seconds, tokens, device):
+    """Whole-job figures over the ranks of a weak-scaling run: the slowest
+    rank's time and the tokens of all ranks.  One rank: unchanged."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(seconds), int(tokens)
+    t = torch.tensor([float(seconds), float(tokens)], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(mx[0]), int(round(float(t[1])))
+
+
 def capture(fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -414,6 +471,9 @@ def cpu_baseline(wl, steps=3):
 # ---------------------------------------------------------------------------
 def main():
     args = parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case, args.profile_reps)
+        return
     wl = WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -501,14 +561,9 @@ def main():
     tokens = int(sum((acc[i % R] + 1).sum() for i in range(args.steps)))
     if int(rnd_obj.status.item()) != 0:
         raise RuntimeError("device status %d" % int(rnd_obj.status.item()))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, float(tokens)], dtype=torch.float64, device=dev)
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        ms, tokens = float(mx[0]), int(t[1])
-    value = tokens / (ms / 1e3)
+    sec, tokens = aggregate_over_ranks(ms / 1e3, tokens, dev)
+    ms = sec * 1e3
+    value = tokens / sec
 
     # dominant kernel: one draft step's W4A4 linears, graph-replayed alone
     g4 = capture(rnd_obj.draft_linears_only, stream)
@@ -548,14 +603,7 @@ def main():
             stream.synchronize()
             e2e_tokens += int((nacc_host + 1).sum())
     t_e2e = time.perf_counter() - t0
-    e2e_ms = [t_e2e * 1e3]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([t_e2e, float(e2e_tokens)], dtype=torch.float64, device=dev)
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        t_e2e, e2e_tokens = float(mx[0]), int(t[1])
+    t_e2e, e2e_tokens = aggregate_over_ranks(t_e2e, e2e_tokens, dev)
 
     if rank != 0:
         return

@@ -93,7 +93,7 @@ int qspec_pack_weights(const uint8_t *codes, const uint16_t *s_fp16, const uint1
  * Per row m and group g: amax = max |x|, sx = amax / 7 (fp32, IEEE
  * division), q = clamp(rint(x / sx), -7, 7) (q = 0 when sx == 0), qs = sum q.
  *
- *   x_bf16 uint16 [M][ldx]  input rows (ldx >= K, ldx % 4 == 0, 8-byte aligned)
+ *   x_bf16 uint16 [M][ldx]  input rows (ldx >= K, ldx % 8 == 0, 16-byte aligned)
  *   xq     uint8  [M][K/2]  out: two's-complement nibbles, byte j = q[2j] | q[2j+1] << 4
  *   sx     float  [M][G]    out: scales
  *   qs     int32  [M][G]    out: group sums of q

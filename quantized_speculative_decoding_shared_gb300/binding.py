@@ -73,7 +73,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "qspec_verify_sample": ([vp, vp, vp, i32, i32, i32, u64, u64, vp, vp, vp, sz_t, vp, vp],
                                     i32),
             "qspec_kv_overwrite": ([vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp],
-                                   i32),
+                                   i32)
         }
         for name, (args, res) in proto.items():
             f = getattr(lib, name)

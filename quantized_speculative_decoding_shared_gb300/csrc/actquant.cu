@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
                                                        int ldx, uint8_t *__restrict__ xq,
                                                        float *__restrict__ sx,
                                                        int32_t *__restrict__ qs, int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int G = K / kGroup;
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4, hl = lane & 15;
@@ -87,6 +89,6 @@ extern "C" int qspec_quant_act_int4(const uint16_t *x_bf16, int M, int K, int ld
     long long warps = (long long)M * ((K / kGroup + 1) / 2);
     long long blocks = (warps * 32 + 255) / 256;
     unsigned grid = (unsigned)std::min<long long>(blocks, (long long)sm_count() * 16);
-    quant_act_kernel<<<grid, 256, 0, as_cuda(stream)>>>(x_bf16, M, K, ldx, xq, sx, qs, dev_status);
-    return check_launch("qspec_quant_act_int4");
+    return launch_pdl("qspec_quant_act_int4", quant_act_kernel, dim3(grid), dim3(256), 0, as_cuda(stream),
+                      x_bf16, M, K, ldx, xq, sx, qs, dev_status);
 }

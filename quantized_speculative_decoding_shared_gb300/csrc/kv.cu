@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(256) kv_overwrite_kernel(uint4 *__restrict__ k
                                                           const int32_t *__restrict__ base_pos,
                                                           const int32_t *__restrict__ n_acc, int L, int B,
                                                           int H, int T, int D, int gamma, int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int D8 = D / 8;
     const long long total = (long long)L * B * (gamma + 1) * H * D8;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -63,9 +65,8 @@ extern "C" int qspec_kv_overwrite(uint16_t *k_cache, uint16_t *v_cache, const ui
     if (rc) return rc;
     long long total = (long long)L * B * (gamma + 1) * H * (D / 8);
     unsigned grid = (unsigned)std::min<long long>((total + 255) / 256, (long long)sm_count() * 16);
-    kv_overwrite_kernel<<<grid, 256, 0, as_cuda(stream)>>>(
-        reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
-        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), base_pos, n_acc, L,
-        B, H, T, D, gamma, dev_status);
-    return check_launch("qspec_kv_overwrite");
+    return launch_pdl("qspec_kv_overwrite", kv_overwrite_kernel, dim3(grid), dim3(256), 0, as_cuda(stream),
+                      reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
+                      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), base_pos,
+                      n_acc, L, B, H, T, D, gamma, dev_status);
 }

@@ -15,6 +15,18 @@ namespace qspec {
 
 constexpr int kGroup = QSPEC_GROUP;
 
+// Programmatic dependent launch (PDL).  A kernel launched with
+// launch_pdl() may start while the previous kernel in the stream is still
+// running.  Rule kept by every kernel of this library: before pdl_wait() it
+// only reads immutable data (packed weights, scale/zero words); every read
+// of another kernel's output and every write comes after pdl_wait(), which
+// returns once the previous grid has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets the next PDL-launched kernel be scheduled as this grid's CTAs retire.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // First data error wins: later codes never overwrite an earlier one.
 __device__ __forceinline__ void flag(int32_t *st, int code) {
     if (st != nullptr && code != QSPEC_OK) atomicCAS(st, 0, code);

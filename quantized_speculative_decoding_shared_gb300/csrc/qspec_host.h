@@ -31,4 +31,36 @@ int sm_count();
 // capture: the first call on a device talks to the driver.
 int smem_limit_once(const void *func, int slot, int bytes);
 
+// Large-M W4A16 on the tensor cores (w4a16_tc.cu).
+int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
+                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream);
+
+// Larger-M W4A4 on the tensor cores (w4a4_tc.cu).
+int launch_w4a4_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
+                   const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st,
+                   cudaStream_t stream);
+
+// Launch `kernel` on `st` with programmatic stream serialisation allowed (the
+// kernel must follow the pdl_wait() rule in qspec_device.cuh).
+template <typename... KArgs, typename... Args>
+int launch_pdl(const char *where, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+               cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) {
+        set_last_error(where, e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    return QSPEC_OK;
+}
+
 }  // namespace qspec

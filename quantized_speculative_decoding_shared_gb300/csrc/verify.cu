@@ -141,10 +141,12 @@ __global__ void __launch_bounds__(kThreads) greedy_argmax_kernel(const uint16_t 
                                                                 int chunk,
                                                                 unsigned long long *__restrict__ keys,
                                                                 int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ unsigned long long sh[kThreads / 32];
-    const int row = blockIdx.y;
+    const int row = blockIdx.x;
     const uint16_t *rp = P + (size_t)row * V;
-    const int c0 = blockIdx.x * chunk, c1 = min(V, c0 + chunk);
+    const int c0 = blockIdx.y * chunk, c1 = min(V, c0 + chunk);
     unsigned long long best = 0;
     bool bad = false;
     for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
@@ -168,6 +170,8 @@ __global__ void greedy_finalize_kernel(const unsigned long long *__restrict__ ke
                                        const int32_t *__restrict__ draft, int B, int gamma, int V,
                                        int32_t *__restrict__ n_acc, int32_t *__restrict__ out,
                                        int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
     int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     const unsigned long long *k = keys + (size_t)b * (gamma + 1);
@@ -202,10 +206,12 @@ __global__ void __launch_bounds__(kThreads) sample_rowmax_kernel(const uint16_t 
                                                                 int gamma, int V, int chunk,
                                                                 uint32_t *__restrict__ maxenc,
                                                                 int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ uint32_t sh[kThreads / 32];
-    const int row = blockIdx.y;
+    const int row = blockIdx.x;
     const uint16_t *rp = row_ptr(P, Q, B, gamma, V, row);
-    const int c0 = blockIdx.x * chunk, c1 = min(V, c0 + chunk);
+    const int c0 = blockIdx.y * chunk, c1 = min(V, c0 + chunk);
     float m = -INFINITY;
     bool bad = false;
     for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
@@ -229,15 +235,17 @@ __global__ void __launch_bounds__(kThreads) sample_rowsum_kernel(const uint16_t 
                                                                 const uint32_t *__restrict__ maxenc,
                                                                 unsigned long long *__restrict__ sums,
                                                                 int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ unsigned long long sh[kThreads / 32];
-    const int row = blockIdx.y;
+    const int row = blockIdx.x;
     const uint16_t *rp = row_ptr(P, Q, B, gamma, V, row);
     const float m = from_ordered_bits(maxenc[row]);
     if (m == -INFINITY) {                      // a row without any mass
-        if (blockIdx.x == 0 && threadIdx.x == 0) flag(st, QSPEC_ERR_NONFINITE);
+        if (blockIdx.y == 0 && threadIdx.x == 0) flag(st, QSPEC_ERR_NONFINITE);
         return;
     }
-    const int c0 = blockIdx.x * chunk, c1 = min(V, c0 + chunk);
+    const int c0 = blockIdx.y * chunk, c1 = min(V, c0 + chunk);
     unsigned long long s = 0;
     for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
         float f[8];
@@ -281,7 +289,7 @@ __device__ int decide(const uint16_t *P, const uint16_t *Q, const int32_t *draft
     return -1;
 }
 
-// grid (chunk, b): decisions (recomputed by every chunk's CTA), then this
+// grid (b, chunk): decisions (recomputed by every chunk's CTA), then this
 // chunk's sums of the residual R_v and of the target row's E_v.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) sample_residual_kernel(
@@ -290,15 +298,18 @@ __global__ void __launch_bounds__(kThreads) sample_residual_kernel(
     const uint32_t *__restrict__ maxenc, const unsigned long long *__restrict__ sums,
     u128 *__restrict__ rsum, unsigned long long *__restrict__ esum, int32_t *__restrict__ accbuf,
     int32_t *__restrict__ n_acc, int32_t *__restrict__ out, int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int sA;
     __shared__ u128 shr[kThreads / 32];
     __shared__ unsigned long long she[kThreads / 32];
-    const int b = blockIdx.y;
+    const int b = blockIdx.x;
+    const int n_chunks = gridDim.y;
     bool range_bad = false;
     int A = decide(P, Q, draft, B, gamma, V, b, seed, round, maxenc, sums, &range_bad);
     if (threadIdx.x == 0) {
         sA = A;
-        if (blockIdx.x == 0) {
+        if (blockIdx.y == 0) {
             if (range_bad) flag(st, QSPEC_ERR_RANGE);
             accbuf[b] = A;
             n_acc[b] = A;
@@ -317,7 +328,7 @@ __global__ void __launch_bounds__(kThreads) sample_residual_kernel(
     const uint64_t Sq = sums[rq];
     const uint16_t *prow = P + (size_t)rp * V;
     const uint16_t *qrow = Q + ((size_t)b * gamma + (residual ? A : 0)) * V;
-    const int c0 = blockIdx.x * chunk, c1 = min(V, c0 + chunk);
+    const int c0 = blockIdx.y * chunk, c1 = min(V, c0 + chunk);
     u128 r = 0;
     unsigned long long e = 0;
     for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
@@ -355,8 +366,8 @@ __global__ void __launch_bounds__(kThreads) sample_residual_kernel(
             rt += shr[w];
             et += she[w];
         }
-        rsum[(size_t)b * gridDim.x + blockIdx.x] = rt;
-        esum[(size_t)b * gridDim.x + blockIdx.x] = et;
+        rsum[(size_t)b * n_chunks + blockIdx.y] = rt;
+        esum[(size_t)b * n_chunks + blockIdx.y] = et;
     }
 }
 
@@ -368,6 +379,8 @@ __global__ void __launch_bounds__(kThreads) sample_draw_kernel(
     const unsigned long long *__restrict__ sums, const u128 *__restrict__ rsum,
     const unsigned long long *__restrict__ esum, const int32_t *__restrict__ accbuf,
     int32_t *__restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ u128 buf[kThreads];
     __shared__ int s_chunk, s_mode;
     __shared__ u128 s_base;
@@ -495,19 +508,19 @@ extern "C" int qspec_verify_greedy(const uint16_t *p_logits, const int32_t *draf
         set_last_error("qspec_verify_greedy memset", e);
         return QSPEC_ERR_LAUNCH;
     }
-    dim3 grid((unsigned)L.n_chunks, (unsigned)(B * (gamma + 1)));
+    dim3 grid((unsigned)(B * (gamma + 1)), (unsigned)L.n_chunks);
     bool vec = (V % 8 == 0) && aligned(p_logits, 16);
-    if (vec)
-        greedy_argmax_kernel<true><<<grid, kThreads, 0, st>>>(p_logits, V, L.chunk, keys, dev_status);
-    else
-        greedy_argmax_kernel<false><<<grid, kThreads, 0, st>>>(p_logits, V, L.chunk, keys, dev_status);
-    greedy_finalize_kernel<<<(B + 127) / 128, 128, 0, st>>>(keys, draft, B, gamma, V, n_acc, out,
-                                                            dev_status);
-    return check_launch("qspec_verify_greedy");
+    rc = vec ? launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<true>, grid, dim3(kThreads), 0, st,
+                          p_logits, V, L.chunk, keys, dev_status)
+             : launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<false>, grid, dim3(kThreads), 0, st,
+                          p_logits, V, L.chunk, keys, dev_status);
+    if (rc) return rc;
+    return launch_pdl("qspec_verify_greedy", greedy_finalize_kernel, dim3((B + 127) / 128), dim3(128), 0, st,
+                      keys, draft, B, gamma, V, n_acc, out, dev_status);
 }
 
 template <bool VEC>
-static void launch_sample(const uint16_t *P, const uint16_t *Q, const int32_t *draft, int B, int gamma,
+static int launch_sample(const uint16_t *P, const uint16_t *Q, const int32_t *draft, int B, int gamma,
                           int V, uint64_t seed, uint64_t round, int32_t *n_acc, int32_t *out,
                           const Layout &L, char *ws, int32_t *dev_status, cudaStream_t st) {
     auto *maxenc = reinterpret_cast<uint32_t *>(ws + L.off_max);
@@ -516,17 +529,20 @@ static void launch_sample(const uint16_t *P, const uint16_t *Q, const int32_t *d
     auto *esum = reinterpret_cast<unsigned long long *>(ws + L.off_esum);
     auto *accbuf = reinterpret_cast<int32_t *>(ws + L.off_acc);
     const int rows = B * (2 * gamma + 1);
-    dim3 grid_rows((unsigned)L.n_chunks, (unsigned)rows);
-    sample_rowmax_kernel<VEC><<<grid_rows, kThreads, 0, st>>>(P, Q, B, gamma, V, L.chunk, maxenc,
-                                                              dev_status);
-    sample_rowsum_kernel<VEC><<<grid_rows, kThreads, 0, st>>>(P, Q, B, gamma, V, L.chunk, maxenc, sums,
-                                                              dev_status);
-    dim3 grid_seq((unsigned)L.n_chunks, (unsigned)B);
-    sample_residual_kernel<VEC><<<grid_seq, kThreads, 0, st>>>(P, Q, draft, B, gamma, V, L.chunk, seed,
-                                                               round, maxenc, sums, rsum, esum, accbuf,
-                                                               n_acc, out, dev_status);
-    sample_draw_kernel<VEC><<<B, kThreads, 0, st>>>(P, Q, B, gamma, V, L.chunk, L.n_chunks, seed, round,
-                                                    maxenc, sums, rsum, esum, accbuf, out);
+    dim3 grid_rows((unsigned)rows, (unsigned)L.n_chunks);
+    const char *w = "qspec_verify_sample";
+    int rc = launch_pdl(w, sample_rowmax_kernel<VEC>, grid_rows, dim3(kThreads), 0, st, P, Q, B, gamma, V,
+                        L.chunk, maxenc, dev_status);
+    if (rc) return rc;
+    rc = launch_pdl(w, sample_rowsum_kernel<VEC>, grid_rows, dim3(kThreads), 0, st, P, Q, B, gamma, V, L.chunk,
+                    maxenc, sums, dev_status);
+    if (rc) return rc;
+    dim3 grid_seq((unsigned)B, (unsigned)L.n_chunks);
+    rc = launch_pdl(w, sample_residual_kernel<VEC>, grid_seq, dim3(kThreads), 0, st, P, Q, draft, B, gamma, V,
+                    L.chunk, seed, round, maxenc, sums, rsum, esum, accbuf, n_acc, out, dev_status);
+    if (rc) return rc;
+    return launch_pdl(w, sample_draw_kernel<VEC>, dim3(B), dim3(kThreads), 0, st, P, Q, B, gamma, V, L.chunk,
+                      L.n_chunks, seed, round, maxenc, sums, rsum, esum, accbuf, out);
 }
 
 extern "C" int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_logits,
@@ -549,11 +565,9 @@ extern "C" int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_l
         return QSPEC_ERR_LAUNCH;
     }
     bool vec = (V % 8 == 0) && aligned(p_logits, 16) && aligned(q_logits, 16);
-    if (vec)
-        launch_sample<true>(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, L, ws,
-                            dev_status, st);
-    else
-        launch_sample<false>(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, L, ws,
-                             dev_status, st);
-    return check_launch("qspec_verify_sample");
+    return vec ? launch_sample<true>(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, L, ws,
+                                     dev_status, st)
+               : launch_sample<false>(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, L, ws,
+                                      dev_status, st);
 }
+

@@ -34,7 +34,6 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kPrefetch = 4;
 
 __device__ __forceinline__ void mma_bf16_16816(float &d0, float &d1, float &d2, float &d3,
                                                uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -86,24 +85,53 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qr = lane >> 2, qc = lane & 3;
     const int tok0 = blockIdx.y * 8 * NT;
+    const int n_tiles = (N + 15) / 16;
+    const size_t row_bytes = (size_t)K / 2;
+    constexpr int kPrefetch = NT == 1 ? 4 : 2;   // groups in flight per warp
 
-    // group sums X_g of this CTA's tokens: one warp per (token, group)
-    for (int i = warp; i < NT * 8 * G; i += kWarps) {
-        int t = i / G, g = i % G, m = tok0 + t;
+    pdl_launch_dependents();
+    // prefetch ring over this warp's groups g = warp, warp + 8, ... of the
+    // first tile: weights are immutable, so this overlaps the previous kernel
+    uint4 ring0[kPrefetch], ring1[kPrefetch];
+    {
+        const int tile = blockIdx.x;
+        const int r0 = tile * 16 + qr, r1 = r0 + 8;
+        const uint4 *w0p = reinterpret_cast<const uint4 *>(packed + (size_t)(r0 < N ? r0 : 0) * row_bytes) + qc;
+        const uint4 *w1p = reinterpret_cast<const uint4 *>(packed + (size_t)(r1 < N ? r1 : 0) * row_bytes) + qc;
+#pragma unroll
+        for (int j = 0; j < kPrefetch; ++j) {
+            int g = warp + j * kWarps;
+            if (tile < n_tiles && g < G) {
+                ring0[j] = ldg_stream(w0p + g * 4);
+                ring1[j] = ldg_stream(w1p + g * 4);
+            }
+        }
+    }
+    pdl_wait();
+
+    // group sums X_g of this CTA's tokens, one (token, group) per thread at a time
+    for (int i = threadIdx.x; i < NT * 8 * G; i += kThreads) {
+        const int t = i / G, g = i % G, m = tok0 + t;
         float s = 0.0f;
         if (m < M) {
-            uint2 v = *reinterpret_cast<const uint2 *>(x + (size_t)m * ldx + (size_t)g * kGroup + lane * 4);
-            s = (__uint_as_float(v.x << 16) + __uint_as_float(v.x & 0xFFFF0000u)) +
-                (__uint_as_float(v.y << 16) + __uint_as_float(v.y & 0xFFFF0000u));
-        }
+            const uint4 *xp = reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup);
+            uint4 v[16];
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) xg[t * G + g] = s;
+            for (int u = 0; u < 16; ++u) v[u] = __ldg(xp + u);
+            float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                part[0] += __uint_as_float(v[u].x << 16) + __uint_as_float(v[u].x & 0xFFFF0000u);
+                part[1] += __uint_as_float(v[u].y << 16) + __uint_as_float(v[u].y & 0xFFFF0000u);
+                part[2] += __uint_as_float(v[u].z << 16) + __uint_as_float(v[u].z & 0xFFFF0000u);
+                part[3] += __uint_as_float(v[u].w << 16) + __uint_as_float(v[u].w & 0xFFFF0000u);
+            }
+            s = (part[0] + part[1]) + (part[2] + part[3]);
+        }
+        xg[t * G + g] = s;
     }
     __syncthreads();
 
-    const int n_tiles = (N + 15) / 16;
-    const size_t row_bytes = (size_t)K / 2;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
         const int r0 = tile * 16 + qr, r1 = r0 + 8;
         const bool v0 = r0 < N, v1 = r1 < N;
@@ -116,15 +144,26 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
 
-        // prefetch ring over this warp's groups g = warp, warp + 8, ...
-        uint4 ring0[kPrefetch], ring1[kPrefetch];
+        if (tile != (int)blockIdx.x) {
 #pragma unroll
-        for (int j = 0; j < kPrefetch; ++j) {
-            int g = warp + j * kWarps;
-            if (g < G) {
-                ring0[j] = ldg_stream(w0p + g * 4);
-                ring1[j] = ldg_stream(w1p + g * 4);
+            for (int j = 0; j < kPrefetch; ++j) {
+                int g = warp + j * kWarps;
+                if (g < G) {
+                    ring0[j] = ldg_stream(w0p + g * 4);
+                    ring1[j] = ldg_stream(w1p + g * 4);
+                }
             }
+        }
+        // activation fragments of the warp's first group
+        uint4 xv[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int m = tok0 + nt * 8 + qr;
+            const uint4 *xp = reinterpret_cast<const uint4 *>(
+                x + (size_t)(m < M ? m : 0) * ldx + (size_t)warp * kGroup + qc * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                xv[nt][u] = (m < M && warp < G) ? __ldg(xp + u) : make_uint4(0, 0, 0, 0);
         }
         for (int gb = warp; gb < G; gb += kPrefetch * kWarps) {
 #pragma unroll
@@ -139,6 +178,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                         ring1[slot] = ldg_stream(w1p + gn * 4);
                     }
                 }
+                // next group's activation fragments
+                uint4 xn[NT][4];
+                const int gx = g + kWarps;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int m = tok0 + nt * 8 + qr;
+                    const uint4 *xp = reinterpret_cast<const uint4 *>(
+                        x + (size_t)(m < M ? m : 0) * ldx + (size_t)(gx < G ? gx : 0) * kGroup + qc * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        xn[nt][u] = (m < M && gx < G) ? __ldg(xp + u) : make_uint4(0, 0, 0, 0);
+                }
                 const uint32_t wr0[4] = {wa.x, wa.y, wa.z, wa.w};
                 const uint32_t wr1[4] = {wb.x, wb.y, wb.z, wb.w};
 
@@ -152,19 +203,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const int m = tok0 + nt * 8 + qr;
-                    uint4 xv[4];
-                    const uint4 *xp = reinterpret_cast<const uint4 *>(
-                        x + (size_t)(m < M ? m : 0) * ldx + (size_t)g * kGroup + qc * 32);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) xv[u] = m < M ? __ldg(xp + u) : make_uint4(0, 0, 0, 0);
                     float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         uint32_t pa0[4], pa1[4], pb[4];
                         codes_to_bf16x2(wr0[u], pa0);
                         codes_to_bf16x2(wr1[u], pa1);
-                        acts_to_pairs(xv[u], pb);
+                        acts_to_pairs(xv[nt][u], pb);
                         mma_bf16_16816(d[0], d[1], d[2], d[3], pa0[0], pa1[0], pa0[1], pa1[1], pb[0], pb[1]);
                         mma_bf16_16816(d[0], d[1], d[2], d[3], pa0[2], pa1[2], pa0[3], pa1[3], pb[2], pb[3]);
                     }
@@ -176,6 +221,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                     acc[nt][2] = __fmaf_rn(s1, __fmaf_rn(-o1, X0, d[2]), acc[nt][2]);
                     acc[nt][3] = __fmaf_rn(s1, __fmaf_rn(-o1, X1, d[3]), acc[nt][3]);
                 }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) xv[nt][u] = xn[nt][u];
             }
         }
 
@@ -191,11 +240,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
         for (int i = threadIdx.x; i < NT * 8 * 16; i += kThreads) {
             int t = i / 16, r = i % 16;
-            float s = 0.0f;
+            float sum = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) s += red[(size_t)w * NT * 8 * 16 + i];
+            for (int w = 0; w < kWarps; ++w) sum += red[(size_t)w * NT * 8 * 16 + i];
             int m = tok0 + t, n = tile * 16 + r;
-            if (m < M && n < N) y[(size_t)m * ldy + n] = float_to_bf16_bits(s);
+            if (m < M && n < N) y[(size_t)m * ldy + n] = float_to_bf16_bits(sum);
         }
         __syncthreads();
     }
@@ -211,8 +260,8 @@ int launch_w4a16(const uint16_t *x, int ldx, const uint8_t *packed, const uint32
     const int token_tiles = (M + 8 * NT - 1) / (8 * NT);
     int per_col = std::max(1, 2 * sm_count() / token_tiles);
     dim3 grid((unsigned)std::min(n_tiles, per_col), (unsigned)token_tiles);
-    w4a16_mma_kernel<NT><<<grid, kThreads, smem, st>>>(x, ldx, packed, sz, M, N, K, y, ldy);
-    return check_launch("qspec_linear_w4a16");
+    return launch_pdl("qspec_linear_w4a16", w4a16_mma_kernel<NT>, grid, dim3(kThreads), smem, st, x, ldx,
+                      packed, sz, M, N, K, y, ldy);
 }
 
 }  // namespace
@@ -224,7 +273,6 @@ using namespace qspec;
 extern "C" int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t *packed,
                                   const uint32_t *sz, int M, int N, int K, uint16_t *y_bf16,
                                   int ldy, int32_t *dev_status, qspec_stream_t stream) {
-    (void)dev_status;
     if (!x_bf16 || !packed || !sz || !y_bf16) return QSPEC_ERR_NULL;
     if (M < 1 || N < 1 || K < kGroup || K % kGroup || ldx < K || ldy < N) return QSPEC_ERR_SHAPE;
     if (!aligned(x_bf16, 16) || ldx % 8 || !aligned(packed, 16) || !aligned(sz, 4) ||
@@ -234,5 +282,6 @@ extern "C" int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t
     if (rc) return rc;
     cudaStream_t st = as_cuda(stream);
     if (M <= 8) return launch_w4a16<1>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
-    return launch_w4a16<2>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
+    if (M <= 16) return launch_w4a16<2>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
+    return launch_w4a16_tc(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, dev_status, st);
 }

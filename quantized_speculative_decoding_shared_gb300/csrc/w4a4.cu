@@ -34,7 +34,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kQuads = kThreads / 4;
 constexpr int kRows = 16;           // output rows per CTA
-constexpr int kPrefetch = 4;        // items in flight per quad
+constexpr int kPrefetch = 8;        // items in flight per quad
 
 __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
     uint4 r;
@@ -45,9 +45,10 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
 }
 
 // smem layout: acts int2 [MT][K/8] (.x: q of k0,k2,k4,k6 ; .y: k1,k3,k5,k7 as
-// signed bytes), then I int32 [G][kRows][MT], then sx float [MT][G], qs int [MT][G].
+// signed bytes), I int32 [G][kRows][MT], s float [G][kRows], sx float [MT][G],
+// qs int [MT][G].
 template <int MT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     w4a4_gemv_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx,
                      const int32_t *__restrict__ qs, const uint8_t *__restrict__ packed,
                      const uint32_t *__restrict__ sz, int M, int N, int K,
@@ -57,11 +58,32 @@ __global__ void __launch_bounds__(kThreads)
     const int K8 = K / 8;
     int2 *acts = reinterpret_cast<int2 *>(smem_raw);
     int32_t *ibuf = reinterpret_cast<int32_t *>(acts + (size_t)MT * K8);
-    float *sxs = reinterpret_cast<float *>(ibuf + kRows * MT * G);
+    float *sbuf = reinterpret_cast<float *>(ibuf + kRows * MT * G);
+    float *sxs = sbuf + kRows * G;
     int32_t *qss = reinterpret_cast<int32_t *>(sxs + MT * G);
 
     const int tok0 = blockIdx.y * MT;
     const int row0 = blockIdx.x * kRows;
+    const int quad = threadIdx.x >> 2, qc = threadIdx.x & 3;
+    const int n_items = kRows * G;
+    const size_t row_u4 = (size_t)K / 32;   // uint4 per packed row
+    const uint4 *wbase = reinterpret_cast<const uint4 *>(packed);
+
+    pdl_launch_dependents();
+    // weights and scale words are immutable: start streaming them before the
+    // previous kernel has finished
+    uint4 ring[kPrefetch];
+    uint32_t ring_sz[kPrefetch];
+#pragma unroll
+    for (int p = 0; p < kPrefetch; ++p) {
+        int it = quad + p * kQuads;
+        int r = it / G, g = it % G, n = row0 + r;
+        if (it < n_items && n < N) {
+            ring[p] = ldg_stream(wbase + (size_t)n * row_u4 + g * 4 + qc);
+            ring_sz[p] = __ldg(sz + (size_t)n * G + g);
+        }
+    }
+    pdl_wait();
 
     // stage activations: nibbles -> signed bytes, even-k and odd-k words
     const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
@@ -82,29 +104,21 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
 
     // phase 1: group integers of the CTA's rows
-    const int quad = threadIdx.x >> 2, qc = threadIdx.x & 3;
-    const int n_items = kRows * G;
-    const size_t row_u4 = (size_t)K / 32;   // uint4 per packed row
-    const uint4 *wbase = reinterpret_cast<const uint4 *>(packed);
-    uint4 ring[kPrefetch];
-#pragma unroll
-    for (int p = 0; p < kPrefetch; ++p) {
-        int it = quad + p * kQuads;
-        int r = it / G, g = it % G, n = row0 + r;
-        if (it < n_items && n < N) ring[p] = ldg_stream(wbase + (size_t)n * row_u4 + g * 4 + qc);
-    }
     for (int base = quad; base < n_items; base += kPrefetch * kQuads) {
 #pragma unroll
         for (int p = 0; p < kPrefetch; ++p) {
             const int it = base + p * kQuads;
             if (it >= n_items) break;
-            const int r = it / G, g = it % G, n = row0 + r;
-            const bool valid = n < N;
-            uint4 wv = ring[p];
+            const int r = it / G, g = it % G;
+            const uint4 wv = ring[p];
+            const uint32_t szw = ring_sz[p];
             {
                 int itn = it + kPrefetch * kQuads;
                 int rn = itn / G, gn = itn % G, nn = row0 + rn;
-                if (itn < n_items && nn < N) ring[p] = ldg_stream(wbase + (size_t)nn * row_u4 + gn * 4 + qc);
+                if (itn < n_items && nn < N) {
+                    ring[p] = ldg_stream(wbase + (size_t)nn * row_u4 + gn * 4 + qc);
+                    ring_sz[p] = __ldg(sz + (size_t)nn * G + gn);
+                }
             }
             const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
             uint32_t wl[4], wh[4];
@@ -113,8 +127,8 @@ __global__ void __launch_bounds__(kThreads)
                 wl[u] = w[u] & 0x0F0F0F0Fu;
                 wh[u] = (w[u] >> 4) & 0x0F0F0F0Fu;
             }
-            int zi = 0;
-            if (qc == 0 && valid) zi = (int)__half2float(__ushort_as_half((uint16_t)(__ldg(sz + (size_t)n * G + g) >> 16)));
+            const int zi = (int)__half2float(__ushort_as_half((uint16_t)(szw >> 16)));
+            if (qc == 0) sbuf[g * kRows + r] = __half2float(__ushort_as_half((uint16_t)(szw & 0xFFFF)));
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 const int4 *ap = reinterpret_cast<const int4 *>(acts + (size_t)t * K8 + g * 16 + qc * 4);
@@ -136,16 +150,15 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
 
-    // phase 2: fold the groups in ascending order, one thread per (row, token)
+    // phase 2: fold the groups in ascending order, one thread per (row, token);
+    // shared memory only
     for (int p = threadIdx.x; p < kRows * MT; p += kThreads) {
         const int r = p / MT, t = p % MT, n = row0 + r, m = tok0 + t;
         if (n >= N || m >= M) continue;
-        const uint32_t *szp = sz + (size_t)n * G;
         float acc = 0.0f;
         for (int g = 0; g < G; ++g) {
-            int32_t I = ibuf[(g * kRows + r) * MT + t];
-            float s = __half2float(__ushort_as_half((uint16_t)(__ldg(szp + g) & 0xFFFF)));
-            float c = __fmul_rn(sxs[t * G + g], s);
+            const int32_t I = ibuf[(g * kRows + r) * MT + t];
+            const float c = __fmul_rn(sxs[t * G + g], sbuf[g * kRows + r]);
             acc = __fmaf_rn(__int2float_rn(I), c, acc);
             if (dbg_I) dbg_I[((size_t)m * N + n) * G + g] = I;
         }
@@ -156,7 +169,8 @@ __global__ void __launch_bounds__(kThreads)
 template <int MT>
 size_t gemv_smem_bytes(int K) {
     const int G = K / kGroup;
-    return (size_t)MT * (K / 8) * sizeof(int2) + (size_t)kRows * MT * G * 4 + (size_t)MT * G * 8;
+    return (size_t)MT * (K / 8) * sizeof(int2) + (size_t)kRows * MT * G * 4 + (size_t)kRows * G * 4 +
+           (size_t)MT * G * 8;
 }
 
 constexpr size_t kMaxSmem = 200 * 1024;
@@ -169,8 +183,8 @@ int launch_gemv(const uint8_t *xq, const float *sx, const int32_t *qs, const uin
     int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_gemv_kernel<MT>), MT, (int)kMaxSmem);
     if (rc) return rc;
     dim3 grid((unsigned)((N + kRows - 1) / kRows), (unsigned)((M + MT - 1) / MT));
-    w4a4_gemv_kernel<MT><<<grid, kThreads, smem, st>>>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I);
-    return check_launch("qspec_linear_w4a4");
+    return launch_pdl("qspec_linear_w4a4", w4a4_gemv_kernel<MT>, grid, dim3(kThreads), smem, st, xq, sx,
+                      qs, packed, sz, M, N, K, y, ldy, dbg_I);
 }
 
 }  // namespace
@@ -183,7 +197,6 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
                                  const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
                                  uint16_t *y_bf16, int ldy, int32_t *dbg_I, int32_t *dev_status,
                                  qspec_stream_t stream) {
-    (void)dev_status;
     if (!xq || !sx || !qs || !packed || !sz || !y_bf16) return QSPEC_ERR_NULL;
     if (M < 1 || N < 1 || K < kGroup || K % kGroup || ldy < N) return QSPEC_ERR_SHAPE;
     if (!aligned(xq, 16) || !aligned(packed, 16) || !aligned(sz, 4) || !aligned(sx, 4) ||
@@ -192,6 +205,7 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
     int rc = check_device();
     if (rc) return rc;
     cudaStream_t st = as_cuda(stream);
+    if (M > 8) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
     if (M == 1 && gemv_smem_bytes<1>(K) <= kMaxSmem)
         return launch_gemv<1>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
     if (M <= 2 && gemv_smem_bytes<2>(K) <= kMaxSmem)

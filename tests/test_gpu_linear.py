@@ -58,12 +58,18 @@ def test_extreme_codes_and_unit_scales():
     codes = torch.from_numpy(rng.choice([0, 15], (N, K)).astype(np.uint8))
     z = torch.from_numpy(rng.choice([0.0, 15.0], (N, G))).to(torch.float16)
     s = torch.ones((N, G), dtype=torch.float16)
+    x = torch.from_numpy(rng.choice([-7.0, 7.0], (M, K)).astype(np.float32))
+    # worst case built in: row 0 all codes 15 with z = 0, token 0 all +7 -> I = 128 * 7 * 15;
+    # row 1 all codes 0 with z = 15 -> I = -128 * 7 * 15
+    codes[0], codes[1] = 15, 0
+    z[0], z[1] = 0.0, 15.0
+    x[0] = 7.0
+    x = x.to(torch.bfloat16)
     packed, sz = q.pack_weights(codes.to(dev), s.to(dev), z.to(dev))
     rc, po, szo = oracle.pack_weights(codes.numpy(), bits(s), bits(z))
-    x = torch.from_numpy(rng.choice([-7.0, 7.0], (M, K)).astype(np.float32)).to(torch.bfloat16)
     (y4, I), xqo, sxo = run_w4a4(x, packed, sz, dev)
     y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
-    assert np.abs(Io).max() == 128 * 7 * 15
+    assert Io[0, 0].max() == 128 * 7 * 15 and Io[0, 1].min() == -128 * 7 * 15
     assert np.array_equal(I.cpu().numpy(), Io) and np.array_equal(bits(y4), y4o)
     y16 = q.linear_w4a16(x.to(dev), packed, sz)
     assert_w4a16_close(y16, oracle.linear_w4a16(bits(x), po, szo), "extreme")
