@@ -187,6 +187,33 @@ int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_logits, cons
                         qspec_stream_t stream);
 
 /*
+ * Sampled verification for callers that cannot allocate device memory (for
+ * example code that runs while a CUDA graph is being captured, or a plugin
+ * with no allocator of its own).  Same inputs, outputs, decisions and device
+ * errors as qspec_verify_sample, bit for bit; the pages have no counterpart,
+ * this is an interface convenience.
+ *
+ * The scratch is a fixed array inside the library, QSPEC_VERIFY_NOALLOC_-
+ * SCRATCH_BYTES (1 MiB) on every GPU that loads the library, held until the
+ * process exits.  Sizes whose workspace (qspec_verify_workspace_bytes) would
+ * not fit return QSPEC_ERR_WORKSPACE before any launch -- e.g. B = 256,
+ * gamma = 4, V = 128256 needs about 0.4 MiB.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and leaves its
+ * contents behind (the parts that must start at zero are cleared on the
+ * stream by each call): calls that may overlap on the GPU -- on different
+ * streams, or from different threads -- race and must not be issued.
+ */
+#define QSPEC_VERIFY_NOALLOC_SCRATCH_BYTES (1 << 20)
+int qspec_verify_sample_noalloc(const uint16_t *p_logits, const uint16_t *q_logits,
+                                const int32_t *draft, int B, int gamma, int V, uint64_t seed,
+                                uint64_t round, int32_t *n_acc, int32_t *out, int32_t *dev_status,
+                                qspec_stream_t stream);
+
+/*
  * a7. KV overwrite.  [QS-design] for accepted tokens the low-precision (W4A4)
  * KV-cache entries are replaced with the W4A16 ones, so later steps read the
  * high-precision context from the one shared cache.  For each sequence b and

@@ -32,7 +32,8 @@ ERR_RANGE, ERR_ZERO_POINT, ERR_NONFINITE, ERR_TIMEOUT, ERR_UNSUPPORTED = 6, 7, 8
 EXPORTED = ["qspec_version", "qspec_status_string", "qspec_last_cuda_error", "qspec_pack_weights",
             "qspec_quant_act_int4", "qspec_linear_w4a4", "qspec_linear_w4a16",
             "qspec_verify_workspace_bytes", "qspec_verify_greedy", "qspec_verify_sample",
-            "qspec_kv_overwrite"]
+            "qspec_kv_overwrite", "qspec_verify_sample_noalloc"]
+NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class QspecError(RuntimeError):
@@ -73,7 +74,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "qspec_verify_sample": ([vp, vp, vp, i32, i32, i32, u64, u64, vp, vp, vp, sz_t, vp, vp],
                                     i32),
             "qspec_kv_overwrite": ([vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp],
-                                   i32)
+                                   i32),
+            "qspec_verify_sample_noalloc": ([vp, vp, vp, i32, i32, i32, u64, u64, vp, vp, vp, vp],
+                                            i32),
         }
         for name, (args, res) in proto.items():
             f = getattr(lib, name)
@@ -155,6 +158,16 @@ def qspec_verify_sample(p, q, draft, B, gamma, V, seed, rnd, n_acc, out, workspa
                                               ctypes.c_uint64(seed), ctypes.c_uint64(rnd),
                                               _ptr(n_acc), _ptr(out), _ptr(workspace), ws_bytes,
                                               _ptr(dev_status), _stream(stream))
+
+
+def qspec_verify_sample_noalloc(p, q, draft, B, gamma, V, seed, rnd, n_acc, out, dev_status=None,
+                                stream=None):
+    """Sampled verification with the library's built-in scratch array: for
+    callers that cannot allocate device memory (see include/qspec.h)."""
+    return load_library().qspec_verify_sample_noalloc(_ptr(p), _ptr(q), _ptr(draft), B, gamma, V,
+                                                      ctypes.c_uint64(seed), ctypes.c_uint64(rnd),
+                                                      _ptr(n_acc), _ptr(out), _ptr(dev_status),
+                                                      _stream(stream))
 
 
 def qspec_kv_overwrite(k_cache, v_cache, k_new, v_new, base_pos, n_acc, L, B, H, T, D, gamma,

@@ -571,3 +571,57 @@ extern "C" int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_l
                                       dev_status, st);
 }
 
+// ---------------------------------------------------------------------------
+// Sampled verification without any allocation by the caller.
+//
+// Some callers cannot call cudaMalloc at all: code running inside a CUDA
+// graph that is being captured (where allocation is not a stream operation),
+// plugins that own no allocator, or runtimes whose memory is fully reserved
+// up front.  For them this variant keeps its scratch in a fixed device array
+// that is part of the library image: every GPU that loads the library holds
+// QSPEC_VERIFY_NOALLOC_SCRATCH_BYTES of it until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QSPEC_VERIFY_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the array, looked up once per device with that device
+// current.  In host code the symbol g_noalloc_scratch is only a host-side
+// stand-in; a kernel handed it would read the wrong memory.
+static void *g_noalloc_addr[64];
+
+static int noalloc_scratch(void **ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_last_error("cudaGetDevice", e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    if (dev < 0 || dev >= 64) return QSPEC_ERR_UNSUPPORTED;
+    if (g_noalloc_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            set_last_error("cudaGetSymbolAddress(g_noalloc_scratch)", e);
+            return QSPEC_ERR_LAUNCH;
+        }
+        g_noalloc_addr[dev] = p;
+    }
+    *ptr = g_noalloc_addr[dev];
+    return QSPEC_OK;
+}
+
+extern "C" int qspec_verify_sample_noalloc(const uint16_t *p_logits, const uint16_t *q_logits,
+                                           const int32_t *draft, int B, int gamma, int V, uint64_t seed,
+                                           uint64_t round, int32_t *n_acc, int32_t *out,
+                                           int32_t *dev_status, qspec_stream_t stream) {
+    if (!p_logits || !q_logits || !draft || !n_acc || !out) return QSPEC_ERR_NULL;
+    if (B < 1 || gamma < 1 || gamma > QSPEC_MAX_GAMMA || V < 1) return QSPEC_ERR_SHAPE;
+    if (make_layout(B, gamma, V).total > (size_t)QSPEC_VERIFY_NOALLOC_SCRATCH_BYTES)
+        return QSPEC_ERR_WORKSPACE;
+    int rc = check_device();
+    if (rc) return rc;
+    void *scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    return qspec_verify_sample(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, scratch,
+                               QSPEC_VERIFY_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+}
