@@ -53,9 +53,22 @@ GROUP = 128
 FALLBACK_HBM_GBS = 6800.0
 
 WORKLOADS = {
+    # Llama-3-8B decode at batch 1: W4A4 draft at M = 1, W4A16 verify at M = 5
     "llama3-8b-decode-b1-g4": dict(shape=syn.LLAMA3_8B, B=1, gamma=4, outliers=0.01,
                                    T=4096, p_std=3.0, q_noise=0.5, seed=1),
+    # Llama-3-8B at batch 16: W4A16 verify at M = 80 (with the LM head), verification
+    # over 16 x 5 x 128256 logits, KV overwrite on the 32-layer cache
+    "llama3-8b-b16-g4": dict(shape=syn.LLAMA3_8B, B=16, gamma=4, outliers=0.0,
+                             T=4096, p_std=3.0, q_noise=0.5, seed=2),
+    # Qwen2.5-7B at batch 32, gamma 2 / 4 / 8 (W4A4 at M = 32, W4A16 at M = 96 / 160 / 288)
+    "qwen2.5-7b-b32-g2": dict(shape=syn.QWEN25_7B, B=32, gamma=2, outliers=0.0,
+                              T=4096, p_std=3.0, q_noise=0.5, seed=3),
+    "qwen2.5-7b-b32-g4": dict(shape=syn.QWEN25_7B, B=32, gamma=4, outliers=0.0,
+                              T=4096, p_std=3.0, q_noise=0.5, seed=3),
+    "qwen2.5-7b-b32-g8": dict(shape=syn.QWEN25_7B, B=32, gamma=8, outliers=0.0,
+                              T=4096, p_std=3.0, q_noise=0.5, seed=3),
 }
+PREFILL = "llama3-8b-prefill-m4096"
 
 
 def parse_args():
@@ -64,7 +77,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3-8b-decode-b1-g4")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + [PREFILL],
+                    default="llama3-8b-decode-b1-g4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rounds", type=int, default=16, help="distinct captured rounds (RNG round ids)")
     ap.add_argument("--profile-case", choices=["w4a4_m1", "w4a16_m5", "quant", "verify_sample",
@@ -364,6 +378,64 @@ def aggregate_over_ranks(seconds, tokens, device):
     return float(mx[0]), int(round(float(t[1])))
 
 
+def row_kernels(dev, stream, reps=5):
+    """Every hot-path row timed on its own at a representative size (CUDA
+    graph replays, CUDA events): algorithmic bytes per call, GB/s, fraction
+    of the measured HBM bandwidth."""
+    from quantized_speculative_decoding_shared_gb300 import binding as q
+    peak, _ = measured_peaks()
+    out = {}
+
+    def rec(name, fn, nbytes, note):
+        fn()
+        torch.cuda.synchronize()
+        g = capture(fn, stream)
+        t = time_graph(g, reps, stream)
+        out[name] = {"case": note, "us": round(t * 1e3, 2), "bytes": int(nbytes),
+                     "GB/s": round(nbytes / (t / 1e3) / 1e9, 1),
+                     "frac_hbm": round(nbytes / (t / 1e3) / 1e9 / peak, 4)}
+        del g
+
+    N, K = 128256, 4096
+    codes, s_, z_ = syn.weights(N, K, 91, device=dev)
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    sz = torch.empty((N, K // GROUP), dtype=torch.int32, device=dev)
+    rec("a1_pack", lambda: q.qspec_pack_weights(codes, s_, z_, N, K, packed, sz),
+        N * K + 4 * N * K // GROUP + N * K // 2 + 4 * N * K // GROUP, "128256 x 4096 (LM head)")
+    del codes, s_, z_, packed, sz
+    M, K = 4096, 14336
+    x = syn.activations(M, K, 92, device=dev)
+    xq = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    sx = torch.empty((M, K // GROUP), dtype=torch.float32, device=dev)
+    qs = torch.empty((M, K // GROUP), dtype=torch.int32, device=dev)
+    rec("a2_quant_act_int4", lambda: q.qspec_quant_act_int4(x, M, K, K, xq, sx, qs),
+        bytes_quant(M, K), "4096 x 14336")
+    del x, xq, sx, qs
+    B, g, V = 16, 4, 128256
+    P, Q, d = syn.logits_noisy_draft(B, g, V, 93, device=dev)
+    ws = q.verify_workspace(256, g, V, dev)
+    n_acc = torch.empty(256, dtype=torch.int32, device=dev)
+    o = torch.empty((256, g + 1), dtype=torch.int32, device=dev)
+    rec("a5_verify_greedy", lambda: q.qspec_verify_greedy(P, d, B, g, V, n_acc, o, ws, ws.numel()),
+        2 * B * (g + 1) * V, "B 16, gamma 4, V 128256")
+    del P, Q, d
+    B = 256
+    P, Q, d = syn.logits_noisy_draft(B, g, V, 94, device=dev)
+    rec("a6_verify_sample", lambda: q.qspec_verify_sample(P, Q, d, B, g, V, 5, 0, n_acc, o, ws, ws.numel()),
+        2 * B * (2 * g + 1) * V, "B 256, gamma 4, V 128256")
+    del P, Q, d, ws
+    L, B, H, T, D = 32, 16, 8, 4096, 128
+    kc, vc = syn.kv_cache(L, B, H, T, D, 95, device=dev)
+    kn, vn = syn.kv_new(L, B, g, H, D, 96, device=dev)
+    base = syn.base_positions(B, T, g, 97, device=dev)
+    na = torch.full((B,), g, dtype=torch.int32, device=dev)
+    rec("a7_kv_overwrite", lambda: q.qspec_kv_overwrite(kc, vc, kn, vn, base, na, L, B, H, T, D, g),
+        2 * 2 * 2 * L * B * (g + 1) * H * D, "32 layers x 16 seq x 8 heads x 4096 x 128, all 4 drafts accepted")
+    del kc, vc, kn, vn
+    torch.cuda.synchronize()
+    return out
+
+
 def capture(fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -469,18 +541,81 @@ def cpu_baseline(wl, steps=3):
 
 
 # ---------------------------------------------------------------------------
+def prefill_bench(args):
+    """M = 4096 tokens through Llama-3-8B gate/up (4096 -> 14336, stacked as
+    28672) and down (14336 -> 4096): W4A4 on the tensor cores (TOPS, exact
+    integer products) and W4A16 (bf16 tensor cores); plus batch-256 sampled
+    verification over 128256 tokens at gamma 4."""
+    from quantized_speculative_decoding_shared_gb300 import binding as q
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    M = 4096
+    shapes = [("gate_up_proj", 28672, 4096), ("down_proj", 4096, 14336)]
+    mats = {}
+    for j, (name, N, K) in enumerate(shapes):
+        codes, s_, z_ = syn.weights(N, K, 40 + j, device=dev)
+        mats[name] = q.pack_weights(codes, s_, z_)
+        del codes
+    xs = {name: syn.activations(M, K, 50 + j, device=dev) for j, (name, N, K) in enumerate(shapes)}
+    qx = {name: q.quant_act_int4(xs[name]) for name, _, _ in shapes}
+    ys = {name: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for name, N, _ in shapes}
+    stream = torch.cuda.Stream(device=dev)
+
+    def run4():
+        for name, N, K in shapes:
+            xq, sx, qs = qx[name]
+            q.linear_w4a4(xq, sx, qs, *mats[name], out=ys[name])
+
+    def run16():
+        for name, N, K in shapes:
+            q.linear_w4a16(xs[name], *mats[name], out=ys[name])
+
+    with torch.cuda.stream(stream):
+        run4(); run16()
+    torch.cuda.synchronize()
+    flops = sum(2 * M * N * K for _, N, K in shapes)
+    g4, g16 = capture(run4, stream), capture(run16, stream)
+    for _ in range(args.warmup):
+        time_graph(g4, 1, stream)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    t4 = time_graph(g4, args.steps, stream)
+    t16 = time_graph(g16, args.steps, stream)
+    clk = clocks.stop()
+    P, Q, d = syn.logits_noisy_draft(256, 4, 128256, 4, device=dev)
+    ws = q.verify_workspace(256, 4, 128256, dev)
+    gv = capture(lambda: q.verify_sample(P, Q, d, 1, 0, workspace=ws), stream)
+    tv = time_graph(gv, args.steps, stream)
+    vbytes = 2 * 256 * 9 * 128256
+    peak_hbm, kind = measured_peaks()
+    line = {"metric": "W4A4 INT TOPS (M = 4096)", "value": round(flops / (t4 / 1e3) / 1e12, 2),
+            "unit": "TOPS", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t4, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int4 x int4 -> exact (e4m3 tensor operands, fp32 = exact int)",
+            "data": "synthetic", "config": {"workload": PREFILL, "M": M, "shapes": shapes},
+            "w4a16": {"TFLOPS": round(flops / (t16 / 1e3) / 1e12, 2), "ms": round(t16, 4)},
+            "verify_b256_g4": {"ms": round(tv, 4), "GB/s": round(vbytes / (tv / 1e3) / 1e9, 1),
+                               "frac_hbm": round(vbytes / (tv / 1e3) / 1e9 / peak_hbm, 4)},
+            "clocks": clk}
+    print(json.dumps(line))
+
+
 def main():
     args = parse_args()
     if args.profile_case:
         profile_case(args.profile_case, args.profile_reps)
         return
+    if args.workload == PREFILL:
+        prefill_bench(args)
+        return
     wl = WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = {"workload": args.workload, "model_shape": "llama3-8b (32 layers, 4096 hidden, "
-           "128256 vocab)", "batch": wl["B"], "gamma": wl["gamma"],
-           "l2": "inputs larger than L2 (3.9 GB of weights per step)",
+    sh = wl["shape"]
+    cfg = {"workload": args.workload, "model_shape": "%d layers, %d hidden, %d vocab" % (
+           sh["layers"], sh["hidden"], sh["vocab"]), "batch": wl["B"], "gamma": wl["gamma"],
+           "l2": "inputs larger than L2 (every step reads all packed weights, ~4 GB)",
            "parallelism": "replicas x%d" % args.gpus}
 
     if args.impl == "reference":
@@ -576,7 +711,7 @@ def main():
     ach4 = rnd_obj.bytes_draft_linears() / (t4 / 1e3) / 1e9
     ach16 = rnd_obj.bytes_verify_linears() / (t16 / 1e3) / 1e9
     traffic = recorded_traffic("w4a4.cu")
-    roofline = {"bound": "hbm", "kernel": "w4a4_gemv_kernel<1> (W4A4 linear, M = 1)",
+    roofline = {"bound": "hbm", "kernel": "w4a4_mma_gemv_kernel (W4A4 linear, M = %d)" % wl["B"],
                 "achieved": round(ach4, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach4 / peak, 4), "peak_source": peak_kind,
                 "bytes_per_launch": rnd_obj.bytes_draft_linears() / n4,
@@ -622,6 +757,7 @@ def main():
                                                  "frac_hbm": round(ach16 / peak, 4),
                                                  "ms_per_verify_pass": round(t16, 4),
                                                  "M": wl["B"] * (wl["gamma"] + 1)}},
+            "rows": row_kernels(dev, stream),
             "gpu_launches": rnd_obj.launches_per_round() * args.steps,
             "clocks": clk}
     if world == 1 and not args.no_cpu_baseline:

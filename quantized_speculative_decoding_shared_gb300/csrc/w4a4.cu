@@ -12,16 +12,8 @@
 //   acc = 0; for g ascending: acc = fmaf((float) I, sx[m][g] * s[n][g], acc)
 //   y[m][n] = bf16_rn(acc)
 //
-// Small-M path (draft decode, M <= 8 tokens per CTA): CUDA-core dp4a.
-//   - the CTA stages its tokens' INT4 activations in shared memory as signed
-//     bytes, in the order the weight nibbles unpack to (even k / odd k);
-//   - a quad of 4 lanes owns one (row, group) item: each lane loads 16 bytes
-//     (32 weights), dp4a against the activations, two shuffles give the
-//     group's integer sum; the quad leader stores I to shared memory;
-//   - once every group of the CTA's 16 rows is in, one thread per
-//     (row, token) folds the groups in ascending order in fp32.
-// HBM-bound at small M: 0.5 byte of weight + 4/128 byte of scale/zero per
-// weight.
+// Small-M path (M <= 32, draft decode): FP8 warp MMA on exact small
+// integers, described below.  Larger M: tcgen05 (w4a4_tc.cu).
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -31,161 +23,234 @@ namespace qspec {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kQuads = kThreads / 4;
-constexpr int kRows = 16;           // output rows per CTA
-constexpr int kPrefetch = 8;        // items in flight per quad
+// ---------------------------------------------------------------------------
+// Small-M path on the FP8 tensor cores (warp MMA m16n8k32, e4m3 operands).
+//
+// An E4M3 byte holding a value b in 0..15 is exactly b * 2^-9 (subnormals for
+// b < 8, exponent 1 above), so the unpacked nibbles feed the MMA with no table:
+//   A (weights): codes c, one byte each            -> c * 2^-9
+//   B (tokens):  u = q + 8 = nibble ^ 8, one byte   -> u * 2^-9
+//   B column OC: all ones                           -> 2^-9
+// and the fp32 accumulator of one 128-wide group holds, exactly,
+//   D = sum u c * 2^-18   and   C = sum c * 2^-18 (column OC).
+// Then I = sum q (c - z) = sum u c - 8 sum c - z qs, all integers below 2^15:
+//   I = fmaf(-z, qs, fmaf(D, 2^18, -8 C 2^18)) exactly in fp32.
+// Each thread loads 16 bytes (32 codes) of two rows per group; the k order
+// inside the MMA is permuted identically on A and B (even k then odd k of
+// every 8), so unpacking is two logic operations per word.  Warps split the
+// groups of a 16-row tile; one thread per (row, token) folds in order.
+// ---------------------------------------------------------------------------
+namespace mmak {
 
-__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
+constexpr int kThreads = 256;
+constexpr int kWarps = 8;
+constexpr int kPrefetch = 4;           // groups in flight per warp
+
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// smem layout: acts int2 [MT][K/8] (.x: q of k0,k2,k4,k6 ; .y: k1,k3,k5,k7 as
-// signed bytes), I int32 [G][kRows][MT], s float [G][kRows], sx float [MT][G],
-// qs int [MT][G].
+// Persistent over 16-row tiles.  smem: actf uint2 [MT][G][16] (B fragments),
+// I float [2][G][16][MT] (double buffer), s float [2][G][16], sx float [MT][G],
+// qs float [MT][G].  Warp w owns groups w, w + 8, ...; per warp the (tile,
+// group) items form one sequence, so the prefetch ring runs across tiles.
+// After a tile, one warp folds it (ascending groups) while the others start
+// the next tile; the next barrier orders the fold before its buffer is reused.
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 2)
-    w4a4_gemv_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx,
-                     const int32_t *__restrict__ qs, const uint8_t *__restrict__ packed,
-                     const uint32_t *__restrict__ sz, int M, int N, int K,
-                     uint16_t *__restrict__ y, int ldy, int32_t *__restrict__ dbg_I) {
+    w4a4_mma_gemv_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx,
+                         const int32_t *__restrict__ qs, const uint8_t *__restrict__ packed,
+                         const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
+                         int32_t *__restrict__ dbg_I) {
+    constexpr int OC = MT == 1 ? 1 : 7;          // the all-ones B column
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int G = K / kGroup;
-    const int K8 = K / 8;
-    int2 *acts = reinterpret_cast<int2 *>(smem_raw);
-    int32_t *ibuf = reinterpret_cast<int32_t *>(acts + (size_t)MT * K8);
-    float *sbuf = reinterpret_cast<float *>(ibuf + kRows * MT * G);
-    float *sxs = sbuf + kRows * G;
-    int32_t *qss = reinterpret_cast<int32_t *>(sxs + MT * G);
-
+    uint2 *actf = reinterpret_cast<uint2 *>(smem_raw);
+    float *ibuf = reinterpret_cast<float *>(actf + (size_t)MT * G * 16);
+    float *sbuf = ibuf + (size_t)2 * G * 16 * MT;
+    float *sxs = sbuf + (size_t)2 * G * 16;
+    float *qss = sxs + (size_t)MT * G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qr = lane >> 2, qc = lane & 3;
     const int tok0 = blockIdx.y * MT;
-    const int row0 = blockIdx.x * kRows;
-    const int quad = threadIdx.x >> 2, qc = threadIdx.x & 3;
-    const int n_items = kRows * G;
-    const size_t row_u4 = (size_t)K / 32;   // uint4 per packed row
-    const uint4 *wbase = reinterpret_cast<const uint4 *>(packed);
+    const int n_tiles = (N + 15) / 16;
+    const size_t row_u4 = (size_t)K / 32;
+    const uint4 *wbase = reinterpret_cast<const uint4 *>(packed) + qc;
+    const int ng = warp < G ? (G - warp + kWarps - 1) / kWarps : 0;     // this warp's groups per tile
+    const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int n_items = ng * my_tiles;
+
+    // item cursor -> (tile, group); advanced incrementally, no division
+    struct Cursor {
+        int step, gi;
+    };
+    auto load_item = [&](const Cursor &c, uint4 &wa, uint4 &wb, uint32_t &za, uint32_t &zb) {
+        const int tile = blockIdx.x + c.step * gridDim.x, g = warp + c.gi * kWarps;
+        const int r0 = tile * 16 + qr, r1 = r0 + 8;
+        const bool v0 = r0 < N, v1 = r1 < N;
+        wa = __ldg(wbase + (size_t)(v0 ? r0 : 0) * row_u4 + g * 4);
+        wb = __ldg(wbase + (size_t)(v1 ? r1 : 0) * row_u4 + g * 4);
+        za = v0 ? __ldg(sz + (size_t)r0 * G + g) : 0u;
+        zb = v1 ? __ldg(sz + (size_t)r1 * G + g) : 0u;
+    };
+    auto advance = [&](Cursor &c) {
+        if (++c.gi == ng) {
+            c.gi = 0;
+            ++c.step;
+        }
+    };
 
     pdl_launch_dependents();
-    // weights and scale words are immutable: start streaming them before the
-    // previous kernel has finished
-    uint4 ring[kPrefetch];
-    uint32_t ring_sz[kPrefetch];
+    // immutable weights and scale words first
+    uint4 ra[kPrefetch], rb[kPrefetch];
+    uint32_t sa[kPrefetch], sb[kPrefetch];
+    Cursor pc = {0, 0};
 #pragma unroll
     for (int p = 0; p < kPrefetch; ++p) {
-        int it = quad + p * kQuads;
-        int r = it / G, g = it % G, n = row0 + r;
-        if (it < n_items && n < N) {
-            ring[p] = ldg_stream(wbase + (size_t)n * row_u4 + g * 4 + qc);
-            ring_sz[p] = __ldg(sz + (size_t)n * G + g);
+        if (p < n_items) {
+            load_item(pc, ra[p], rb[p], sa[p], sb[p]);
+            advance(pc);
         }
     }
     pdl_wait();
 
-    // stage activations: nibbles -> signed bytes, even-k and odd-k words
+    // this CTA's tokens, once: B fragments (u = q + 8 as bytes, even k then odd k), sx, qs
     const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
-    for (int i = threadIdx.x; i < MT * K8; i += kThreads) {
-        int t = i / K8, j = i % K8, m = tok0 + t;
-        uint32_t w = m < M ? xw[(size_t)m * K8 + j] : 0u;
-        uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
-        // two's-complement nibble -> byte: (v ^ 8) - 8, per byte without borrows
-        lo = __vsub4(lo ^ 0x08080808u, 0x08080808u);
-        hi = __vsub4(hi ^ 0x08080808u, 0x08080808u);
-        acts[i] = make_int2((int)lo, (int)hi);
-    }
-    for (int i = threadIdx.x; i < MT * G; i += kThreads) {
-        int t = i / G, m = tok0 + t;
-        sxs[i] = m < M ? sx[(size_t)m * G + i % G] : 0.0f;
-        qss[i] = m < M ? qs[(size_t)m * G + i % G] : 0;
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        const int m = tok0 + t;
+        for (int i = threadIdx.x; i < G * 16; i += kThreads) {
+            const uint32_t w = m < M ? xw[(size_t)m * (K / 8) + i] ^ 0x88888888u : 0u;
+            actf[(size_t)t * G * 16 + i] = make_uint2(w & 0x0F0F0F0Fu, (w >> 4) & 0x0F0F0F0Fu);
+        }
+        for (int g = threadIdx.x; g < G; g += kThreads) {
+            sxs[t * G + g] = m < M ? sx[(size_t)m * G + g] : 0.0f;
+            qss[t * G + g] = m < M ? (float)qs[(size_t)m * G + g] : 0.0f;
+        }
     }
     __syncthreads();
 
-    // phase 1: group integers of the CTA's rows
-    for (int base = quad; base < n_items; base += kPrefetch * kQuads) {
+    const bool tok_row = qr < MT && tok0 + qr < M;     // this thread feeds a real token column
+    const int tq = qr < MT ? qr : 0;
+    const float two18 = 262144.0f;
+
+    // end of tile `step`: every warp arrives once per tile; then one warp folds it
+    auto tile_done = [&](int step) {
+        __syncthreads();
+        if (warp != (step & (kWarps - 1))) return;
+        const int tile = blockIdx.x + step * gridDim.x;
+        const float *ib = ibuf + (size_t)(step & 1) * G * 16 * MT;
+        const float *sbb = sbuf + (size_t)(step & 1) * G * 16;
+        for (int p = lane; p < 16 * MT; p += 32) {
+            const int r = p / MT, t = p - (p / MT) * MT, n = tile * 16 + r, m = tok0 + t;
+            if (n >= N || m >= M) continue;
+            float acc = 0.0f;
+            for (int g = 0; g < G; ++g) {
+                const float I = ib[((size_t)g * 16 + r) * MT + t];
+                acc = __fmaf_rn(I, __fmul_rn(sxs[t * G + g], sbb[(size_t)g * 16 + r]), acc);
+                if (dbg_I) dbg_I[((size_t)m * N + n) * G + g] = (int32_t)I;
+            }
+            y[(size_t)m * ldy + n] = float_to_bf16_bits(acc);
+        }
+    };
+
+    Cursor cc = {0, 0};
+    int cur = 0;                                          // tile step being produced
+    for (int base = 0; base < n_items; base += kPrefetch) {
 #pragma unroll
         for (int p = 0; p < kPrefetch; ++p) {
-            const int it = base + p * kQuads;
+            const int it = base + p;
             if (it >= n_items) break;
-            const int r = it / G, g = it % G;
-            const uint4 wv = ring[p];
-            const uint32_t szw = ring_sz[p];
-            {
-                int itn = it + kPrefetch * kQuads;
-                int rn = itn / G, gn = itn % G, nn = row0 + rn;
-                if (itn < n_items && nn < N) {
-                    ring[p] = ldg_stream(wbase + (size_t)nn * row_u4 + gn * 4 + qc);
-                    ring_sz[p] = __ldg(sz + (size_t)nn * G + gn);
+            if (cc.step != cur) {                         // this warp's first item of the next tile
+                tile_done(cur);
+                cur = cc.step;
+            }
+            const int g = warp + cc.gi * kWarps;
+            float *ib = ibuf + (size_t)(cur & 1) * G * 16 * MT;
+            float *sbb = sbuf + (size_t)(cur & 1) * G * 16;
+            const uint4 wa = ra[p], wb = rb[p];
+            const uint32_t za = sa[p], zb = sb[p];
+            if (it + kPrefetch < n_items) {
+                load_item(pc, ra[p], rb[p], sa[p], sb[p]);
+                advance(pc);
+            }
+            uint32_t bf0[4], bf1[4];
+            if (tok_row) {
+                const uint4 *ap = reinterpret_cast<const uint4 *>(actf + ((size_t)tq * G + g) * 16 + qc * 4);
+                const uint4 f01 = ap[0], f23 = ap[1];
+                bf0[0] = f01.x; bf1[0] = f01.y; bf0[1] = f01.z; bf1[1] = f01.w;
+                bf0[2] = f23.x; bf1[2] = f23.y; bf0[3] = f23.z; bf1[3] = f23.w;
+            } else {
+                const uint32_t one = qr == OC ? 0x01010101u : 0u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bf0[j] = bf1[j] = one;
+            }
+            const uint32_t wa_[4] = {wa.x, wa.y, wa.z, wa.w}, wb_[4] = {wb.x, wb.y, wb.z, wb.w};
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mma_e4m3_16832(d, wa_[j] & 0x0F0F0F0Fu, wb_[j] & 0x0F0F0F0Fu, (wa_[j] >> 4) & 0x0F0F0F0Fu,
+                               (wb_[j] >> 4) & 0x0F0F0F0Fu, bf0[j], bf1[j]);
+            // D: rows (qr, qr + 8) x columns (2 qc, 2 qc + 1); C from column OC
+            float c_a, c_b;
+            if (MT == 1) {
+                c_a = d[1];
+                c_b = d[3];
+            } else {
+                c_a = __shfl_sync(0xffffffffu, d[1], (lane & ~3) | 3);
+                c_b = __shfl_sync(0xffffffffu, d[3], (lane & ~3) | 3);
+            }
+            if (2 * qc < MT) {
+                const float ia = c_a * (-8.0f * two18), ibv = c_b * (-8.0f * two18);   // exact
+                const float zfa = __half2float(__ushort_as_half((uint16_t)(za >> 16)));
+                const float zfb = __half2float(__ushort_as_half((uint16_t)(zb >> 16)));
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = 2 * qc + e;
+                    if (t < MT && t != OC) {
+                        const float q_s = qss[t * G + g];
+                        ib[((size_t)g * 16 + qr) * MT + t] = __fmaf_rn(-zfa, q_s, __fmaf_rn(d[e], two18, ia));
+                        ib[((size_t)g * 16 + qr + 8) * MT + t] = __fmaf_rn(-zfb, q_s, __fmaf_rn(d[2 + e], two18, ibv));
+                    }
                 }
             }
-            const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-            uint32_t wl[4], wh[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                wl[u] = w[u] & 0x0F0F0F0Fu;
-                wh[u] = (w[u] >> 4) & 0x0F0F0F0Fu;
+            if (qc == 0) {
+                sbb[(size_t)g * 16 + qr] = __half2float(__ushort_as_half((uint16_t)(za & 0xFFFF)));
+                sbb[(size_t)g * 16 + qr + 8] = __half2float(__ushort_as_half((uint16_t)(zb & 0xFFFF)));
             }
-            const int zi = (int)__half2float(__ushort_as_half((uint16_t)(szw >> 16)));
-            if (qc == 0) sbuf[g * kRows + r] = __half2float(__ushort_as_half((uint16_t)(szw & 0xFFFF)));
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                const int4 *ap = reinterpret_cast<const int4 *>(acts + (size_t)t * K8 + g * 16 + qc * 4);
-                int4 a01 = ap[0], a23 = ap[1];
-                int s = 0;
-                s = __dp4a(a01.x, (int)wl[0], s);
-                s = __dp4a(a01.y, (int)wh[0], s);
-                s = __dp4a(a01.z, (int)wl[1], s);
-                s = __dp4a(a01.w, (int)wh[1], s);
-                s = __dp4a(a23.x, (int)wl[2], s);
-                s = __dp4a(a23.y, (int)wh[2], s);
-                s = __dp4a(a23.z, (int)wl[3], s);
-                s = __dp4a(a23.w, (int)wh[3], s);
-                s += __shfl_xor_sync(0xffffffffu, s, 1);
-                s += __shfl_xor_sync(0xffffffffu, s, 2);
-                if (qc == 0) ibuf[(g * kRows + r) * MT + t] = s - zi * qss[t * G + g];
-            }
+            advance(cc);
         }
     }
-    __syncthreads();
-
-    // phase 2: fold the groups in ascending order, one thread per (row, token);
-    // shared memory only
-    for (int p = threadIdx.x; p < kRows * MT; p += kThreads) {
-        const int r = p / MT, t = p % MT, n = row0 + r, m = tok0 + t;
-        if (n >= N || m >= M) continue;
-        float acc = 0.0f;
-        for (int g = 0; g < G; ++g) {
-            const int32_t I = ibuf[(g * kRows + r) * MT + t];
-            const float c = __fmul_rn(sxs[t * G + g], sbuf[g * kRows + r]);
-            acc = __fmaf_rn(__int2float_rn(I), c, acc);
-            if (dbg_I) dbg_I[((size_t)m * N + n) * G + g] = I;
-        }
-        y[(size_t)m * ldy + n] = float_to_bf16_bits(acc);
-    }
+    // the last tile with items, then the remaining ones (warps without groups)
+    for (; cur < my_tiles; ++cur) tile_done(cur);
 }
 
 template <int MT>
-size_t gemv_smem_bytes(int K) {
+size_t smem_bytes(int K) {
     const int G = K / kGroup;
-    return (size_t)MT * (K / 8) * sizeof(int2) + (size_t)kRows * MT * G * 4 + (size_t)kRows * G * 4 +
+    return (size_t)MT * G * 16 * sizeof(uint2) + (size_t)2 * G * 16 * MT * 4 + (size_t)2 * G * 16 * 4 +
            (size_t)MT * G * 8;
 }
 
-constexpr size_t kMaxSmem = 200 * 1024;
-
 template <int MT>
-int launch_gemv(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
-                const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I,
-                cudaStream_t st) {
-    size_t smem = gemv_smem_bytes<MT>(K);
-    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_gemv_kernel<MT>), MT, (int)kMaxSmem);
+int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed, const uint32_t *sz, int M,
+           int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, cudaStream_t st) {
+    const size_t smem = smem_bytes<MT>(K);
+    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_mma_gemv_kernel<MT>), 8 + MT, 200 * 1024);
     if (rc) return rc;
-    dim3 grid((unsigned)((N + kRows - 1) / kRows), (unsigned)((M + MT - 1) / MT));
-    return launch_pdl("qspec_linear_w4a4", w4a4_gemv_kernel<MT>, grid, dim3(kThreads), smem, st, xq, sx,
-                      qs, packed, sz, M, N, K, y, ldy, dbg_I);
+    const int n_tiles = (N + 15) / 16, token_tiles = (M + MT - 1) / MT;
+    const int per_col = std::max(1, 2 * sm_count() / token_tiles);
+    dim3 grid((unsigned)std::min(n_tiles, per_col), (unsigned)token_tiles);
+    return launch_pdl("qspec_linear_w4a4", w4a4_mma_gemv_kernel<MT>, grid, dim3(kThreads), smem, st, xq, sx, qs,
+                      packed, sz, M, N, K, y, ldy, dbg_I);
 }
+
+}  // namespace mmak
 
 }  // namespace
 
@@ -205,16 +270,19 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
     int rc = check_device();
     if (rc) return rc;
     cudaStream_t st = as_cuda(stream);
-    if (M > 8) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
-    if (M == 1 && gemv_smem_bytes<1>(K) <= kMaxSmem)
-        return launch_gemv<1>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (M <= 2 && gemv_smem_bytes<2>(K) <= kMaxSmem)
-        return launch_gemv<2>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (M <= 4 && gemv_smem_bytes<4>(K) <= kMaxSmem)
-        return launch_gemv<4>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (gemv_smem_bytes<8>(K) <= kMaxSmem)
-        return launch_gemv<8>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (gemv_smem_bytes<4>(K) <= kMaxSmem)
-        return launch_gemv<4>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+    if (M > 32) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
+    constexpr size_t kMaxSmem = 200 * 1024;
+    if (M == 1 && mmak::smem_bytes<1>(K) <= kMaxSmem)
+        return mmak::launch<1>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+    if (M == 2 && mmak::smem_bytes<2>(K) <= kMaxSmem)
+        return mmak::launch<2>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+    if (M <= 4 && mmak::smem_bytes<4>(K) <= kMaxSmem)
+        return mmak::launch<4>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+    if (mmak::smem_bytes<7>(K) <= kMaxSmem)
+        return mmak::launch<7>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+    if (mmak::smem_bytes<4>(K) <= kMaxSmem)
+        return mmak::launch<4>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+    if (mmak::smem_bytes<1>(K) <= kMaxSmem)
+        return mmak::launch<1>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
     return QSPEC_ERR_SHAPE;
 }
