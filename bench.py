@@ -711,7 +711,7 @@ def main():
     ach4 = rnd_obj.bytes_draft_linears() / (t4 / 1e3) / 1e9
     ach16 = rnd_obj.bytes_verify_linears() / (t16 / 1e3) / 1e9
     traffic = recorded_traffic("w4a4.cu")
-    roofline = {"bound": "hbm", "kernel": "w4a4_mma_gemv_kernel (W4A4 linear, M = %d)" % wl["B"],
+    roofline = {"bound": "hbm", "kernel": "w4a4_hmma_gemv_kernel (W4A4 linear, M = %d)" % wl["B"],
                 "achieved": round(ach4, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach4 / peak, 4), "peak_source": peak_kind,
                 "bytes_per_launch": rnd_obj.bytes_draft_linears() / n4,

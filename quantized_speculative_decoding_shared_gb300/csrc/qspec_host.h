@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "qspec.h"
@@ -39,6 +40,17 @@ int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uin
 int launch_w4a4_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                    const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st,
                    cudaStream_t stream);
+
+// Decode-sized W4A4 (M <= 8) on the tensor cores with the weights staged in
+// TMEM (w4a4_gemv_tc.cu); QSPEC_ERR_SHAPE before any launch when the shape
+// does not suit it.
+int launch_w4a4_gemv_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
+                        const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I,
+                        int32_t *dev_status, cudaStream_t stream);
+
+// 2-D TMA map over a packed weight matrix [N][K / 2] bytes: boxes of 128
+// bytes x box_rows rows, 128-byte swizzle, rows past N read as zeros.
+int weight_tmap(CUtensorMap *out, const uint8_t *packed, int N, int K, int box_rows);
 
 // Launch `kernel` on `st` with programmatic stream serialisation allowed (the
 // kernel must follow the pdl_wait() rule in qspec_device.cuh).

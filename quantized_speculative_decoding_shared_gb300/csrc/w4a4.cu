@@ -12,8 +12,9 @@
 //   acc = 0; for g ascending: acc = fmaf((float) I, sx[m][g] * s[n][g], acc)
 //   y[m][n] = bf16_rn(acc)
 //
-// Small-M path (M <= 32, draft decode): FP8 warp MMA on exact small
-// integers, described below.  Larger M: tcgen05 (w4a4_tc.cu).
+// Small-M path (M <= 32, draft decode): f16 warp MMA on exact small
+// integers, described below; 3 <= M <= 8 with at least one 128-row tile per
+// SM: tensor-memory GEMV (w4a4_gemv_tc.cu).  Larger M: tcgen05 (w4a4_tc.cu).
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -24,120 +25,233 @@ namespace qspec {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Small-M path on the FP8 tensor cores (warp MMA m16n8k32, e4m3 operands).
+// Small-M path: warp MMA m16n8k16 with f16 operands and fp32 accumulation.
 //
-// An E4M3 byte holding a value b in 0..15 is exactly b * 2^-9 (subnormals for
-// b < 8, exponent 1 above), so the unpacked nibbles feed the MMA with no table:
-//   A (weights): codes c, one byte each            -> c * 2^-9
-//   B (tokens):  u = q + 8 = nibble ^ 8, one byte   -> u * 2^-9
-//   B column OC: all ones                           -> 2^-9
-// and the fp32 accumulator of one 128-wide group holds, exactly,
-//   D = sum u c * 2^-18   and   C = sum c * 2^-18 (column OC).
-// Then I = sum q (c - z) = sum u c - 8 sum c - z qs, all integers below 2^15:
-//   I = fmaf(-z, qs, fmaf(D, 2^18, -8 C 2^18)) exactly in fp32.
-// Each thread loads 16 bytes (32 codes) of two rows per group; the k order
-// inside the MMA is permuted identically on A and B (even k then odd k of
-// every 8), so unpacking is two logic operations per word.  Warps split the
-// groups of a 16-row tile; one thread per (row, token) folds in order.
+// OR-ing a code into the mantissa of the f16 value 1024 (bits 0x6400) gives
+// 1024 + c exactly when the code sits in bits 0..3 of a half, and 1024 + 16 c
+// when it sits in bits 4..7, so one logic operation turns a weight word (codes
+// c0..c7 in nibbles 0..7) into an f16 pair:
+//   nibbles (0, 4) -> (1024 + c0, 1024 + c4)
+//   nibbles (1, 5) -> (1024 + 16 c1, 1024 + 16 c5)
+// and the word shifted right by 8 gives nibbles (2, 6) and (3, 7) the same
+// way.  The token operand carries q opposite the first kind and q / 16
+// opposite the second (both exact in f16), so every product is an integer:
+//   (1024 + c) q = 1024 q + c q,      (1024 + 16 c) q / 16 = 64 q + c q.
+// The accumulator starts at -(1024 Q_even + 64 Q_odd) (Q_even / Q_odd: sums
+// of q over the even / odd k of the group), so after the group's MMAs it holds
+// exactly D = sum_k c q (every partial sum an integer below 2^20), and
+//   I = sum_k q (c - z) = D - z qs
+// exactly in fp32.  The k order inside the MMA is one permutation applied to
+// both operands, so each thread's 16-byte weight loads (32 codes of rows r
+// and r + 8) feed its A fragments directly.  Token fragments (f16 pairs) and
+// the per-group offsets are built once per CTA in shared memory.
+//
+// Work split: persistent CTAs over 16-row tiles; an item is a tile and a pair
+// of adjacent groups; the 8 warps of a CTA split a tile's pairs; each tile's
+// group integers go to shared memory and one warp folds them in ascending
+// group order while the others start the next tile (double-buffered).
 // ---------------------------------------------------------------------------
-namespace mmak {
+namespace hm {
 
-constexpr int kThreads = 256;
 constexpr int kWarps = 8;
-constexpr int kPrefetch = 4;           // groups in flight per warp
+constexpr int kThreads = kWarps * 32;
 
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Persistent over 16-row tiles.  smem: actf uint2 [MT][G][16] (B fragments),
-// I float [2][G][16][MT] (double buffer), s float [2][G][16], sx float [MT][G],
-// qs float [MT][G].  Warp w owns groups w, w + 8, ...; per warp the (tile,
-// group) items form one sequence, so the prefetch ring runs across tiles.
-// After a tile, one warp folds it (ascending groups) while the others start
-// the next tile; the next barrier orders the fold before its buffer is reused.
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 2)
-    w4a4_mma_gemv_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx,
-                         const int32_t *__restrict__ qs, const uint8_t *__restrict__ packed,
-                         const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
-                         int32_t *__restrict__ dbg_I) {
-    constexpr int OC = MT == 1 ? 1 : 7;          // the all-ones B column
+// one weight word -> (c0, c4), (16 c1, 16 c5), (c2, c6), (16 c3, 16 c7), each + 1024
+__device__ __forceinline__ void codes_f16(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t magic = 0x64006400u;
+    p[0] = (w & 0x000F000Fu) | magic;
+    p[1] = (w & 0x00F000F0u) | magic;
+    const uint32_t t = w >> 8;
+    p[2] = (t & 0x000F000Fu) | magic;
+    p[3] = (t & 0x00F000F0u) | magic;
+}
+
+// one group of a 16-row tile: 8 MMAs over the thread's 4 words of rows r, r + 8
+__device__ __forceinline__ void group_mma(float (&d)[4], const uint4 &wr0, const uint4 &wr1, const uint4 *bf) {
+    const uint32_t w0[4] = {wr0.x, wr0.y, wr0.z, wr0.w}, w1[4] = {wr1.x, wr1.y, wr1.z, wr1.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint4 b = bf[u * 4];
+        uint32_t a0[4], a1[4];
+        codes_f16(w0[u], a0);
+        codes_f16(w1[u], a1);
+        mma_f16_16816(d, a0[0], a1[0], a0[1], a1[1], b.x, b.y);
+        mma_f16_16816(d, a0[2], a1[2], a0[3], a1[3], b.z, b.w);
+    }
+}
+
+__device__ __forceinline__ uint32_t f16_pair(float lo, float hi) {
+    return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+}
+
+// signed 4-bit activation code i of a word, as a float
+__device__ __forceinline__ float act_code(uint32_t w, int i) {
+    return (float)((int32_t)(w << (28 - 4 * i)) >> 28);
+}
+
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// shared memory: token fragments uint4 [MT + 1][G * 16 + 4] (padded per
+// token; slot MT stays zero for the lanes of absent tokens), {offset, qs}
+// float2 [G][MT], sx float [MT][G], I float [2][G][16][MT], scale words
+// uint32 [2][G][16]
+inline size_t smem_bytes(int MT, int K) {
+    const size_t G = (size_t)K / kGroup;
+    return (size_t)(MT + 1) * (G * 16 + 4) * 16 + (size_t)MT * G * 8 + (size_t)MT * G * 4 + 2 * G * 16 * MT * 4 +
+           2 * G * 16 * 4;
+}
+
+// One item: a 16-row tile and a pair of adjacent groups (g0, g0 + 1), the
+// thread's 16-byte pieces of rows r, r + 8 and their scale words.
+struct Item {
+    uint4 w00, w01, w10, w11;     // [row r / r + 8][group g0 / g0 + 1]
+    uint32_t z00, z01, z10, z11;
+};
+
+// kPrefetch: items in flight per warp; kMinBlocks: CTAs per SM the register
+// budget is sized for
+template <int MT, int kPrefetch, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+    w4a4_hmma_gemv_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx,
+                          const int32_t *__restrict__ qs, const uint8_t *__restrict__ packed,
+                          const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
+                          int32_t *__restrict__ dbg_I) {
+    static_assert(MT >= 1 && MT <= 8 && (MT == 1 || MT % 2 == 0), "one n8 block of tokens");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int G = K / kGroup;
-    uint2 *actf = reinterpret_cast<uint2 *>(smem_raw);
-    float *ibuf = reinterpret_cast<float *>(actf + (size_t)MT * G * 16);
-    float *sbuf = ibuf + (size_t)2 * G * 16 * MT;
-    float *sxs = sbuf + (size_t)2 * G * 16;
-    float *qss = sxs + (size_t)MT * G;
+    const int P = (G + 1) / 2;                                   // group pairs per row
+    const size_t tstride = (size_t)G * 16 + 4;
+    uint4 *bfr = reinterpret_cast<uint4 *>(smem_raw);
+    float2 *oq = reinterpret_cast<float2 *>(bfr + (size_t)(MT + 1) * tstride);
+    float *sxs = reinterpret_cast<float *>(oq + (size_t)MT * G);
+    float *ibuf = sxs + (size_t)MT * G;
+    uint32_t *sbuf = reinterpret_cast<uint32_t *>(ibuf + (size_t)2 * G * 16 * MT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qr = lane >> 2, qc = lane & 3;
     const int tok0 = blockIdx.y * MT;
     const int n_tiles = (N + 15) / 16;
-    const size_t row_u4 = (size_t)K / 32;
-    const uint4 *wbase = reinterpret_cast<const uint4 *>(packed) + qc;
-    const int ng = warp < G ? (G - warp + kWarps - 1) / kWarps : 0;     // this warp's groups per tile
-    const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    const int n_items = ng * my_tiles;
+    const size_t row_bytes = (size_t)K / 2;
+    const int ngw = warp < P ? (P - warp + kWarps - 1) / kWarps : 0;   // this warp's pairs per tile
+    const int my_tiles = (int)blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int n_items = ngw * my_tiles;
+    // scale words of a pair in one 8-byte load when every pair is complete and aligned
+    const bool z64 = (G % 2 == 0) && ((reinterpret_cast<uintptr_t>(sz) & 7) == 0);
 
-    // item cursor -> (tile, group); advanced incrementally, no division
-    struct Cursor {
-        int step, gi;
+    // producer cursor: tile step, pair index and the tile's row pointers
+    // (rows past N read row 0; their results are never stored)
+    struct Prod {
+        int step, j;
+        const uint8_t *p0, *p1;
+        const uint32_t *z0, *z1;
     };
-    auto load_item = [&](const Cursor &c, uint4 &wa, uint4 &wb, uint32_t &za, uint32_t &zb) {
-        const int tile = blockIdx.x + c.step * gridDim.x, g = warp + c.gi * kWarps;
-        const int r0 = tile * 16 + qr, r1 = r0 + 8;
-        const bool v0 = r0 < N, v1 = r1 < N;
-        wa = __ldg(wbase + (size_t)(v0 ? r0 : 0) * row_u4 + g * 4);
-        wb = __ldg(wbase + (size_t)(v1 ? r1 : 0) * row_u4 + g * 4);
-        za = v0 ? __ldg(sz + (size_t)r0 * G + g) : 0u;
-        zb = v1 ? __ldg(sz + (size_t)r1 * G + g) : 0u;
+    auto set_tile = [&](Prod &c) {
+        const int r0 = (blockIdx.x + c.step * gridDim.x) * 16 + qr, r1 = r0 + 8;
+        const int s0 = r0 < N ? r0 : 0, s1 = r1 < N ? r1 : 0;
+        c.p0 = packed + (size_t)s0 * row_bytes + qc * 16;
+        c.p1 = packed + (size_t)s1 * row_bytes + qc * 16;
+        c.z0 = sz + (size_t)s0 * G;
+        c.z1 = sz + (size_t)s1 * G;
     };
-    auto advance = [&](Cursor &c) {
-        if (++c.gi == ng) {
-            c.gi = 0;
+    auto load_item = [&](const Prod &c, Item &x) {
+        const int g0 = 2 * (warp + c.j * kWarps);
+        const int d1 = g0 + 1 < G ? 1 : 0;                       // an odd last group pairs with itself
+        const uint4 *a = reinterpret_cast<const uint4 *>(c.p0 + (size_t)g0 * 64);
+        const uint4 *b = reinterpret_cast<const uint4 *>(c.p1 + (size_t)g0 * 64);
+        x.w00 = ldg_stream(a);
+        x.w01 = ldg_stream(a + d1 * 4);
+        x.w10 = ldg_stream(b);
+        x.w11 = ldg_stream(b + d1 * 4);
+        if (z64) {
+            const uint2 za = __ldg(reinterpret_cast<const uint2 *>(c.z0 + g0));
+            const uint2 zb = __ldg(reinterpret_cast<const uint2 *>(c.z1 + g0));
+            x.z00 = za.x;
+            x.z01 = za.y;
+            x.z10 = zb.x;
+            x.z11 = zb.y;
+        } else {
+            x.z00 = __ldg(c.z0 + g0);
+            x.z01 = __ldg(c.z0 + g0 + d1);
+            x.z10 = __ldg(c.z1 + g0);
+            x.z11 = __ldg(c.z1 + g0 + d1);
+        }
+    };
+    auto advance_prod = [&](Prod &c) {
+        if (++c.j == ngw) {
+            c.j = 0;
             ++c.step;
+            set_tile(c);
         }
     };
 
     pdl_launch_dependents();
     // immutable weights and scale words first
-    uint4 ra[kPrefetch], rb[kPrefetch];
-    uint32_t sa[kPrefetch], sb[kPrefetch];
-    Cursor pc = {0, 0};
+    Item ring[kPrefetch];
+    Prod pc = {0, 0, nullptr, nullptr, nullptr, nullptr};
+    set_tile(pc);
 #pragma unroll
     for (int p = 0; p < kPrefetch; ++p) {
         if (p < n_items) {
-            load_item(pc, ra[p], rb[p], sa[p], sb[p]);
-            advance(pc);
+            load_item(pc, ring[p]);
+            advance_prod(pc);
         }
     }
     pdl_wait();
 
-    // this CTA's tokens, once: B fragments (u = q + 8 as bytes, even k then odd k), sx, qs
+    // token fragments, one thread per activation word (8 codes); the 16 words
+    // of a group sit in 16 consecutive lanes, which reduce the group offset
+    const int wpr = K / 8;
     const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
+    for (int base = 0; base < MT * wpr; base += kThreads) {
+        const int i = base + threadIdx.x;
+        const bool valid = i < MT * wpr;
+        const int t = valid ? i / wpr : 0, wi = i - t * wpr;
         const int m = tok0 + t;
-        for (int i = threadIdx.x; i < G * 16; i += kThreads) {
-            const uint32_t w = m < M ? xw[(size_t)m * (K / 8) + i] ^ 0x88888888u : 0u;
-            actf[(size_t)t * G * 16 + i] = make_uint2(w & 0x0F0F0F0Fu, (w >> 4) & 0x0F0F0F0Fu);
+        const uint32_t w = valid && m < M ? xw[(size_t)m * wpr + wi] : 0u;
+        float q[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = act_code(w, e);
+        float part = 1024.0f * ((q[0] + q[2]) + (q[4] + q[6])) + 64.0f * ((q[1] + q[3]) + (q[5] + q[7]));
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (valid) {
+            const int g = wi >> 4, qcw = (wi >> 2) & 3, u = wi & 3;
+            bfr[(size_t)t * tstride + (g * 4 + u) * 4 + qcw] =
+                make_uint4(f16_pair(q[0], q[4]), f16_pair(q[1] * 0.0625f, q[5] * 0.0625f), f16_pair(q[2], q[6]),
+                           f16_pair(q[3] * 0.0625f, q[7] * 0.0625f));
+            if ((wi & 15) == 0) oq[g * MT + t].x = part;
         }
-        for (int g = threadIdx.x; g < G; g += kThreads) {
-            sxs[t * G + g] = m < M ? sx[(size_t)m * G + g] : 0.0f;
-            qss[t * G + g] = m < M ? (float)qs[(size_t)m * G + g] : 0.0f;
-        }
+    }
+    for (int i = threadIdx.x; i < (int)tstride; i += kThreads) bfr[(size_t)MT * tstride + i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < MT * G; i += kThreads) {
+        const int t = i / G, g = i - t * G, m = tok0 + t;
+        oq[g * MT + t].y = m < M ? (float)qs[(size_t)m * G + g] : 0.0f;
+        sxs[i] = m < M ? sx[(size_t)m * G + g] : 0.0f;
     }
     __syncthreads();
 
-    const bool tok_row = qr < MT && tok0 + qr < M;     // this thread feeds a real token column
-    const int tq = qr < MT ? qr : 0;
-    const float two18 = 262144.0f;
+    // lanes of absent token columns read the zero slot
+    const uint4 *brow = bfr + (size_t)(qr < MT ? qr : MT) * tstride + qc;
+    // this lane's D columns are tokens 2 qc, 2 qc + 1 (clamped for the
+    // offset loads; columns past MT are never stored)
+    const int tq = MT == 1 ? 0 : (2 * qc < MT ? 2 * qc : 0);
 
     // end of tile `step`: every warp arrives once per tile; then one warp folds it
     auto tile_done = [&](int step) {
@@ -145,112 +259,104 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (warp != (step & (kWarps - 1))) return;
         const int tile = blockIdx.x + step * gridDim.x;
         const float *ib = ibuf + (size_t)(step & 1) * G * 16 * MT;
-        const float *sbb = sbuf + (size_t)(step & 1) * G * 16;
+        const uint32_t *sbb = sbuf + (size_t)(step & 1) * G * 16;
         for (int p = lane; p < 16 * MT; p += 32) {
             const int r = p / MT, t = p - (p / MT) * MT, n = tile * 16 + r, m = tok0 + t;
             if (n >= N || m >= M) continue;
+            const float *ip = ib + (size_t)r * MT + t;
+            const uint32_t *sp = sbb + r;
+            const float *xp = sxs + (size_t)t * G;
             float acc = 0.0f;
-            for (int g = 0; g < G; ++g) {
-                const float I = ib[((size_t)g * 16 + r) * MT + t];
-                acc = __fmaf_rn(I, __fmul_rn(sxs[t * G + g], sbb[(size_t)g * 16 + r]), acc);
-                if (dbg_I) dbg_I[((size_t)m * N + n) * G + g] = (int32_t)I;
-            }
+#pragma unroll 4
+            for (int g = 0; g < G; ++g)
+                acc = __fmaf_rn(ip[(size_t)g * 16 * MT], __fmul_rn(xp[g], half_lo(sp[g * 16])), acc);
             y[(size_t)m * ldy + n] = float_to_bf16_bits(acc);
+            if (dbg_I)
+                for (int g = 0; g < G; ++g) dbg_I[((size_t)m * N + n) * G + g] = (int32_t)ip[(size_t)g * 16 * MT];
         }
     };
 
-    Cursor cc = {0, 0};
-    int cur = 0;                                          // tile step being produced
+    // group g: D starts at minus the token offsets, so after the MMAs
+    // D = sum c q and I = D - z qs (rows qr, qr + 8 x tokens 2 qc, 2 qc + 1)
+    auto group = [&](const uint4 &wr0, const uint4 &wr1, uint32_t za, uint32_t zb, int g, float *ib,
+                     uint32_t *sbb) {
+        float d[4];
+        float qs0, qs1;
+        if (MT == 1) {
+            const float2 o = oq[g];
+            d[0] = d[1] = d[2] = d[3] = -o.x;
+            qs0 = qs1 = o.y;
+        } else {
+            const float4 o = *reinterpret_cast<const float4 *>(oq + g * MT + tq);
+            d[0] = d[2] = -o.x;
+            d[1] = d[3] = -o.z;
+            qs0 = o.y;
+            qs1 = o.w;
+        }
+        group_mma(d, wr0, wr1, brow + (size_t)g * 16);
+        const float zfa = half_hi(za), zfb = half_hi(zb);
+        if (2 * qc < MT) {
+            float *i0 = ib + ((size_t)g * 16 + qr) * MT + 2 * qc;
+            float *i1 = i0 + 8 * MT;
+            i0[0] = __fmaf_rn(-zfa, qs0, d[0]);
+            i1[0] = __fmaf_rn(-zfb, qs0, d[2]);
+            if (MT > 1) {
+                i0[1] = __fmaf_rn(-zfa, qs1, d[1]);
+                i1[1] = __fmaf_rn(-zfb, qs1, d[3]);
+            }
+        }
+        if (qc == 0) {
+            sbb[(size_t)g * 16 + qr] = za;
+            sbb[(size_t)g * 16 + qr + 8] = zb;
+        }
+    };
+
+    int cj = 0, cstep = 0;                                 // consumer cursor
+    int cur = 0;                                           // tile step being produced
     for (int base = 0; base < n_items; base += kPrefetch) {
 #pragma unroll
         for (int p = 0; p < kPrefetch; ++p) {
             const int it = base + p;
             if (it >= n_items) break;
-            if (cc.step != cur) {                         // this warp's first item of the next tile
+            if (cstep != cur) {                            // this warp's first item of the next tile
                 tile_done(cur);
-                cur = cc.step;
+                cur = cstep;
             }
-            const int g = warp + cc.gi * kWarps;
+            const int g0 = 2 * (warp + cj * kWarps);
             float *ib = ibuf + (size_t)(cur & 1) * G * 16 * MT;
-            float *sbb = sbuf + (size_t)(cur & 1) * G * 16;
-            const uint4 wa = ra[p], wb = rb[p];
-            const uint32_t za = sa[p], zb = sb[p];
+            uint32_t *sbb = sbuf + (size_t)(cur & 1) * G * 16;
+            const Item x = ring[p];
             if (it + kPrefetch < n_items) {
-                load_item(pc, ra[p], rb[p], sa[p], sb[p]);
-                advance(pc);
+                load_item(pc, ring[p]);
+                advance_prod(pc);
             }
-            uint32_t bf0[4], bf1[4];
-            if (tok_row) {
-                const uint4 *ap = reinterpret_cast<const uint4 *>(actf + ((size_t)tq * G + g) * 16 + qc * 4);
-                const uint4 f01 = ap[0], f23 = ap[1];
-                bf0[0] = f01.x; bf1[0] = f01.y; bf0[1] = f01.z; bf1[1] = f01.w;
-                bf0[2] = f23.x; bf1[2] = f23.y; bf0[3] = f23.z; bf1[3] = f23.w;
-            } else {
-                const uint32_t one = qr == OC ? 0x01010101u : 0u;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) bf0[j] = bf1[j] = one;
+            group(x.w00, x.w10, x.z00, x.z10, g0, ib, sbb);
+            if (g0 + 1 < G) group(x.w01, x.w11, x.z01, x.z11, g0 + 1, ib, sbb);
+            if (++cj == ngw) {
+                cj = 0;
+                ++cstep;
             }
-            const uint32_t wa_[4] = {wa.x, wa.y, wa.z, wa.w}, wb_[4] = {wb.x, wb.y, wb.z, wb.w};
-            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                mma_e4m3_16832(d, wa_[j] & 0x0F0F0F0Fu, wb_[j] & 0x0F0F0F0Fu, (wa_[j] >> 4) & 0x0F0F0F0Fu,
-                               (wb_[j] >> 4) & 0x0F0F0F0Fu, bf0[j], bf1[j]);
-            // D: rows (qr, qr + 8) x columns (2 qc, 2 qc + 1); C from column OC
-            float c_a, c_b;
-            if (MT == 1) {
-                c_a = d[1];
-                c_b = d[3];
-            } else {
-                c_a = __shfl_sync(0xffffffffu, d[1], (lane & ~3) | 3);
-                c_b = __shfl_sync(0xffffffffu, d[3], (lane & ~3) | 3);
-            }
-            if (2 * qc < MT) {
-                const float ia = c_a * (-8.0f * two18), ibv = c_b * (-8.0f * two18);   // exact
-                const float zfa = __half2float(__ushort_as_half((uint16_t)(za >> 16)));
-                const float zfb = __half2float(__ushort_as_half((uint16_t)(zb >> 16)));
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = 2 * qc + e;
-                    if (t < MT && t != OC) {
-                        const float q_s = qss[t * G + g];
-                        ib[((size_t)g * 16 + qr) * MT + t] = __fmaf_rn(-zfa, q_s, __fmaf_rn(d[e], two18, ia));
-                        ib[((size_t)g * 16 + qr + 8) * MT + t] = __fmaf_rn(-zfb, q_s, __fmaf_rn(d[2 + e], two18, ibv));
-                    }
-                }
-            }
-            if (qc == 0) {
-                sbb[(size_t)g * 16 + qr] = __half2float(__ushort_as_half((uint16_t)(za & 0xFFFF)));
-                sbb[(size_t)g * 16 + qr + 8] = __half2float(__ushort_as_half((uint16_t)(zb & 0xFFFF)));
-            }
-            advance(cc);
         }
     }
-    // the last tile with items, then the remaining ones (warps without groups)
+    // the last tile with items, then the remaining ones (warps without pairs)
     for (; cur < my_tiles; ++cur) tile_done(cur);
 }
 
-template <int MT>
-size_t smem_bytes(int K) {
-    const int G = K / kGroup;
-    return (size_t)MT * G * 16 * sizeof(uint2) + (size_t)2 * G * 16 * MT * 4 + (size_t)2 * G * 16 * 4 +
-           (size_t)MT * G * 8;
-}
-
-template <int MT>
+template <int MT, int PF = 1, int MINB = 2>
 int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed, const uint32_t *sz, int M,
-           int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, cudaStream_t st) {
-    const size_t smem = smem_bytes<MT>(K);
-    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_mma_gemv_kernel<MT>), 8 + MT, 200 * 1024);
+           int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, cudaStream_t st, int ctas_per_sm = MINB) {
+    const size_t smem = smem_bytes(MT, K);
+    auto kern = w4a4_hmma_gemv_kernel<MT, PF, MINB>;
+    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 8 + MT, 200 * 1024);
     if (rc) return rc;
     const int n_tiles = (N + 15) / 16, token_tiles = (M + MT - 1) / MT;
-    const int per_col = std::max(1, 2 * sm_count() / token_tiles);
+    const int per_col = std::max(1, ctas_per_sm * sm_count() / token_tiles);
     dim3 grid((unsigned)std::min(n_tiles, per_col), (unsigned)token_tiles);
-    return launch_pdl("qspec_linear_w4a4", w4a4_mma_gemv_kernel<MT>, grid, dim3(kThreads), smem, st, xq, sx, qs,
-                      packed, sz, M, N, K, y, ldy, dbg_I);
+    return launch_pdl("qspec_linear_w4a4", kern, grid, dim3(kThreads), smem, st, xq, sx, qs, packed, sz, M, N, K, y,
+                      ldy, dbg_I);
 }
 
-}  // namespace mmak
+}  // namespace hm
 
 }  // namespace
 
@@ -271,18 +377,22 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
     if (rc) return rc;
     cudaStream_t st = as_cuda(stream);
     if (M > 32) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
-    constexpr size_t kMaxSmem = 200 * 1024;
-    if (M == 1 && mmak::smem_bytes<1>(K) <= kMaxSmem)
-        return mmak::launch<1>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (M == 2 && mmak::smem_bytes<2>(K) <= kMaxSmem)
-        return mmak::launch<2>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (M <= 4 && mmak::smem_bytes<4>(K) <= kMaxSmem)
-        return mmak::launch<4>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (mmak::smem_bytes<7>(K) <= kMaxSmem)
-        return mmak::launch<7>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (mmak::smem_bytes<4>(K) <= kMaxSmem)
-        return mmak::launch<4>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    if (mmak::smem_bytes<1>(K) <= kMaxSmem)
-        return mmak::launch<1>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-    return QSPEC_ERR_SHAPE;
+    // 3..8 tokens and at least one 128-row tile per SM: weights through TMA
+    // and TMEM, MMAs async (at 1-2 tokens the warp-MMA kernel below is faster)
+    if (M >= 3 && M <= 8 && (N + 127) / 128 >= sm_count()) {
+        rc = launch_w4a4_gemv_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
+        if (rc != QSPEC_ERR_SHAPE) return rc;
+    }
+    // tokens per CTA: up to 8 (one MMA column block), halved while two CTAs
+    // would not fit on an SM
+    constexpr size_t kTwoPerSm = 112 * 1024, kMaxSmem = 200 * 1024;
+    int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
+    while (mt > 1 && hm::smem_bytes(mt, K) > kTwoPerSm) mt /= 2;
+    if (hm::smem_bytes(mt, K) > kMaxSmem) return QSPEC_ERR_SHAPE;
+    switch (mt) {
+        case 1: return hm::launch<1>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+        case 2: return hm::launch<2>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+        case 4: return hm::launch<4>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+        default: return hm::launch<8>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+    }
 }

@@ -121,3 +121,47 @@ def test_prefill_m4096():
     dev = need_gpu()
     shapes = [("gate_proj", 14336, 4096), ("down_proj", 4096, 14336)]
     sampled_compare([4096], shapes, 4, dev)
+
+
+# ----------------------------------------------------------------- decode M, many row tiles
+# Shapes with at least one 128-row tile per SM take the tensor-memory GEMV
+# path at 3 <= M <= 8 (the warp-MMA kernel below that); a ragged last tile,
+# an odd group count and every token count class are covered.
+@pytest.mark.parametrize("M,K,seed", [(1, 1152, 20), (2, 2048, 21), (3, 1152, 22), (5, 2048, 23), (8, 1152, 24)])
+def test_decode_many_tiles_full_compare(M, K, seed):
+    dev = need_gpu()
+    N = 19456 + 77
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100, outlier_frac=0.01)
+    (y4, I), xqo, sxo = run_w4a4(x, packed, sz, dev)
+    y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert np.array_equal(I.cpu().numpy(), Io)
+    assert np.array_equal(bits(y4), y4o)
+
+
+def test_decode_many_tiles_extreme():
+    """|I| = 128 * 7 * 15 in both signs on the decode path."""
+    dev = need_gpu()
+    M, N, K = 3, 19456 + 5, 256
+    G = K // 128
+    rng = np.random.default_rng(3)
+    codes = torch.from_numpy(rng.choice([0, 15], (N, K)).astype(np.uint8))
+    z = torch.from_numpy(rng.choice([0.0, 15.0], (N, G))).to(torch.float16)
+    s = torch.ones((N, G), dtype=torch.float16)
+    x = torch.from_numpy(rng.choice([-7.0, 7.0], (M, K)).astype(np.float32))
+    codes[0], codes[1], codes[N - 1] = 15, 0, 15
+    z[0], z[1], z[N - 1] = 0.0, 15.0, 0.0
+    x[0] = 7.0
+    x = x.to(torch.bfloat16)
+    packed, sz = q.pack_weights(codes.to(dev), s.to(dev), z.to(dev))
+    rc, po, szo = oracle.pack_weights(codes.numpy(), bits(s), bits(z))
+    (y4, I), xqo, sxo = run_w4a4(x, packed, sz, dev)
+    y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert Io[0, 0].max() == 128 * 7 * 15 and Io[0, 1].min() == -128 * 7 * 15
+    assert np.array_equal(I.cpu().numpy(), Io) and np.array_equal(bits(y4), y4o)
+
+
+def test_lm_head_decode_m1_m4():
+    """The LM head (128256 x 4096) at draft M = 1 and M = 4, sampled outputs."""
+    dev = need_gpu()
+    sampled_compare([1, 4], [("lm_head", 128256, 4096)], 6, dev, outliers=0.01, w4a16=False, points=1024)
