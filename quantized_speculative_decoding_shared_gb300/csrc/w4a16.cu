@@ -6,23 +6,25 @@
 // W^ = s (W_INT4 - z); "QSPEC structure": the verify pass over the gamma + 1
 // candidate rows of every sequence.
 //
-// Small-M path (decode verify, M = B (gamma + 1) <= 16 per token tile): warp
-// MMA m16n8k16 bf16 with fp32 accumulation.  The weight tile is the MMA's A
-// operand (16 output channels x 16 k), the activations its B operand (16 k x 8
-// tokens).  Dequantisation happens in registers and is split so the tensor
-// core sees exact small integers:
+// Small-M path (decode verify, M <= 16): warp MMA m16n8k16 bf16 with fp32
+// accumulation; the weight tile is the MMA's A operand (16 output channels x
+// 16 k), the tokens its B operand (16 k x 8 tokens).  Dequantisation is split
+// so the tensor core sees exact small integers:
 //   - a code c becomes the bf16 value 128 + c by OR-ing it into the mantissa
 //     of 128.0 (bits 0x4300 | c); no conversion instruction is needed;
-//   - per group g, D = sum_k (128 + c_k) x_k is accumulated by the MMA, and the
-//     epilogue applies y += s_g (D - (128 + z_g) X_g), X_g = sum_{k in g} x_k,
-//     which equals sum_k s_g (c_k - z_g) x_k, the definition.
-// The k order inside the MMA is permuted identically on A and B so that each
-// thread's 16-byte weight load and 16-byte activation loads feed its fragments
-// without shuffles (a dot product does not depend on the k order).
+//   - per group g the accumulator starts at -128 X_g (X_g = sum of the
+//     group's activations), so the MMAs leave D = sum_k c_k x_k, and the
+//     epilogue adds s_g (D - z_g X_g), which is sum_k s_g (c_k - z_g) x_k.
+// The k order inside the MMA is one permutation applied to both operands:
+// the tokens' bf16 pairs are permuted once per CTA into shared memory, and
+// each thread's 16-byte weight loads feed its A fragments directly.
 //
-// HBM-bound for M <= 16: 0.5 byte of weight + 4/128 byte of scale/zero per
-// weight dominates; each CTA streams 16-row tiles, split over its 8 warps by
-// group, with a 4-group prefetch per warp.
+// Work split as in the small-M W4A4 kernel: persistent CTAs over 16-row
+// tiles; an item is a tile and a pair of adjacent groups; the 8 warps split a
+// tile's pairs and keep fp32 partial sums in registers; at the end of a tile
+// the partials go to shared memory (double-buffered) and one warp adds the 8
+// warps' partials in a fixed order and stores bf16.  Larger M: tcgen05
+// (w4a16_tc.cu).
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -32,22 +34,19 @@ namespace qspec {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
 
-__device__ __forceinline__ void mma_bf16_16816(float &d0, float &d1, float &d2, float &d3,
-                                               uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Eight codes of one 32-bit word (k0..k7 in nibbles 0..7) -> four bf16x2 of
-// (128 + c): (k0,k4), (k1,k5), (k2,k6), (k3,k7).
-__device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t p[4]) {
+// one weight word (codes c0..c7 in nibbles 0..7) -> bf16 pairs of 128 + c:
+// (c0, c4), (c1, c5), (c2, c6), (c3, c7)
+__device__ __forceinline__ void codes_bf16(uint32_t w, uint32_t (&p)[4]) {
     const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;
     p[0] = (w & mask) | magic;
     p[1] = ((w >> 4) & mask) | magic;
@@ -55,13 +54,8 @@ __device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t p[4]) {
     p[3] = ((w >> 12) & mask) | magic;
 }
 
-// Eight bf16 activations x0..x7 (four 32-bit words) -> the same pairing.
-__device__ __forceinline__ void acts_to_pairs(uint4 v, uint32_t p[4]) {
-    p[0] = __byte_perm(v.x, v.z, 0x5410);
-    p[1] = __byte_perm(v.x, v.z, 0x7632);
-    p[2] = __byte_perm(v.y, v.w, 0x5410);
-    p[3] = __byte_perm(v.y, v.w, 0x7632);
-}
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
 
 __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
     uint4 r;
@@ -71,197 +65,270 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
     return r;
 }
 
-// NT token tiles of 8 per CTA (NT = 1 or 2).  grid.x: persistent over 16-row
-// tiles; grid.y: token tiles of 8 * NT.
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 2)
-    w4a16_mma_kernel(const uint16_t *__restrict__ x, int ldx, const uint8_t *__restrict__ packed,
-                     const uint32_t *__restrict__ sz, int M, int N, int K,
-                     uint16_t *__restrict__ y, int ldy) {
-    extern __shared__ float smem[];
+// shared memory: token fragments uint4 [slots][G * 16 + 4] (bf16 pairs, k
+// permuted, padded so two tokens of a lane phase hit different banks; slots =
+// min(MT, M), the most tokens a CTA holds), 16 zero uint4 for the lanes of
+// absent tokens, X float [G][MT], partial sums float [2][warps][16][MT]
+inline size_t smem_bytes(int MT, int M, int K, int warps) {
+    const size_t G = (size_t)K / kGroup, slots = (size_t)std::min(MT, M);
+    return slots * (G * 16 + 4) * 16 + 16 * 16 + (size_t)G * MT * 4 + (size_t)2 * warps * 16 * MT * 4;
+}
+
+// One item: a 16-row tile and a pair of adjacent groups (g0, g0 + 1), the
+// thread's 16-byte pieces of rows r, r + 8 and their scale words.
+struct Item {
+    uint4 w00, w01, w10, w11;     // [row r / r + 8][group g0 / g0 + 1]
+    uint32_t z00, z01, z10, z11;
+};
+
+// kWarps: 8 (two CTAs per SM) or 16 (one CTA per SM when the token
+// fragments are large)
+template <int MT, int kPrefetch, int kWarps>
+__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
+    w4a16_hmma_gemv_kernel(const uint16_t *__restrict__ x, int ldx, const uint8_t *__restrict__ packed,
+                           const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y,
+                           int ldy) {
+    static_assert(MT >= 1 && MT <= 8 && (MT == 1 || MT % 2 == 0), "one n8 block of tokens");
+    constexpr int kThreads = kWarps * 32;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     const int G = K / kGroup;
-    float *xg = smem;                                   // [NT*8][G]   group sums of x
-    float *red = smem + NT * 8 * G;                     // [kWarps][NT*8][16]
+    const int P = (G + 1) / 2;
+    const size_t tstride = (size_t)G * 16 + 4;
+    uint4 *bfr = reinterpret_cast<uint4 *>(smem_raw);
+    uint4 *zero = bfr + (size_t)min(MT, M) * tstride;
+    float *xg = reinterpret_cast<float *>(zero + 16);
+    float *red = xg + (size_t)G * MT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qr = lane >> 2, qc = lane & 3;
-    const int tok0 = blockIdx.y * 8 * NT;
+    const int tok0 = blockIdx.y * MT;
     const int n_tiles = (N + 15) / 16;
     const size_t row_bytes = (size_t)K / 2;
-    constexpr int kPrefetch = NT == 1 ? 4 : 2;   // groups in flight per warp
+    const int ngw = warp < P ? (P - warp + kWarps - 1) / kWarps : 0;   // this warp's pairs per tile
+    const int my_tiles = (int)blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int n_items = ngw * my_tiles;
+    const bool z64 = (G % 2 == 0) && ((reinterpret_cast<uintptr_t>(sz) & 7) == 0);
+
+    // producer cursor: tile step, pair index and the tile's row pointers
+    // (rows past N read row 0; their results are never stored)
+    struct Prod {
+        int step, j;
+        const uint8_t *p0, *p1;
+        const uint32_t *z0, *z1;
+    };
+    auto set_tile = [&](Prod &c) {
+        const int r0 = (blockIdx.x + c.step * gridDim.x) * 16 + qr, r1 = r0 + 8;
+        const int s0 = r0 < N ? r0 : 0, s1 = r1 < N ? r1 : 0;
+        c.p0 = packed + (size_t)s0 * row_bytes + qc * 16;
+        c.p1 = packed + (size_t)s1 * row_bytes + qc * 16;
+        c.z0 = sz + (size_t)s0 * G;
+        c.z1 = sz + (size_t)s1 * G;
+    };
+    auto load_item = [&](const Prod &c, Item &it) {
+        const int g0 = 2 * (warp + c.j * kWarps);
+        const int d1 = g0 + 1 < G ? 1 : 0;                       // an odd last group pairs with itself
+        const uint4 *a = reinterpret_cast<const uint4 *>(c.p0 + (size_t)g0 * 64);
+        const uint4 *b = reinterpret_cast<const uint4 *>(c.p1 + (size_t)g0 * 64);
+        it.w00 = ldg_stream(a);
+        it.w01 = ldg_stream(a + d1 * 4);
+        it.w10 = ldg_stream(b);
+        it.w11 = ldg_stream(b + d1 * 4);
+        if (z64) {
+            const uint2 za = __ldg(reinterpret_cast<const uint2 *>(c.z0 + g0));
+            const uint2 zb = __ldg(reinterpret_cast<const uint2 *>(c.z1 + g0));
+            it.z00 = za.x;
+            it.z01 = za.y;
+            it.z10 = zb.x;
+            it.z11 = zb.y;
+        } else {
+            it.z00 = __ldg(c.z0 + g0);
+            it.z01 = __ldg(c.z0 + g0 + d1);
+            it.z10 = __ldg(c.z1 + g0);
+            it.z11 = __ldg(c.z1 + g0 + d1);
+        }
+    };
+    auto advance_prod = [&](Prod &c) {
+        if (++c.j == ngw) {
+            c.j = 0;
+            ++c.step;
+            set_tile(c);
+        }
+    };
 
     pdl_launch_dependents();
-    // prefetch ring over this warp's groups g = warp, warp + 8, ... of the
-    // first tile: weights are immutable, so this overlaps the previous kernel
-    uint4 ring0[kPrefetch], ring1[kPrefetch];
-    {
-        const int tile = blockIdx.x;
-        const int r0 = tile * 16 + qr, r1 = r0 + 8;
-        const uint4 *w0p = reinterpret_cast<const uint4 *>(packed + (size_t)(r0 < N ? r0 : 0) * row_bytes) + qc;
-        const uint4 *w1p = reinterpret_cast<const uint4 *>(packed + (size_t)(r1 < N ? r1 : 0) * row_bytes) + qc;
+    // immutable weights and scale words first
+    Item ring[kPrefetch];
+    Prod pc = {0, 0, nullptr, nullptr, nullptr, nullptr};
+    set_tile(pc);
 #pragma unroll
-        for (int j = 0; j < kPrefetch; ++j) {
-            int g = warp + j * kWarps;
-            if (tile < n_tiles && g < G) {
-                ring0[j] = ldg_stream(w0p + g * 4);
-                ring1[j] = ldg_stream(w1p + g * 4);
-            }
+    for (int p = 0; p < kPrefetch; ++p) {
+        if (p < n_items) {
+            load_item(pc, ring[p]);
+            advance_prod(pc);
         }
     }
     pdl_wait();
 
-    // group sums X_g of this CTA's tokens, one (token, group) per thread at a time
-    for (int i = threadIdx.x; i < NT * 8 * G; i += kThreads) {
-        const int t = i / G, g = i % G, m = tok0 + t;
-        float s = 0.0f;
-        if (m < M) {
-            const uint4 *xp = reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup);
-            uint4 v[16];
+    // token fragments, one thread per 8 activations; the 16 words of a group
+    // sit in 16 consecutive lanes, which reduce the group sum X_g
+    const int mt_real = min(MT, M - tok0);
+    const int wpr = K / 8;
+    constexpr int kBatch = 4;                              // loads in flight per thread
+    for (int base = 0; base < mt_real * wpr; base += kBatch * kThreads) {
+        uint4 v[kBatch];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) v[u] = __ldg(xp + u);
-            float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                part[0] += __uint_as_float(v[u].x << 16) + __uint_as_float(v[u].x & 0xFFFF0000u);
-                part[1] += __uint_as_float(v[u].y << 16) + __uint_as_float(v[u].y & 0xFFFF0000u);
-                part[2] += __uint_as_float(v[u].z << 16) + __uint_as_float(v[u].z & 0xFFFF0000u);
-                part[3] += __uint_as_float(v[u].w << 16) + __uint_as_float(v[u].w & 0xFFFF0000u);
-            }
-            s = (part[0] + part[1]) + (part[2] + part[3]);
+        for (int b = 0; b < kBatch; ++b) {
+            const int i = base + b * kThreads + threadIdx.x;
+            const int t = i / wpr, wi = i - t * wpr;
+            v[b] = i < mt_real * wpr ? *reinterpret_cast<const uint4 *>(x + (size_t)(tok0 + t) * ldx + (size_t)wi * 8)
+                                     : make_uint4(0u, 0u, 0u, 0u);
         }
-        xg[t * G + g] = s;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int i = base + b * kThreads + threadIdx.x;
+            const bool valid = i < mt_real * wpr;
+            const int t = valid ? i / wpr : 0, wi = i - t * wpr;
+            const uint4 w = v[b];
+            float part = ((bf16_bits_to_float(w.x & 0xFFFF) + bf16_bits_to_float(w.x >> 16)) +
+                          (bf16_bits_to_float(w.y & 0xFFFF) + bf16_bits_to_float(w.y >> 16))) +
+                         ((bf16_bits_to_float(w.z & 0xFFFF) + bf16_bits_to_float(w.z >> 16)) +
+                          (bf16_bits_to_float(w.w & 0xFFFF) + bf16_bits_to_float(w.w >> 16)));
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (valid) {
+                const int g = wi >> 4, qcw = (wi >> 2) & 3, u = wi & 3;
+                bfr[(size_t)t * tstride + (g * 4 + u) * 4 + qcw] =
+                    make_uint4(__byte_perm(w.x, w.z, 0x5410), __byte_perm(w.x, w.z, 0x7632),
+                               __byte_perm(w.y, w.w, 0x5410), __byte_perm(w.y, w.w, 0x7632));
+                if ((wi & 15) == 0) xg[g * MT + t] = part;
+            }
+        }
     }
+    for (int i = threadIdx.x; i < 16; i += kThreads) zero[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < G * MT; i += kThreads)
+        if (i % MT >= mt_real) xg[i] = 0.0f;
     __syncthreads();
 
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        const int r0 = tile * 16 + qr, r1 = r0 + 8;
-        const bool v0 = r0 < N, v1 = r1 < N;
-        const uint4 *w0p = reinterpret_cast<const uint4 *>(packed + (size_t)(v0 ? r0 : 0) * row_bytes) + qc;
-        const uint4 *w1p = reinterpret_cast<const uint4 *>(packed + (size_t)(v1 ? r1 : 0) * row_bytes) + qc;
+    // lanes of absent token columns read the zero words for every group
+    const bool present = qr < mt_real;
+    const uint4 *brow = present ? bfr + (size_t)qr * tstride + qc : zero + qc;
+    const int gstride = present ? 16 : 0;
+    // this lane's D columns are tokens 2 qc, 2 qc + 1 (clamped for the
+    // X loads; columns past MT are never stored)
+    const int tq = MT == 1 ? 0 : (2 * qc < MT ? 2 * qc : 0);
 
-        float acc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
-
-        if (tile != (int)blockIdx.x) {
-#pragma unroll
-            for (int j = 0; j < kPrefetch; ++j) {
-                int g = warp + j * kWarps;
-                if (g < G) {
-                    ring0[j] = ldg_stream(w0p + g * 4);
-                    ring1[j] = ldg_stream(w1p + g * 4);
-                }
-            }
-        }
-        // activation fragments of the warp's first group
-        uint4 xv[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int m = tok0 + nt * 8 + qr;
-            const uint4 *xp = reinterpret_cast<const uint4 *>(
-                x + (size_t)(m < M ? m : 0) * ldx + (size_t)warp * kGroup + qc * 32);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                xv[nt][u] = (m < M && warp < G) ? __ldg(xp + u) : make_uint4(0, 0, 0, 0);
-        }
-        for (int gb = warp; gb < G; gb += kPrefetch * kWarps) {
-#pragma unroll
-            for (int slot = 0; slot < kPrefetch; ++slot) {
-                const int g = gb + slot * kWarps;
-                if (g >= G) break;
-                uint4 wa = ring0[slot], wb = ring1[slot];
-                {
-                    int gn = g + kPrefetch * kWarps;
-                    if (gn < G) {
-                        ring0[slot] = ldg_stream(w0p + gn * 4);
-                        ring1[slot] = ldg_stream(w1p + gn * 4);
-                    }
-                }
-                // next group's activation fragments
-                uint4 xn[NT][4];
-                const int gx = g + kWarps;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int m = tok0 + nt * 8 + qr;
-                    const uint4 *xp = reinterpret_cast<const uint4 *>(
-                        x + (size_t)(m < M ? m : 0) * ldx + (size_t)(gx < G ? gx : 0) * kGroup + qc * 32);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        xn[nt][u] = (m < M && gx < G) ? __ldg(xp + u) : make_uint4(0, 0, 0, 0);
-                }
-                const uint32_t wr0[4] = {wa.x, wa.y, wa.z, wa.w};
-                const uint32_t wr1[4] = {wb.x, wb.y, wb.z, wb.w};
-
-                // this group's scale and zero point for rows r0, r1
-                uint32_t sz0 = v0 ? __ldg(sz + (size_t)r0 * G + g) : 0u;
-                uint32_t sz1 = v1 ? __ldg(sz + (size_t)r1 * G + g) : 0u;
-                float s0 = __half2float(__ushort_as_half((uint16_t)(sz0 & 0xFFFF)));
-                float s1 = __half2float(__ushort_as_half((uint16_t)(sz1 & 0xFFFF)));
-                float o0 = 128.0f + __half2float(__ushort_as_half((uint16_t)(sz0 >> 16)));
-                float o1 = 128.0f + __half2float(__ushort_as_half((uint16_t)(sz1 >> 16)));
-
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint32_t pa0[4], pa1[4], pb[4];
-                        codes_to_bf16x2(wr0[u], pa0);
-                        codes_to_bf16x2(wr1[u], pa1);
-                        acts_to_pairs(xv[nt][u], pb);
-                        mma_bf16_16816(d[0], d[1], d[2], d[3], pa0[0], pa1[0], pa0[1], pa1[1], pb[0], pb[1]);
-                        mma_bf16_16816(d[0], d[1], d[2], d[3], pa0[2], pa1[2], pa0[3], pa1[3], pb[2], pb[3]);
-                    }
-                    // D holds rows (qr, qr+8) x tokens (2qc, 2qc+1) of this tile
-                    const float X0 = xg[(nt * 8 + 2 * qc) * G + g];
-                    const float X1 = xg[(nt * 8 + 2 * qc + 1) * G + g];
-                    acc[nt][0] = __fmaf_rn(s0, __fmaf_rn(-o0, X0, d[0]), acc[nt][0]);
-                    acc[nt][1] = __fmaf_rn(s0, __fmaf_rn(-o0, X1, d[1]), acc[nt][1]);
-                    acc[nt][2] = __fmaf_rn(s1, __fmaf_rn(-o1, X0, d[2]), acc[nt][2]);
-                    acc[nt][3] = __fmaf_rn(s1, __fmaf_rn(-o1, X1, d[3]), acc[nt][3]);
-                }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) xv[nt][u] = xn[nt][u];
-            }
-        }
-
-        // reduce the 8 warps' partial sums and store bf16
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float *rw = red + (size_t)warp * NT * 8 * 16;
-            rw[(nt * 8 + 2 * qc) * 16 + qr] = acc[nt][0];
-            rw[(nt * 8 + 2 * qc + 1) * 16 + qr] = acc[nt][1];
-            rw[(nt * 8 + 2 * qc) * 16 + qr + 8] = acc[nt][2];
-            rw[(nt * 8 + 2 * qc + 1) * 16 + qr + 8] = acc[nt][3];
-        }
+    // end of tile `step`: partials are in red[step & 1]; one warp adds them
+    auto tile_done = [&](int step) {
         __syncthreads();
-        for (int i = threadIdx.x; i < NT * 8 * 16; i += kThreads) {
-            int t = i / 16, r = i % 16;
+        if (warp != (step & (kWarps - 1))) return;
+        const int tile = blockIdx.x + step * gridDim.x;
+        const float *rb = red + (size_t)(step & 1) * kWarps * 16 * MT;
+        for (int p = lane; p < 16 * MT; p += 32) {
+            const int r = p / MT, t = p - (p / MT) * MT, n = tile * 16 + r, m = tok0 + t;
+            if (n >= N || m >= M) continue;
             float sum = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) sum += red[(size_t)w * NT * 8 * 16 + i];
-            int m = tok0 + t, n = tile * 16 + r;
-            if (m < M && n < N) y[(size_t)m * ldy + n] = float_to_bf16_bits(sum);
+            for (int w = 0; w < kWarps; ++w) sum += rb[(size_t)w * 16 * MT + p];
+            y[(size_t)m * ldy + n] = float_to_bf16_bits(sum);
         }
-        __syncthreads();
+    };
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    auto flush = [&](int step) {                          // this warp's partials of tile `step`
+        float *rw = red + (size_t)(step & 1) * kWarps * 16 * MT + (size_t)warp * 16 * MT;
+        if (2 * qc < MT) {
+            rw[qr * MT + 2 * qc] = acc[0];
+            rw[(qr + 8) * MT + 2 * qc] = acc[2];
+            if (MT > 1) {
+                rw[qr * MT + 2 * qc + 1] = acc[1];
+                rw[(qr + 8) * MT + 2 * qc + 1] = acc[3];
+            }
+        }
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+    };
+
+    // group g: D starts at -128 X_g, so after the MMAs D = sum c x
+    auto group = [&](const uint4 &wr0, const uint4 &wr1, uint32_t za, uint32_t zb, int g) {
+        float X0, X1;
+        if (MT == 1) {
+            X0 = X1 = xg[g];
+        } else {
+            const float2 o = *reinterpret_cast<const float2 *>(xg + g * MT + tq);
+            X0 = o.x;
+            X1 = o.y;
+        }
+        float d[4] = {-128.0f * X0, -128.0f * X1, -128.0f * X0, -128.0f * X1};
+        const uint4 *bf = brow + (size_t)g * gstride;
+        const uint32_t w0[4] = {wr0.x, wr0.y, wr0.z, wr0.w}, w1[4] = {wr1.x, wr1.y, wr1.z, wr1.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint4 b = bf[u * 4];
+            uint32_t a0[4], a1[4];
+            codes_bf16(w0[u], a0);
+            codes_bf16(w1[u], a1);
+            mma_bf16_16816(d, a0[0], a1[0], a0[1], a1[1], b.x, b.y);
+            mma_bf16_16816(d, a0[2], a1[2], a0[3], a1[3], b.z, b.w);
+        }
+        const float sa = half_lo(za), zfa = half_hi(za), sb = half_lo(zb), zfb = half_hi(zb);
+        acc[0] = __fmaf_rn(sa, __fmaf_rn(-zfa, X0, d[0]), acc[0]);
+        acc[2] = __fmaf_rn(sb, __fmaf_rn(-zfb, X0, d[2]), acc[2]);
+        if (MT > 1) {
+            acc[1] = __fmaf_rn(sa, __fmaf_rn(-zfa, X1, d[1]), acc[1]);
+            acc[3] = __fmaf_rn(sb, __fmaf_rn(-zfb, X1, d[3]), acc[3]);
+        }
+    };
+
+    int cj = 0, cstep = 0;                                 // consumer cursor
+    int cur = 0;                                           // tile step being produced
+    for (int base = 0; base < n_items; base += kPrefetch) {
+#pragma unroll
+        for (int p = 0; p < kPrefetch; ++p) {
+            const int it = base + p;
+            if (it >= n_items) break;
+            if (cstep != cur) {                            // this warp's first item of the next tile
+                flush(cur);
+                tile_done(cur);
+                cur = cstep;
+            }
+            const int g0 = 2 * (warp + cj * kWarps);
+            const Item c = ring[p];
+            if (it + kPrefetch < n_items) {
+                load_item(pc, ring[p]);
+                advance_prod(pc);
+            }
+            group(c.w00, c.w10, c.z00, c.z10, g0);
+            if (g0 + 1 < G) group(c.w01, c.w11, c.z01, c.z11, g0 + 1);
+            if (++cj == ngw) {
+                cj = 0;
+                ++cstep;
+            }
+        }
+    }
+    // the last tile with items, then the remaining ones (warps without pairs)
+    for (; cur < my_tiles; ++cur) {
+        flush(cur);
+        tile_done(cur);
     }
 }
 
-template <int NT>
-int launch_w4a16(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N,
-                 int K, uint16_t *y, int ldy, cudaStream_t st) {
-    const int G = K / kGroup;
-    size_t smem = (size_t)(NT * 8 * G + kWarps * NT * 8 * 16) * sizeof(float);
-    if (smem > 48 * 1024) return QSPEC_ERR_SHAPE;   // K up to ~90k
-    const int n_tiles = (N + 15) / 16;
-    const int token_tiles = (M + 8 * NT - 1) / (8 * NT);
-    int per_col = std::max(1, 2 * sm_count() / token_tiles);
+template <int MT, int kWarps>
+int launch_w4a16_w(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
+                   uint16_t *y, int ldy, cudaStream_t st) {
+    const size_t smem = smem_bytes(MT, M, K, kWarps);
+    auto kern = w4a16_hmma_gemv_kernel<MT, 1, kWarps>;
+    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), (kWarps == 16 ? 48 : 24) + MT, 200 * 1024);
+    if (rc) return rc;
+    const int n_tiles = (N + 15) / 16, token_tiles = (M + MT - 1) / MT;
+    const int per_col = std::max(1, (16 / kWarps) * sm_count() / token_tiles);
     dim3 grid((unsigned)std::min(n_tiles, per_col), (unsigned)token_tiles);
-    return launch_pdl("qspec_linear_w4a16", w4a16_mma_kernel<NT>, grid, dim3(kThreads), smem, st, x, ldx,
-                      packed, sz, M, N, K, y, ldy);
+    return launch_pdl("qspec_linear_w4a16", kern, grid, dim3(kWarps * 32), smem, st, x, ldx, packed, sz, M, N, K, y,
+                      ldy);
+}
+
+// two 8-warp CTAs per SM when their shared memory fits, else one of 16 warps
+template <int MT>
+int launch_w4a16(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
+                 uint16_t *y, int ldy, cudaStream_t st) {
+    if (smem_bytes(MT, M, K, 8) <= 112 * 1024) return launch_w4a16_w<MT, 8>(x, ldx, packed, sz, M, N, K, y, ldy, st);
+    return launch_w4a16_w<MT, 16>(x, ldx, packed, sz, M, N, K, y, ldy, st);
 }
 
 }  // namespace
@@ -281,7 +348,19 @@ extern "C" int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t
     int rc = check_device();
     if (rc) return rc;
     cudaStream_t st = as_cuda(stream);
-    if (M <= 8) return launch_w4a16<1>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
-    if (M <= 16) return launch_w4a16<2>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
+    if (M <= 16) {
+        // tokens per CTA: up to 8 (one MMA column block), halved while the
+        // token fragments do not fit
+        int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
+        while (mt > 1 && smem_bytes(mt, M, K, 16) > 200 * 1024) mt /= 2;
+        if (smem_bytes(mt, M, K, 16) <= 200 * 1024) {
+            switch (mt) {
+                case 1: return launch_w4a16<1>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
+                case 2: return launch_w4a16<2>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
+                case 4: return launch_w4a16<4>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
+                default: return launch_w4a16<8>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
+            }
+        }
+    }
     return launch_w4a16_tc(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, dev_status, st);
 }

@@ -219,24 +219,34 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     // of a group sit in 16 consecutive lanes, which reduce the group offset
     const int wpr = K / 8;
     const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
-    for (int base = 0; base < MT * wpr; base += kThreads) {
-        const int i = base + threadIdx.x;
-        const bool valid = i < MT * wpr;
-        const int t = valid ? i / wpr : 0, wi = i - t * wpr;
-        const int m = tok0 + t;
-        const uint32_t w = valid && m < M ? xw[(size_t)m * wpr + wi] : 0u;
-        float q[8];
+    constexpr int kBatch = 4;                              // loads in flight per thread
+    for (int base = 0; base < MT * wpr; base += kBatch * kThreads) {
+        uint32_t wv[kBatch];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = act_code(w, e);
-        float part = 1024.0f * ((q[0] + q[2]) + (q[4] + q[6])) + 64.0f * ((q[1] + q[3]) + (q[5] + q[7]));
+        for (int b = 0; b < kBatch; ++b) {
+            const int i = base + b * kThreads + threadIdx.x;
+            const int t = i / wpr, wi = i - t * wpr;
+            wv[b] = i < MT * wpr && tok0 + t < M ? xw[(size_t)(tok0 + t) * wpr + wi] : 0u;
+        }
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (valid) {
-            const int g = wi >> 4, qcw = (wi >> 2) & 3, u = wi & 3;
-            bfr[(size_t)t * tstride + (g * 4 + u) * 4 + qcw] =
-                make_uint4(f16_pair(q[0], q[4]), f16_pair(q[1] * 0.0625f, q[5] * 0.0625f), f16_pair(q[2], q[6]),
-                           f16_pair(q[3] * 0.0625f, q[7] * 0.0625f));
-            if ((wi & 15) == 0) oq[g * MT + t].x = part;
+        for (int b = 0; b < kBatch; ++b) {
+            const int i = base + b * kThreads + threadIdx.x;
+            const bool valid = i < MT * wpr;
+            const int t = valid ? i / wpr : 0, wi = i - t * wpr;
+            const uint32_t w = wv[b];
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = act_code(w, e);
+            float part = 1024.0f * ((q[0] + q[2]) + (q[4] + q[6])) + 64.0f * ((q[1] + q[3]) + (q[5] + q[7]));
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (valid) {
+                const int g = wi >> 4, qcw = (wi >> 2) & 3, u = wi & 3;
+                bfr[(size_t)t * tstride + (g * 4 + u) * 4 + qcw] =
+                    make_uint4(f16_pair(q[0], q[4]), f16_pair(q[1] * 0.0625f, q[5] * 0.0625f), f16_pair(q[2], q[6]),
+                               f16_pair(q[3] * 0.0625f, q[7] * 0.0625f));
+                if ((wi & 15) == 0) oq[g * MT + t].x = part;
+            }
         }
     }
     for (int i = threadIdx.x; i < (int)tstride; i += kThreads) bfr[(size_t)MT * tstride + i] = make_uint4(0u, 0u, 0u, 0u);
