@@ -75,4 +75,31 @@ int launch_pdl(const char *where, void (*kernel)(KArgs...), dim3 grid, dim3 bloc
     return QSPEC_OK;
 }
 
+// The same with thread-block clusters of `cluster_x` CTAs along x (grid.x a
+// multiple of it).
+template <typename... KArgs, typename... Args>
+int launch_pdl_cluster(const char *where, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, int cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) {
+        set_last_error(where, e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    return QSPEC_OK;
+}
+
 }  // namespace qspec

@@ -23,6 +23,10 @@
 //              of the token columns: per group, TMEM -> registers,
 //              y = fma(D, s, y) in packed f32x2; finally bf16
 //   warp 12    issues 8 MMAs (K = 16) per group into one of two TMEM buffers
+// When the 128-channel tiles alone would leave SMs idle, a cluster of up to 8
+// CTAs splits a tile's groups; each CTA keeps its fp32 partial sums, and
+// rank 0 reads its peers' partials from distributed shared memory, adds them
+// in rank order and stores bf16.
 // Bounded waits everywhere (QSPEC_ERR_TIMEOUT on expiry, then clean exit).
 #include <algorithm>
 
@@ -81,12 +85,16 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_umma_kernel(const uint16_t *__restrict__ x, int ldx, const uint8_t *__restrict__ packed,
                       const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
-                      int32_t *st) {
+                      int32_t *st, int C) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem<BN> &sm = *reinterpret_cast<Smem<BN> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * kTileN, t0 = blockIdx.y * BN;
+    // cluster of C CTAs splits the groups of one 128-channel tile
+    const int rank = C > 1 ? (int)umma::cluster_rank() : 0;
+    const int n0 = (blockIdx.x / C) * kTileN, t0 = blockIdx.y * BN;
     const int G = K / kGroup;
+    const int g_lo = (int)(((long long)rank * G) / C), g_hi = (int)(((long long)(rank + 1) * G) / C);
+    const int NG = g_hi - g_lo;                          // this CTA's groups
     constexpr uint32_t kBuf = BN <= 32 ? 32 : BN <= 64 ? 64 : 128;
     constexpr uint32_t kCols = 2 * kBuf;
 
@@ -108,77 +116,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem;
+    // epilogue partial sums: per thread (row n, token half) BN / 2 values
+    constexpr int kHalf = BN / 2;
+    uint64_t acc[kHalf / 2];
+    bool epi_ok = false;
 
     if (warp < 4) {
         // ------------------------------------------------------------ producers
+        // weights: kD groups in flight per thread (one row each); activations
+        // of a group: all of a thread's chunks loaded before any is stored
+        constexpr int kD = 2;
+        constexpr int kChunks = BN * 16 / kProducers;  // 16-byte activation chunks per thread per group
         const int r = tid, n = n0 + r;
         const bool row_ok = n < N;
         const uint4 *wrow = reinterpret_cast<const uint4 *>(packed + (size_t)(row_ok ? n : 0) * (K / 2));
-        uint4 w[4];
-        uint32_t szn = 0;
+        uint4 ring[kD][4];
+        uint32_t zring[kD];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = row_ok ? __ldg(wrow + u) : make_uint4(0, 0, 0, 0);
-        if (row_ok) szn = __ldg(sz + (size_t)n * G);
+        for (int p = 0; p < kD; ++p) {
+            const int g = g_lo + p;
+            if (g < g_hi) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) ring[p][u] = __ldg(wrow + (size_t)g * 4 + u);
+                zring[p] = row_ok ? __ldg(sz + (size_t)n * G + g) : 0u;
+            }
+        }
         pdl_wait();
-        for (int g = 0; g < G; ++g) {
-            const int s = g % kStages;
-            if (g >= kStages && !umma::mbar_wait(&sm.empty[s], ((g / kStages) - 1) & 1)) {
-                atomicExch(&sm.timeout, 1);
-                break;
-            }
-            uint4 cw[4];
+        bool ok = true;
+        for (int lb = 0; lb < NG && ok; lb += kD) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) cw[u] = w[u];
-            const uint32_t szc = szn;
-            if (row_ok && g + 1 < G) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) w[u] = __ldg(wrow + (g + 1) * 4 + u);
-                szn = __ldg(sz + (size_t)n * G + g + 1);
-            }
-            const uint32_t zb = float_to_bf16_bits(128.0f + __half2float(__ushort_as_half((uint16_t)(szc >> 16))));
-            const uint32_t zz = zb | (zb << 16);
-            // weights: 128 codes of row r -> 16 chunks of 8 bf16
-            uint8_t *a = sm.a[s];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t words[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 v = row_ok ? codes_minus_z(words[q], zz) : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(a + umma::core_offset(r, 4 * u + q, kKB)) = v;
+            for (int p = 0; p < kD; ++p) {
+                const int l = lb + p, g = g_lo + l;
+                if (l >= NG) break;
+                const int s = l % kStages;
+                if (l >= kStages && !umma::mbar_wait(&sm.empty[s], ((l / kStages) - 1) & 1)) {
+                    atomicExch(&sm.timeout, 1);
+                    ok = false;
+                    break;
                 }
+                uint4 cw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) cw[u] = ring[p][u];
+                const uint32_t szc = zring[p];
+                if (l + kD < NG) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) ring[p][u] = __ldg(wrow + (size_t)(g + kD) * 4 + u);
+                    zring[p] = row_ok ? __ldg(sz + (size_t)n * G + g + kD) : 0u;
+                }
+                const uint32_t zb =
+                    float_to_bf16_bits(128.0f + __half2float(__ushort_as_half((uint16_t)(szc >> 16))));
+                const uint32_t zz = zb | (zb << 16);
+                // weights: 128 codes of row r -> 16 chunks of 8 bf16
+                uint8_t *a = sm.a[s];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t words[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 v = row_ok ? codes_minus_z(words[q], zz) : make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(a + umma::core_offset(r, 4 * u + q, kKB)) = v;
+                    }
+                }
+                // this group's activation chunks, in batches: loads first
+                uint8_t *b = sm.b[s];
+                constexpr int kBatch = kChunks % 8 == 0 ? 8 : kChunks % 6 == 0 ? 6 : 4;
+                static_assert(kChunks % kBatch == 0, "batches cover the chunks exactly");
+#pragma unroll
+                for (int j0 = 0; j0 < kChunks; j0 += kBatch) {
+                    uint4 av[kBatch];
+#pragma unroll
+                    for (int j = 0; j < kBatch; ++j) {
+                        const int c = tid + (j0 + j) * kProducers, t = c >> 4, jj = c & 15, m = t0 + t;
+                        av[j] = m < M ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx +
+                                                                              (size_t)g * kGroup + jj * 8))
+                                      : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int j = 0; j < kBatch; ++j) {
+                        const int c = tid + (j0 + j) * kProducers, t = c >> 4, jj = c & 15;
+                        *reinterpret_cast<uint4 *>(b + umma::core_offset(t, jj, kKB)) = acts_permuted(av[j]);
+                    }
+                }
+                umma::fence_proxy_async();
+                umma::mbar_arrive(&sm.full[s]);
             }
-            // activations: BN tokens x 128 bf16 of the group, 16 chunks each
-            uint8_t *b = sm.b[s];
-            for (int c = tid; c < BN * 16; c += kProducers) {
-                const int t = c >> 4, j = c & 15, m = t0 + t;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (m < M)
-                    v = acts_permuted(
-                        __ldg(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup + j * 8)));
-                *reinterpret_cast<uint4 *>(b + umma::core_offset(t, j, kKB)) = v;
-            }
-            umma::fence_proxy_async();
-            umma::mbar_arrive(&sm.full[s]);
         }
     } else if (warp < 12) {
         // ------------------------------------------------------------ epilogue
         pdl_wait();
-        constexpr int kHalf = BN / 2;
         constexpr int kW = kHalf % 32 == 0 ? 32 : 16;
         const int eq = warp & 3, eh = (warp - 4) >> 2;
         const int n = n0 + eq * 32 + lane;
         const bool row_ok = n < N;
-        uint64_t acc[kHalf / 2];
 #pragma unroll
         for (int i = 0; i < kHalf / 2; ++i) acc[i] = 0;
         bool ok = true;
-        for (int g = 0; g < G && ok; ++g) {
-            const int buf = g & 1;
-            const uint32_t szw = row_ok ? __ldg(sz + (size_t)n * G + g) : 0u;
+        uint32_t szn = row_ok && NG > 0 ? __ldg(sz + (size_t)n * G + g_lo) : 0u;
+        for (int l = 0; l < NG && ok; ++l) {
+            const int buf = l & 1;
+            const uint32_t szw = szn;
+            if (row_ok && l + 1 < NG) szn = __ldg(sz + (size_t)n * G + g_lo + l + 1);
             const float sn = __half2float(__ushort_as_half((uint16_t)(szw & 0xFFFF)));
             const uint64_t s2 = f2(sn, sn);
-            if (!umma::mbar_wait(&sm.accf[buf], (g >> 1) & 1)) {
+            if (!umma::mbar_wait(&sm.accf[buf], (l >> 1) & 1)) {
                 atomicExch(&sm.timeout, 1);
                 ok = false;
                 break;
@@ -200,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::fence_before_sync();
             umma::mbar_arrive(&sm.acce[buf]);
         }
-        if (ok && row_ok) {
+        epi_ok = ok;
+        if (C == 1 && ok && row_ok) {
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {
                 const int m = t0 + eh * kHalf + 2 * i;
@@ -214,10 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         if (lane == 0) {
             constexpr uint32_t idesc = umma::instr_desc(1, 1, kTileN, BN);
-            for (int g = 0; g < G; ++g) {
-                const int s = g % kStages, buf = g & 1;
-                if (!umma::mbar_wait(&sm.full[s], (g / kStages) & 1) ||
-                    (g >= 2 && !umma::mbar_wait(&sm.acce[buf], ((g >> 1) - 1) & 1))) {
+            for (int l = 0; l < NG; ++l) {
+                const int s = l % kStages, buf = l & 1;
+                if (!umma::mbar_wait(&sm.full[s], (l / kStages) & 1) ||
+                    (l >= 2 && !umma::mbar_wait(&sm.acce[buf], ((l >> 1) - 1) & 1))) {
                     atomicExch(&sm.timeout, 1);
                     break;
                 }
@@ -238,6 +279,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     umma::fence_before_sync();
     __syncthreads();
+    if (C > 1) {
+        // split groups: every CTA's partials -> its shared memory (the operand
+        // stages are free now: all MMAs have completed); rank 0 adds them in
+        // rank order and stores bf16
+        float *red = reinterpret_cast<float *>(smem_raw);          // [BN tokens][128 channels]
+        const int eq = warp & 3, eh = (warp - 4) >> 2, row = eq * 32 + lane;
+        if (warp >= 4 && warp < 12) {
+#pragma unroll
+            for (int i = 0; i < kHalf / 2; ++i) {
+                const int t = eh * kHalf + 2 * i;
+                red[(size_t)t * kTileN + row] = epi_ok ? __uint_as_float((uint32_t)acc[i]) : 0.0f;
+                red[(size_t)(t + 1) * kTileN + row] = epi_ok ? __uint_as_float((uint32_t)(acc[i] >> 32)) : 0.0f;
+            }
+        }
+        umma::cluster_sync();
+        if (rank == 0 && warp >= 4 && warp < 12) {
+            const int n = n0 + row;
+            if (n < N) {
+                for (int t = eh * kHalf; t < eh * kHalf + kHalf; ++t) {
+                    const int m = t0 + t;
+                    if (m >= M) break;
+                    float sum = red[(size_t)t * kTileN + row];
+                    for (int q = 1; q < C; ++q) sum += umma::ld_peer_f32(&red[(size_t)t * kTileN + row], (uint32_t)q);
+                    y[(size_t)m * ldy + n] = float_to_bf16_bits(sum);
+                }
+            }
+        }
+        umma::cluster_sync();
+    }
     if (tid == 0 && sm.timeout) flag(st, QSPEC_ERR_TIMEOUT);
     if (warp == 0) umma::tmem_free(tmem, kCols);
 }
@@ -245,12 +315,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN>
 int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
               uint16_t *y, int ldy, int32_t *st, cudaStream_t stream) {
+    static_assert(sizeof(float) * BN * kTileN <= sizeof(Smem<BN>), "partials fit in the operand stages");
     const size_t smem = sizeof(Smem<BN>) + 1024;
     int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a16_umma_kernel<BN>), 32 + BN / 16, (int)smem);
     if (rc) return rc;
-    dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + BN - 1) / BN));
-    return launch_pdl("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, x, ldx,
-                      packed, sz, M, N, K, y, ldy, st);
+    const int n_tiles = (N + kTileN - 1) / kTileN, token_tiles = (M + BN - 1) / BN, G = K / kGroup;
+    // split the groups over a cluster (2, 4 or 8 CTAs: sizes that pack into
+    // the GPCs) when the tiles alone leave SMs idle
+    int C = 1;
+    while (C < 8 && n_tiles * token_tiles * C * 2 <= sm_count() && 2 * C * 2 <= G) C *= 2;
+    dim3 grid((unsigned)(n_tiles * C), (unsigned)token_tiles);
+    if (C == 1)
+        return launch_pdl("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, x, ldx,
+                          packed, sz, M, N, K, y, ldy, st, C);
+    return launch_pdl_cluster("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, C, x,
+                              ldx, packed, sz, M, N, K, y, ldy, st, C);
 }
 
 }  // namespace

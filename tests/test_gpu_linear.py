@@ -35,7 +35,10 @@ def run_w4a4(x, packed, sz, dev, want_I=True):
     (4, 512, 512, 0),                     # the single-layer case: K = N = 512, M = gamma + 1 = 4
     (1, 16, 128, 1), (2, 100, 384, 2), (3, 1000, 1024, 3), (5, 48, 3072, 4),
     (8, 33, 256, 5), (9, 64, 512, 6), (13, 17, 128, 7), (16, 256, 640, 8), (17, 40, 384, 9),
-    (33, 31, 1152, 10)])
+    (33, 31, 1152, 10),
+    # W4A16 with the groups of a tile split over a cluster of 4 or 8 CTAs
+    # (uneven splits included), W4A4 on the tensor cores
+    (80, 300, 1024, 11), (50, 1000, 2048, 12), (24, 130, 1152, 13), (128, 257, 4096, 14)])
 def test_small_full_compare(M, N, K, seed):
     dev = need_gpu()
     packed, sz, po, szo = make_layer(N, K, seed, dev)
