@@ -25,48 +25,62 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
     long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
     const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
     bool bad = false;
-    for (; warp < (long long)M * pairs_per_row; warp += n_warps) {
-        int m = (int)(warp / pairs_per_row);
-        int g = (int)(warp % pairs_per_row) * 2 + half;
-        bool active = g < G;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (active)
-            v = __ldcs(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup) + hl);
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float f[8];
+    // kBatch pair-tasks per warp and pass, their loads issued first
+    constexpr int kBatch = 4;
+    const long long tasks = (long long)M * pairs_per_row;
+    for (; warp < tasks; warp += kBatch * n_warps) {
+        uint4 v[kBatch];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            bad |= !isfinite(f[i]);
-            amax = fmaxf(amax, fabsf(f[i]));
+        for (int j = 0; j < kBatch; ++j) {
+            const long long w = warp + j * n_warps;
+            const int m = (int)(w / pairs_per_row);
+            const int g = (int)(w % pairs_per_row) * 2 + half;
+            v[j] = w < tasks && g < G
+                       ? __ldcs(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup) + hl)
+                       : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        float scale = __fdiv_rn(amax, 7.0f);
-        int sum = 0;
-        uint32_t nib = 0;
+        for (int j = 0; j < kBatch; ++j) {
+            const long long w = warp + j * n_warps;
+            const int m = (int)(w / pairs_per_row);
+            const int g = (int)(w % pairs_per_row) * 2 + half;
+            const bool active = w < tasks && g < G;
+            float f[8];
+            const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int q = 0;
-            if (scale != 0.0f) {
-                q = __float2int_rn(__fdiv_rn(f[i], scale));
-                q = max(-7, min(7, q));
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = __uint_as_float(wv[i] << 16);
+                f[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
             }
-            sum += q;
-            nib |= (uint32_t)(q & 15) << (4 * i);
-        }
+            float amax = 0.0f;
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (active) {
-            reinterpret_cast<uint32_t *>(xq + (size_t)m * (K / 2) + (size_t)g * (kGroup / 2))[hl] = nib;
-            if (hl == 0) {
-                sx[(size_t)m * G + g] = scale;
-                qs[(size_t)m * G + g] = sum;
+            for (int i = 0; i < 8; ++i) {
+                bad |= !isfinite(f[i]);
+                amax = fmaxf(amax, fabsf(f[i]));
+            }
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            float scale = __fdiv_rn(amax, 7.0f);
+            int sum = 0;
+            uint32_t nib = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                int q = 0;
+                if (scale != 0.0f) {
+                    q = __float2int_rn(__fdiv_rn(f[i], scale));
+                    q = max(-7, min(7, q));
+                }
+                sum += q;
+                nib |= (uint32_t)(q & 15) << (4 * i);
+            }
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (active) {
+                reinterpret_cast<uint32_t *>(xq + (size_t)m * (K / 2) + (size_t)g * (kGroup / 2))[hl] = nib;
+                if (hl == 0) {
+                    sx[(size_t)m * G + g] = scale;
+                    qs[(size_t)m * G + g] = sum;
+                }
             }
         }
     }

@@ -17,10 +17,13 @@
 // many CTAs and combined with atomics without changing a single bit.
 //
 // Launch sequence (one stream, no host synchronisation):
-//   greedy : memset, argmax (chunk x row), finalize (per sequence)
-//   sampled: memset, row max (chunk x row), row sums (chunk x row),
-//            decisions + residual chunk sums (chunk x sequence),
-//            draw (per sequence)
+//   greedy : argmax (one CTA per row when there are at least two rows per
+//            SM; else memset, chunk x row with atomics), finalize (per
+//            sequence)
+//   sampled: row max and row sums (one CTA per row, the second pass over the
+//            row hitting L2; else memset, then chunk x row kernels for each
+//            with atomics), decisions + residual chunk sums (chunk x
+//            sequence), draw (per sequence)
 // HBM traffic: one read of every logit (B (2 gamma + 1) V bf16) plus L2
 // re-reads of the rows a later phase needs.
 #include <algorithm>
@@ -166,6 +169,39 @@ __global__ void __launch_bounds__(kThreads) greedy_argmax_kernel(const uint16_t 
     if (threadIdx.x == 0) atomicMax(keys + row, best);
 }
 
+// one CTA per row: the row's argmax key written directly
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) greedy_rowargmax_kernel(const uint16_t *__restrict__ P, int V,
+                                                                   unsigned long long *__restrict__ keys,
+                                                                   int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ unsigned long long sh[kThreads / 32];
+    const int row = blockIdx.x;
+    const uint16_t *rp = P + (size_t)row * V;
+    unsigned long long best = 0;
+    bool bad = false;
+    for (int v0 = threadIdx.x * 8; v0 < V; v0 += kSub * 4) {
+        float f[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) load8<VEC>(rp, v0 + u * kSub, V, f[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int v = v0 + u * kSub + i;
+                if (v >= V) break;
+                bad |= isnan(f[u][i]);
+                const unsigned long long key =
+                    ((unsigned long long)ordered_bits(f[u][i]) << 32) | (0xFFFFFFFFu - (uint32_t)v);
+                best = key > best ? key : best;
+            }
+    }
+    if (bad) flag(st, QSPEC_ERR_NONFINITE);
+    best = block_reduce_max(best, sh);
+    if (threadIdx.x == 0) keys[row] = best;
+}
+
 __global__ void greedy_finalize_kernel(const unsigned long long *__restrict__ keys,
                                        const int32_t *__restrict__ draft, int B, int gamma, int V,
                                        int32_t *__restrict__ n_acc, int32_t *__restrict__ out,
@@ -255,6 +291,69 @@ __global__ void __launch_bounds__(kThreads) sample_rowsum_kernel(const uint16_t 
     }
     s = block_reduce_sum(s, sh);
     if (threadIdx.x == 0 && s) atomicAdd(sums + row, s);
+}
+
+// one CTA per row (used when there are enough rows to fill the GPU): the row
+// maximum, then the sum of fixed weights over the same row, which is still in
+// L2; both written directly (no atomics, no cleared workspace).  The first
+// pass keeps kUnroll loads in flight per thread.
+constexpr int kUnroll = 4;
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) sample_rowstats_kernel(const uint16_t *__restrict__ P,
+                                                                  const uint16_t *__restrict__ Q, int B,
+                                                                  int gamma, int V,
+                                                                  uint32_t *__restrict__ maxenc,
+                                                                  unsigned long long *__restrict__ sums,
+                                                                  int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ uint32_t shm[kThreads / 32];
+    __shared__ unsigned long long shs[kThreads / 32];
+    __shared__ uint32_t s_m;
+    const int row = blockIdx.x;
+    const uint16_t *rp = row_ptr(P, Q, B, gamma, V, row);
+    float m = -INFINITY;
+    bool bad = false;
+    for (int v0 = threadIdx.x * 8; v0 < V; v0 += kSub * kUnroll) {
+        float f[kUnroll][8];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) load8<VEC>(rp, v0 + u * kSub, V, f[u]);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                bad |= isnan(f[u][i]) || f[u][i] == INFINITY;
+                m = fmaxf(m, f[u][i]);
+            }
+    }
+    if (bad) flag(st, QSPEC_ERR_NONFINITE);
+    const uint32_t e = block_reduce_max(ordered_bits(m), shm);
+    if (threadIdx.x == 0) {
+        s_m = e;
+        maxenc[row] = e;
+    }
+    __syncthreads();
+    m = from_ordered_bits(s_m);
+    if (m == -INFINITY) {                      // a row without any mass
+        if (threadIdx.x == 0) {
+            flag(st, QSPEC_ERR_NONFINITE);
+            sums[row] = 0;
+        }
+        return;
+    }
+    unsigned long long sum = 0;
+    for (int v0 = threadIdx.x * 8; v0 < V; v0 += kSub * kUnroll) {
+        float f[kUnroll][8];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) load8<VEC>(rp, v0 + u * kSub, V, f[u]);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sum += fixed_weight(f[u][i], m);
+    }
+    sum = block_reduce_sum(sum, shs);
+    if (threadIdx.x == 0) sums[row] = sum;
 }
 
 // decisions of sequence b: A_b (first rejected draft index, gamma if none)
@@ -503,17 +602,27 @@ extern "C" int qspec_verify_greedy(const uint16_t *p_logits, const int32_t *draf
     Layout L = make_layout(B, gamma, V);
     char *ws = static_cast<char *>(workspace);
     auto *keys = reinterpret_cast<unsigned long long *>(ws + L.off_key);
-    cudaError_t e = cudaMemsetAsync(keys, 0, (size_t)B * (gamma + 1) * 8, st);
-    if (e != cudaSuccess) {
-        set_last_error("qspec_verify_greedy memset", e);
-        return QSPEC_ERR_LAUNCH;
-    }
-    dim3 grid((unsigned)(B * (gamma + 1)), (unsigned)L.n_chunks);
+    const int rows = B * (gamma + 1);
     bool vec = (V % 8 == 0) && aligned(p_logits, 16);
-    rc = vec ? launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<true>, grid, dim3(kThreads), 0, st,
-                          p_logits, V, L.chunk, keys, dev_status)
-             : launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<false>, grid, dim3(kThreads), 0, st,
-                          p_logits, V, L.chunk, keys, dev_status);
+    if (rows >= 2 * sm_count()) {
+        // enough rows: one CTA per row
+        rc = vec ? launch_pdl("qspec_verify_greedy", greedy_rowargmax_kernel<true>, dim3(rows), dim3(kThreads), 0,
+                              st, p_logits, V, keys, dev_status)
+                 : launch_pdl("qspec_verify_greedy", greedy_rowargmax_kernel<false>, dim3(rows), dim3(kThreads), 0,
+                              st, p_logits, V, keys, dev_status);
+    } else {
+        // few rows: chunks of every row combined with atomics
+        cudaError_t e = cudaMemsetAsync(keys, 0, (size_t)rows * 8, st);
+        if (e != cudaSuccess) {
+            set_last_error("qspec_verify_greedy memset", e);
+            return QSPEC_ERR_LAUNCH;
+        }
+        dim3 grid((unsigned)rows, (unsigned)L.n_chunks);
+        rc = vec ? launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<true>, grid, dim3(kThreads), 0, st,
+                              p_logits, V, L.chunk, keys, dev_status)
+                 : launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<false>, grid, dim3(kThreads), 0, st,
+                              p_logits, V, L.chunk, keys, dev_status);
+    }
     if (rc) return rc;
     return launch_pdl("qspec_verify_greedy", greedy_finalize_kernel, dim3((B + 127) / 128), dim3(128), 0, st,
                       keys, draft, B, gamma, V, n_acc, out, dev_status);
@@ -529,14 +638,29 @@ static int launch_sample(const uint16_t *P, const uint16_t *Q, const int32_t *dr
     auto *esum = reinterpret_cast<unsigned long long *>(ws + L.off_esum);
     auto *accbuf = reinterpret_cast<int32_t *>(ws + L.off_acc);
     const int rows = B * (2 * gamma + 1);
-    dim3 grid_rows((unsigned)rows, (unsigned)L.n_chunks);
     const char *w = "qspec_verify_sample";
-    int rc = launch_pdl(w, sample_rowmax_kernel<VEC>, grid_rows, dim3(kThreads), 0, st, P, Q, B, gamma, V,
-                        L.chunk, maxenc, dev_status);
-    if (rc) return rc;
-    rc = launch_pdl(w, sample_rowsum_kernel<VEC>, grid_rows, dim3(kThreads), 0, st, P, Q, B, gamma, V, L.chunk,
-                    maxenc, sums, dev_status);
-    if (rc) return rc;
+    int rc;
+    if (rows >= 2 * sm_count()) {
+        // enough rows: one CTA per row, both statistics in one launch
+        rc = launch_pdl(w, sample_rowstats_kernel<VEC>, dim3(rows), dim3(kThreads), 0, st, P, Q, B, gamma, V,
+                        maxenc, sums, dev_status);
+        if (rc) return rc;
+    } else {
+        // few rows: chunks of every row; maxima and sums combined with atomics
+        // from 0 (below every encoded value)
+        cudaError_t e = cudaMemsetAsync(ws + L.off_max, 0, L.off_rsum - L.off_max, st);
+        if (e != cudaSuccess) {
+            set_last_error("qspec_verify_sample memset", e);
+            return QSPEC_ERR_LAUNCH;
+        }
+        dim3 grid_rows((unsigned)rows, (unsigned)L.n_chunks);
+        rc = launch_pdl(w, sample_rowmax_kernel<VEC>, grid_rows, dim3(kThreads), 0, st, P, Q, B, gamma, V, L.chunk,
+                        maxenc, dev_status);
+        if (rc) return rc;
+        rc = launch_pdl(w, sample_rowsum_kernel<VEC>, grid_rows, dim3(kThreads), 0, st, P, Q, B, gamma, V,
+                        L.chunk, maxenc, sums, dev_status);
+        if (rc) return rc;
+    }
     dim3 grid_seq((unsigned)B, (unsigned)L.n_chunks);
     rc = launch_pdl(w, sample_residual_kernel<VEC>, grid_seq, dim3(kThreads), 0, st, P, Q, draft, B, gamma, V,
                     L.chunk, seed, round, maxenc, sums, rsum, esum, accbuf, n_acc, out, dev_status);
@@ -558,12 +682,6 @@ extern "C" int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_l
     cudaStream_t st = as_cuda(stream);
     Layout L = make_layout(B, gamma, V);
     char *ws = static_cast<char *>(workspace);
-    // row maxima start at 0 (below every encoded value), row sums at 0
-    cudaError_t e = cudaMemsetAsync(ws + L.off_max, 0, L.off_rsum - L.off_max, st);
-    if (e != cudaSuccess) {
-        set_last_error("qspec_verify_sample memset", e);
-        return QSPEC_ERR_LAUNCH;
-    }
     bool vec = (V % 8 == 0) && aligned(p_logits, 16) && aligned(q_logits, 16);
     return vec ? launch_sample<true>(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, L, ws,
                                      dev_status, st)

@@ -72,7 +72,9 @@ def test_single_layer_case_vocab_1024():
 
 @pytest.mark.parametrize("B,gamma,V,seed", [
     (1, 1, 2, 0), (3, 2, 7, 1), (2, 4, 8, 2), (4, 16, 1000, 3), (16, 3, 4099, 4),
-    (5, 8, 30000, 5), (2, 1, 1, 6), (7, 5, 2048, 7), (1, 16, 70001, 8), (2, 2, 600000, 9)])
+    (5, 8, 30000, 5), (2, 1, 1, 6), (7, 5, 2048, 7), (1, 16, 70001, 8), (2, 2, 600000, 9),
+    # at least two rows per SM: one CTA per row (V % 8 != 0 takes the scalar loads)
+    (64, 4, 3001, 10), (40, 7, 1000, 11), (70, 4, 8192, 12)])
 def test_random_shapes(B, gamma, V, seed):
     dev = need_gpu()
     P, Q, d = syn.logits_noisy_draft(B, gamma, V, seed, p_std=3.0, q_noise=0.5)
@@ -80,11 +82,13 @@ def test_random_shapes(B, gamma, V, seed):
         check_both(P, Q, d, dev, seed=seed, rnd=rnd)
 
 
-def test_row_statistics_in_workspace():
+@pytest.mark.parametrize("B", [3, 64])
+def test_row_statistics_in_workspace(B):
     """The sampled call leaves each row's max and exact fixed-point sum in the
-    workspace (rows: P[b][i] then Q[b][i]); they match the oracle's."""
+    workspace (rows: P[b][i] then Q[b][i]); they match the oracle's, both for
+    chunked rows (B = 3) and one CTA per row (B = 64: 320 rows)."""
     dev = need_gpu()
-    B, gamma, V = 3, 2, 5000
+    gamma, V = 2, 5000
     P, Q, d = syn.logits_noisy_draft(B, gamma, V, 3)
     ws = q.verify_workspace(B, gamma, V, dev)
     gpu_sample(P, Q, d, 1, 1, dev, ws=ws)
@@ -145,10 +149,11 @@ def test_degenerate_rows():
     check_both(P.to(torch.bfloat16), Q.to(torch.bfloat16), d, dev)
 
 
+@pytest.mark.parametrize("B", [2, 64])
 @pytest.mark.parametrize("what", ["p_nan", "q_inf", "q_all_neg_inf", "draft_range"])
-def test_device_status(what):
+def test_device_status(what, B):
     dev = need_gpu()
-    P, Q, d = syn.logits_noisy_draft(2, 2, 300, 1)
+    P, Q, d = syn.logits_noisy_draft(B, 4 if B > 2 else 2, 300, 1)
     if what == "p_nan":
         P[1, 2, 17] = float("nan")
     elif what == "q_inf":
