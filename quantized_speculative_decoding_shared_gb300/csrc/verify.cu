@@ -293,32 +293,51 @@ __global__ void __launch_bounds__(kThreads) sample_rowsum_kernel(const uint16_t 
     if (threadIdx.x == 0 && s) atomicAdd(sums + row, s);
 }
 
-// one CTA per row (used when there are enough rows to fill the GPU): the row
-// maximum, then the sum of fixed weights over the same row, which is still in
-// L2; both written directly (no atomics, no cleared workspace).  The first
-// pass keeps kUnroll loads in flight per thread.
+// one CTA of kRowThreads per row (used when there are enough rows to fill the
+// GPU): the row maximum, then the sum of fixed weights over the same row.  Two
+// CTAs per SM keep 2 x 152 rows in flight, few enough that the second pass
+// finds the row in L2.  Both results are written directly (no atomics, no
+// cleared workspace); the first pass keeps kUnroll loads in flight per thread.
+constexpr int kRowThreads = 512;
 constexpr int kUnroll = 4;
 
+// block reduction over kRowThreads threads with operator op and its identity
+template <typename T, typename Op>
+__device__ __forceinline__ T row_reduce(T v, T *sh, T identity, Op op) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        v = threadIdx.x < kRowThreads / 32 ? sh[threadIdx.x] : identity;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    }
+    __syncthreads();
+    return v;   // valid in thread 0
+}
+
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads) sample_rowstats_kernel(const uint16_t *__restrict__ P,
-                                                                  const uint16_t *__restrict__ Q, int B,
-                                                                  int gamma, int V,
-                                                                  uint32_t *__restrict__ maxenc,
-                                                                  unsigned long long *__restrict__ sums,
-                                                                  int32_t *st) {
+__global__ void __launch_bounds__(kRowThreads, 2) sample_rowstats_kernel(const uint16_t *__restrict__ P,
+                                                                        const uint16_t *__restrict__ Q, int B,
+                                                                        int gamma, int V,
+                                                                        uint32_t *__restrict__ maxenc,
+                                                                        unsigned long long *__restrict__ sums,
+                                                                        int32_t *st) {
     pdl_launch_dependents();
     pdl_wait();
-    __shared__ uint32_t shm[kThreads / 32];
-    __shared__ unsigned long long shs[kThreads / 32];
+    constexpr int kStep = kRowThreads * 8;
+    __shared__ uint32_t shm[kRowThreads / 32];
+    __shared__ unsigned long long shs[kRowThreads / 32];
     __shared__ uint32_t s_m;
     const int row = blockIdx.x;
     const uint16_t *rp = row_ptr(P, Q, B, gamma, V, row);
     float m = -INFINITY;
     bool bad = false;
-    for (int v0 = threadIdx.x * 8; v0 < V; v0 += kSub * kUnroll) {
+    for (int v0 = threadIdx.x * 8; v0 < V; v0 += kStep * kUnroll) {
         float f[kUnroll][8];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) load8<VEC>(rp, v0 + u * kSub, V, f[u]);
+        for (int u = 0; u < kUnroll; ++u) load8<VEC>(rp, v0 + u * kStep, V, f[u]);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
@@ -328,7 +347,8 @@ __global__ void __launch_bounds__(kThreads) sample_rowstats_kernel(const uint16_
             }
     }
     if (bad) flag(st, QSPEC_ERR_NONFINITE);
-    const uint32_t e = block_reduce_max(ordered_bits(m), shm);
+    const uint32_t e =
+        row_reduce(ordered_bits(m), shm, 0u, [](uint32_t a, uint32_t b) { return a > b ? a : b; });
     if (threadIdx.x == 0) {
         s_m = e;
         maxenc[row] = e;
@@ -343,16 +363,16 @@ __global__ void __launch_bounds__(kThreads) sample_rowstats_kernel(const uint16_
         return;
     }
     unsigned long long sum = 0;
-    for (int v0 = threadIdx.x * 8; v0 < V; v0 += kSub * kUnroll) {
-        float f[kUnroll][8];
+    for (int v0 = threadIdx.x * 8; v0 < V; v0 += kStep * 2) {
+        float f[2][8];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) load8<VEC>(rp, v0 + u * kSub, V, f[u]);
+        for (int u = 0; u < 2; ++u) load8<VEC>(rp, v0 + u * kStep, V, f[u]);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
             for (int i = 0; i < 8; ++i) sum += fixed_weight(f[u][i], m);
     }
-    sum = block_reduce_sum(sum, shs);
+    sum = row_reduce(sum, shs, 0ull, [](unsigned long long a, unsigned long long b) { return a + b; });
     if (threadIdx.x == 0) sums[row] = sum;
 }
 
@@ -642,7 +662,7 @@ static int launch_sample(const uint16_t *P, const uint16_t *Q, const int32_t *dr
     int rc;
     if (rows >= 2 * sm_count()) {
         // enough rows: one CTA per row, both statistics in one launch
-        rc = launch_pdl(w, sample_rowstats_kernel<VEC>, dim3(rows), dim3(kThreads), 0, st, P, Q, B, gamma, V,
+        rc = launch_pdl(w, sample_rowstats_kernel<VEC>, dim3(rows), dim3(kRowThreads), 0, st, P, Q, B, gamma, V,
                         maxenc, sums, dev_status);
         if (rc) return rc;
     } else {
