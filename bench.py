@@ -716,7 +716,11 @@ def main():
                 "frac": round(ach4 / peak, 4), "peak_source": peak_kind,
                 "bytes_per_launch": rnd_obj.bytes_draft_linears() / n4,
                 "launch_us": 1e3 * t4 / n4,
-                "traffic": traffic["dram_bytes_per_launch"] if traffic else None}
+                # ncu DRAM bytes of one captured launch (the LM head at this M),
+                # scaled by algorithmic bytes to the average launch above
+                "traffic": (round(traffic["dram_bytes_per_algorithmic_byte"] *
+                                  rnd_obj.bytes_draft_linears() / n4)
+                            if traffic and wl["B"] == 1 else None)}
 
     # e2e: host buffers, copies inside the timed region
     host_in = [t.cpu().pin_memory() for t in rnd_obj.host_inputs()]
