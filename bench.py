@@ -291,7 +291,15 @@ class GpuRound:
     # kernel launches of the library per step (for gpu_launches)
     def launches_per_round(self):
         n_lin = len(self.linears)
-        draft = self.gamma * (self.L * n_lin * 2 + 2)
+        sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
+
+        def w4a4_launches(N):
+            # the fused call is one launch on the warp-MMA path (M <= 32, not
+            # the tensor-memory GEMV), else quantiser + linear
+            two = self.B > 32 or (3 <= self.B <= 8 and (N + 127) // 128 >= sms)
+            return 2 if two else 1
+        draft = self.gamma * (self.L * sum(w4a4_launches(N) for _, N, _ in self.linears) +
+                              w4a4_launches(self.V))
         verify = self.L * n_lin + 1
         return draft + verify + 4 + 1
 
@@ -300,12 +308,13 @@ class GpuRound:
             raise RuntimeError("%s returned %s" % (what, self.q.STATUS.get(rc, rc)))
 
     def _w4a4(self, x, pk, N, K, y):
+        """a2 + a3: quantise the bf16 activations and run the W4A4 linear (one
+        launch on the warp-MMA path; the quantised activations are kept)."""
         q = self.q
         xq, sx, qs = self.qbuf[K]
         M = x.shape[0]
-        self._check(q.qspec_quant_act_int4(x, M, K, K, xq, sx, qs, self.status), "quant")
-        self._check(q.qspec_linear_w4a4(xq, sx, qs, pk[0], pk[1], M, N, K, y, N, None,
-                                        self.status), "w4a4")
+        self._check(q.qspec_linear_w4a4_bf16(x, K, pk[0], pk[1], M, N, K, y, N, xq, sx, qs, None,
+                                             self.status), "w4a4_bf16")
 
     def draft_linears_only(self, j=0):
         """One draft step's W4A4 launches without the quantiser (kernel timing)."""

@@ -124,6 +124,27 @@ int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32_t *qs,
                       qspec_stream_t stream);
 
 /*
+ * a2 + a3 in one call: the draft-pass linear on bf16 activations.  The
+ * activations are quantised exactly as qspec_quant_act_int4 does it and the
+ * product is exactly qspec_linear_w4a4's; [QS-design] the draft pass runs
+ * the quantiser in front of every W4A4 linear, and at decode sizes one launch
+ * instead of two removes the second launch's latency from the critical path
+ * (every CTA quantises the tokens it needs; CTA column 0 stores them).
+ *
+ *   x_bf16 uint16 [M][ldx]  (ldx >= K, ldx % 8 == 0, 16-byte aligned)
+ *   packed, sz              from qspec_pack_weights, N rows
+ *   y_bf16 uint16 [M][ldy]  out (ldy >= N)
+ *   xq, sx, qs              out: the quantised activations, as from
+ *                           qspec_quant_act_int4 (xq 16-byte aligned)
+ *   dbg_I  int32 [M][N][G]  nullable: out, the group integers I
+ * Device errors: QSPEC_ERR_NONFINITE (a NaN or inf input).
+ */
+int qspec_linear_w4a4_bf16(const uint16_t *x_bf16, int ldx, const uint8_t *packed,
+                           const uint32_t *sz, int M, int N, int K, uint16_t *y_bf16, int ldy,
+                           uint8_t *xq, float *sx, int32_t *qs, int32_t *dbg_I,
+                           int32_t *dev_status, qspec_stream_t stream);
+
+/*
  * a4. W4A16 linear (verify).  [QS-bg] Y = X W^, W^ = s (W_INT4 - z),
  * 16-bit activations; [QS-design] the verify pass over the gamma+1 rows of
  * every sequence (M = B (gamma + 1)).  fp32 accumulation, bf16 output,

@@ -30,7 +30,7 @@ OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_LAUNCH, ERR_WORKSPACE = 0, 1, 2, 3, 4, 5
 ERR_RANGE, ERR_ZERO_POINT, ERR_NONFINITE, ERR_TIMEOUT, ERR_UNSUPPORTED = 6, 7, 8, 9, 10
 
 EXPORTED = ["qspec_version", "qspec_status_string", "qspec_last_cuda_error", "qspec_pack_weights",
-            "qspec_quant_act_int4", "qspec_linear_w4a4", "qspec_linear_w4a16",
+            "qspec_quant_act_int4", "qspec_linear_w4a4", "qspec_linear_w4a4_bf16", "qspec_linear_w4a16",
             "qspec_verify_workspace_bytes", "qspec_verify_greedy", "qspec_verify_sample",
             "qspec_kv_overwrite", "qspec_verify_sample_noalloc"]
 NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -68,6 +68,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "qspec_pack_weights": ([vp, vp, vp, i32, i32, vp, vp, vp, vp], i32),
             "qspec_quant_act_int4": ([vp, i32, i32, i32, vp, vp, vp, vp, vp], i32),
             "qspec_linear_w4a4": ([vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp], i32),
+            "qspec_linear_w4a4_bf16": ([vp, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp],
+                                       i32),
             "qspec_linear_w4a16": ([vp, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp], i32),
             "qspec_verify_workspace_bytes": ([i32, i32, i32], sz_t),
             "qspec_verify_greedy": ([vp, vp, i32, i32, i32, vp, vp, vp, sz_t, vp, vp], i32),
@@ -134,6 +136,13 @@ def qspec_linear_w4a4(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I=None, dev_s
     return load_library().qspec_linear_w4a4(_ptr(xq), _ptr(sx), _ptr(qs), _ptr(packed), _ptr(sz),
                                             M, N, K, _ptr(y), ldy, _ptr(dbg_I), _ptr(dev_status),
                                             _stream(stream))
+
+
+def qspec_linear_w4a4_bf16(x, ldx, packed, sz, M, N, K, y, ldy, xq, sx, qs, dbg_I=None,
+                           dev_status=None, stream=None):
+    return load_library().qspec_linear_w4a4_bf16(_ptr(x), ldx, _ptr(packed), _ptr(sz), M, N, K,
+                                                 _ptr(y), ldy, _ptr(xq), _ptr(sx), _ptr(qs),
+                                                 _ptr(dbg_I), _ptr(dev_status), _stream(stream))
 
 
 def qspec_linear_w4a16(x, ldx, packed, sz, M, N, K, y, ldy, dev_status=None, stream=None):
@@ -211,6 +220,24 @@ def linear_w4a4(xq, sx, qs, packed, sz, want_I=False, out=None, dev_status=None,
     _check(qspec_linear_w4a4(xq, sx, qs, packed, sz, M, N, K, y, y.stride(0), I, dev_status,
                              stream), "qspec_linear_w4a4")
     return (y, I) if want_I else y
+
+
+def linear_w4a4_bf16(x, packed, sz, want_I=False, out=None, dev_status=None, stream=None):
+    """Quantise bf16 activations and run the W4A4 linear in one call:
+    returns (y, xq, sx, qs) (and I when want_I), equal to quant_act_int4
+    followed by linear_w4a4."""
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    N = packed.shape[0]
+    dev = x.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    xq = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    sx = torch.empty((M, K // GROUP), dtype=torch.float32, device=dev)
+    qs = torch.empty((M, K // GROUP), dtype=torch.int32, device=dev)
+    I = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=dev) if want_I else None
+    _check(qspec_linear_w4a4_bf16(x, x.stride(0), packed, sz, M, N, K, y, y.stride(0), xq, sx, qs, I,
+                                  dev_status, stream), "qspec_linear_w4a4_bf16")
+    return (y, xq, sx, qs, I) if want_I else (y, xq, sx, qs)
 
 
 def linear_w4a16(x, packed, sz, out=None, dev_status=None, stream=None):

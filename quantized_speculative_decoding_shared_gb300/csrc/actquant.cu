@@ -3,7 +3,8 @@
 // activations to 4 bits as well as the weights).
 //
 // Per (m, g): amax = max |x|, sx = amax / 7 (IEEE fp32 division),
-// q = clamp(rint(x / sx), -7, 7) (0 when sx == 0), qs = sum q.
+// q = clamp(rint(x / sx), -7, 7) (0 when sx == 0; the quotient through the
+// rounded reciprocal, the division itself near rounding ties), qs = sum q.
 // Half a warp per group: 16 lanes x 8 bf16 (one 16-byte load each), amax and
 // qs by shuffles over the half warp.  HBM-bound: 2 bytes read and ~0.53
 // bytes written per element.
@@ -45,36 +46,9 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
             const int m = (int)(w / pairs_per_row);
             const int g = (int)(w % pairs_per_row) * 2 + half;
             const bool active = w < tasks && g < G;
-            float f[8];
-            const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                f[2 * i] = __uint_as_float(wv[i] << 16);
-                f[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                bad |= !isfinite(f[i]);
-                amax = fmaxf(amax, fabsf(f[i]));
-            }
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            float scale = __fdiv_rn(amax, 7.0f);
-            int sum = 0;
-            uint32_t nib = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                int q = 0;
-                if (scale != 0.0f) {
-                    q = __float2int_rn(__fdiv_rn(f[i], scale));
-                    q = max(-7, min(7, q));
-                }
-                sum += q;
-                nib |= (uint32_t)(q & 15) << (4 * i);
-            }
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            float scale;
+            int sum;
+            const uint32_t nib = quant_group_halfwarp(v[j], scale, sum, bad);
             if (active) {
                 reinterpret_cast<uint32_t *>(xq + (size_t)m * (K / 2) + (size_t)g * (kGroup / 2))[hl] = nib;
                 if (hl == 0) {

@@ -142,6 +142,59 @@ __device__ __forceinline__ uint64_t fixed_weight(float l, float m) {
     return v >= 4294967296.0f ? (1ull << 32) : (uint64_t)__float2uint_rn(v);
 }
 
+// One activation code of the a2 quantiser, q = clamp(rint(x / sx), -7, 7),
+// with rs = 1 / sx rounded to nearest.  t = x * rs differs from the
+// correctly rounded quotient fl(x / sx) by at most |x / sx| * 2^-23 + 2^-24
+// relative, i.e. below 1.4e-6 since |x / sx| <= 7 (1 + 2^-23); so rint(t) and
+// rint(fl(x / sx)) can differ only when t lies within that distance of a
+// half-integer.  Within 1e-5 of one (or for a tiny sx, whose reciprocal may
+// overflow) the IEEE division decides, so the result is the division's.
+__device__ __forceinline__ int quant_code(float x, float sx, float rs) {
+    const float t = __fmul_rn(x, rs);
+    float n = rintf(t);
+    if (sx < 1.0e-30f || fabsf(fabsf(__fsub_rn(t, n)) - 0.5f) < 1.0e-5f) n = rintf(__fdiv_rn(x, sx));
+    return max(-7, min(7, (int)n));
+}
+
+// a2 quantisation of one 128-element group by half a warp (16 lanes x 8
+// bf16 in one 16-byte word each; both halves of the warp take part, each
+// with its own group): amax over the group, sx = amax / 7 (IEEE division),
+// q = clamp(rint(x / sx), -7, 7) (0 when sx == 0), qs = sum q over the group.
+// Returns this lane's 8 codes as nibbles (two's complement, code i in bits
+// 4i..4i+3); `bad` is set by a NaN or inf input.  Shared by the quantiser and
+// the kernels that quantise their own activations, so all agree bit for bit.
+__device__ __forceinline__ uint32_t quant_group_halfwarp(uint4 v, float &scale, int &qsum, bool &bad) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        bad |= !isfinite(f[i]);
+        amax = fmaxf(amax, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    scale = __fdiv_rn(amax, 7.0f);
+    const float rs = __frcp_rn(scale);
+    int sum = 0;
+    uint32_t nib = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int q = scale != 0.0f ? quant_code(f[i], scale, rs) : 0;
+        sum += q;
+        nib |= (uint32_t)(q & 15) << (4 * i);
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    qsum = sum;
+    return nib;
+}
+
 typedef unsigned __int128 u128;
 
 }  // namespace qspec

@@ -133,7 +133,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     w4a4_hmma_gemv_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx,
                           const int32_t *__restrict__ qs, const uint8_t *__restrict__ packed,
                           const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
-                          int32_t *__restrict__ dbg_I) {
+                          int32_t *__restrict__ dbg_I, const uint16_t *__restrict__ x, int ldx,
+                          uint8_t *__restrict__ xq_out, float *__restrict__ sx_out, int32_t *__restrict__ qs_out,
+                          int32_t *__restrict__ st) {
     static_assert(MT >= 1 && MT <= 8 && (MT == 1 || MT % 2 == 0), "one n8 block of tokens");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int G = K / kGroup;
@@ -216,24 +218,54 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     pdl_wait();
 
     // token fragments, one thread per activation word (8 codes); the 16 words
-    // of a group sit in 16 consecutive lanes, which reduce the group offset
+    // of a group sit in 16 consecutive lanes, which reduce the group offset.
+    // With x given, the words come from quantising x here (the a2 step, the
+    // same routine as the quantiser; CTA column 0 also stores xq, sx, qs).
     const int wpr = K / 8;
+    const bool fused = x != nullptr;
+    bool bad = false;
     const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
     constexpr int kBatch = 4;                              // loads in flight per thread
     for (int base = 0; base < MT * wpr; base += kBatch * kThreads) {
+        uint4 xv[kBatch];
         uint32_t wv[kBatch];
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
             const int i = base + b * kThreads + threadIdx.x;
             const int t = i / wpr, wi = i - t * wpr;
-            wv[b] = i < MT * wpr && tok0 + t < M ? xw[(size_t)(tok0 + t) * wpr + wi] : 0u;
+            const bool live = i < MT * wpr && tok0 + t < M;
+            if (fused)
+                xv[b] = live ? *reinterpret_cast<const uint4 *>(x + (size_t)(tok0 + t) * ldx + (size_t)wi * 8)
+                             : make_uint4(0u, 0u, 0u, 0u);
+            else
+                wv[b] = live ? xw[(size_t)(tok0 + t) * wpr + wi] : 0u;
         }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
             const int i = base + b * kThreads + threadIdx.x;
             const bool valid = i < MT * wpr;
             const int t = valid ? i / wpr : 0, wi = i - t * wpr;
-            const uint32_t w = wv[b];
+            const bool live = valid && tok0 + t < M;
+            uint32_t w = wv[b];
+            if (fused) {
+                float scale;
+                int qsum;
+                w = quant_group_halfwarp(xv[b], scale, qsum, bad);
+                if (live) {
+                    const int m = tok0 + t, g = wi >> 4;
+                    if ((wi & 15) == 0) {
+                        sxs[t * G + g] = scale;
+                        oq[g * MT + t].y = (float)qsum;
+                    }
+                    if (blockIdx.x == 0) {
+                        reinterpret_cast<uint32_t *>(xq_out + (size_t)m * (K / 2))[wi] = w;
+                        if ((wi & 15) == 0) {
+                            sx_out[(size_t)m * G + g] = scale;
+                            qs_out[(size_t)m * G + g] = qsum;
+                        }
+                    }
+                }
+            }
             float q[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) q[e] = act_code(w, e);
@@ -252,9 +284,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     for (int i = threadIdx.x; i < (int)tstride; i += kThreads) bfr[(size_t)MT * tstride + i] = make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < MT * G; i += kThreads) {
         const int t = i / G, g = i - t * G, m = tok0 + t;
+        if (fused && m < M) continue;                    // set while quantising
         oq[g * MT + t].y = m < M ? (float)qs[(size_t)m * G + g] : 0.0f;
         sxs[i] = m < M ? sx[(size_t)m * G + g] : 0.0f;
     }
+    if (bad) flag(st, QSPEC_ERR_NONFINITE);
     __syncthreads();
 
     // lanes of absent token columns read the zero slot
@@ -352,9 +386,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     for (; cur < my_tiles; ++cur) tile_done(cur);
 }
 
+// Quantised activations as input (x == nullptr), or bf16 x quantised in the
+// kernel with xq, sx, qs stored as outputs.
+struct Act {
+    const uint8_t *xq;
+    const float *sx;
+    const int32_t *qs;
+    const uint16_t *x;
+    int ldx;
+    uint8_t *xq_out;
+    float *sx_out;
+    int32_t *qs_out;
+};
+
 template <int MT, int PF = 1, int MINB = 2>
-int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed, const uint32_t *sz, int M,
-           int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, cudaStream_t st, int ctas_per_sm = MINB) {
+int launch(const Act &a, const uint8_t *packed, const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy,
+           int32_t *dbg_I, int32_t *dev_status, cudaStream_t st, int ctas_per_sm = MINB) {
     const size_t smem = smem_bytes(MT, K);
     auto kern = w4a4_hmma_gemv_kernel<MT, PF, MINB>;
     int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 8 + MT, 200 * 1024);
@@ -362,9 +409,29 @@ int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t 
     const int n_tiles = (N + 15) / 16, token_tiles = (M + MT - 1) / MT;
     const int per_col = std::max(1, ctas_per_sm * sm_count() / token_tiles);
     dim3 grid((unsigned)std::min(n_tiles, per_col), (unsigned)token_tiles);
-    return launch_pdl("qspec_linear_w4a4", kern, grid, dim3(kThreads), smem, st, xq, sx, qs, packed, sz, M, N, K, y,
-                      ldy, dbg_I);
+    return launch_pdl("qspec_linear_w4a4", kern, grid, dim3(kThreads), smem, st, a.xq, a.sx, a.qs, packed, sz, M, N,
+                      K, y, ldy, dbg_I, a.x, a.ldx, a.xq_out, a.sx_out, a.qs_out, dev_status);
 }
+
+// warp-MMA path for M <= 32: QSPEC_ERR_SHAPE when the shape does not fit
+int launch_small(const Act &a, const uint8_t *packed, const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy,
+                 int32_t *dbg_I, int32_t *dev_status, cudaStream_t st) {
+    // tokens per CTA: up to 8 (one MMA column block), halved while two CTAs
+    // would not fit on an SM
+    constexpr size_t kTwoPerSm = 112 * 1024, kMaxSmem = 200 * 1024;
+    int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
+    while (mt > 1 && smem_bytes(mt, K) > kTwoPerSm) mt /= 2;
+    if (smem_bytes(mt, K) > kMaxSmem) return QSPEC_ERR_SHAPE;
+    switch (mt) {
+        case 1: return launch<1>(a, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, st);
+        case 2: return launch<2>(a, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, st);
+        case 4: return launch<4>(a, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, st);
+        default: return launch<8>(a, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, st);
+    }
+}
+
+// the tensor-memory GEMV takes 3..8 tokens when every SM gets a 128-row tile
+bool use_gemv_tc(int M, int N) { return M >= 3 && M <= 8 && (N + 127) / 128 >= sm_count(); }
 
 }  // namespace hm
 
@@ -389,20 +456,32 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
     if (M > 32) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
     // 3..8 tokens and at least one 128-row tile per SM: weights through TMA
     // and TMEM, MMAs async (at 1-2 tokens the warp-MMA kernel below is faster)
-    if (M >= 3 && M <= 8 && (N + 127) / 128 >= sm_count()) {
+    if (hm::use_gemv_tc(M, N)) {
         rc = launch_w4a4_gemv_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
         if (rc != QSPEC_ERR_SHAPE) return rc;
     }
-    // tokens per CTA: up to 8 (one MMA column block), halved while two CTAs
-    // would not fit on an SM
-    constexpr size_t kTwoPerSm = 112 * 1024, kMaxSmem = 200 * 1024;
-    int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
-    while (mt > 1 && hm::smem_bytes(mt, K) > kTwoPerSm) mt /= 2;
-    if (hm::smem_bytes(mt, K) > kMaxSmem) return QSPEC_ERR_SHAPE;
-    switch (mt) {
-        case 1: return hm::launch<1>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-        case 2: return hm::launch<2>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-        case 4: return hm::launch<4>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
-        default: return hm::launch<8>(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, st);
+    const hm::Act act = {xq, sx, qs, nullptr, 0, nullptr, nullptr, nullptr};
+    return hm::launch_small(act, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
+}
+
+extern "C" int qspec_linear_w4a4_bf16(const uint16_t *x_bf16, int ldx, const uint8_t *packed, const uint32_t *sz,
+                                      int M, int N, int K, uint16_t *y_bf16, int ldy, uint8_t *xq, float *sx,
+                                      int32_t *qs, int32_t *dbg_I, int32_t *dev_status, qspec_stream_t stream) {
+    if (!x_bf16 || !packed || !sz || !y_bf16 || !xq || !sx || !qs) return QSPEC_ERR_NULL;
+    if (M < 1 || N < 1 || K < kGroup || K % kGroup || ldx < K || ldy < N) return QSPEC_ERR_SHAPE;
+    if (!aligned(x_bf16, 16) || ldx % 8 || !aligned(xq, 16) || !aligned(sx, 4) || !aligned(qs, 4) ||
+        !aligned(packed, 16) || !aligned(sz, 4) || !aligned(y_bf16, 2) || (dbg_I && !aligned(dbg_I, 4)))
+        return QSPEC_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    cudaStream_t st = as_cuda(stream);
+    if (M <= 32 && !hm::use_gemv_tc(M, N)) {
+        const hm::Act act = {xq, sx, qs, x_bf16, ldx, xq, sx, qs};
+        rc = hm::launch_small(act, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
+        if (rc != QSPEC_ERR_SHAPE) return rc;
     }
+    // the other paths: the quantiser, then the linear on its outputs
+    rc = qspec_quant_act_int4(x_bf16, M, K, ldx, xq, sx, qs, dev_status, stream);
+    if (rc) return rc;
+    return qspec_linear_w4a4(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, stream);
 }

@@ -65,12 +65,16 @@ def test_null_and_shape_rejected_on_host(lib):
     assert lib.qspec_linear_w4a4(fake(), fake(), fake(), None, fake(), 1, 1, 128, fake(), 1,
                                  None, None, st) == 1
     assert lib.qspec_linear_w4a16(fake(), 128, fake(), fake(), 1, 1, 128, None, 1, None, st) == 1
+    assert lib.qspec_linear_w4a4_bf16(fake(), 128, fake(), fake(), 1, 1, 128, fake(), 1, None,
+                                      fake(), fake(), None, None, st) == 1
     # K not a multiple of 128, M < 1, gamma out of range, ld too small
     assert lib.qspec_pack_weights(fake(), fake(), fake(), 4, 100, fake(), fake(), None, st) == 2
     assert lib.qspec_quant_act_int4(fake(), 0, 128, 128, fake(), fake(), fake(), None, st) == 2
     assert lib.qspec_quant_act_int4(fake(), 1, 256, 128, fake(), fake(), fake(), None, st) == 2
     assert lib.qspec_linear_w4a16(fake(), 128, fake(), fake(), 1, 8, 128, fake(), 4, None,
                                   st) == 2
+    assert lib.qspec_linear_w4a4_bf16(fake(), 64, fake(), fake(), 1, 8, 128, fake(), 8, fake(),
+                                      fake(), fake(), None, None, st) == 2
     assert lib.qspec_verify_greedy(fake(), fake(), 1, 0, 10, fake(), fake(), fake(), 1 << 20,
                                    None, st) == 2
     assert lib.qspec_verify_greedy(fake(), fake(), 1, 17, 10, fake(), fake(), fake(), 1 << 20,
@@ -84,6 +88,8 @@ def test_alignment_and_workspace_rejected_on_host(lib):
     assert lib.qspec_pack_weights(fake(0x1001), fake(), fake(), 4, 128, fake(), fake(), None,
                                   st) == 3
     assert lib.qspec_quant_act_int4(fake(), 1, 128, 132, fake(), fake(), fake(), None, st) == 3
+    assert lib.qspec_linear_w4a4_bf16(fake(), 132, fake(), fake(), 1, 8, 128, fake(), 8, fake(),
+                                      fake(), fake(), None, None, st) == 3
     assert lib.qspec_kv_overwrite(fake(0x1008), fake(), fake(), fake(), fake(), fake(), 1, 1, 1,
                                   16, 8, 2, None, st) == 3
     need = binding.qspec_verify_workspace_bytes(2, 3, 1000)

@@ -168,3 +168,36 @@ def test_lm_head_decode_m1_m4():
     """The LM head (128256 x 4096) at draft M = 1 and M = 4, sampled outputs."""
     dev = need_gpu()
     sampled_compare([1, 4], [("lm_head", 128256, 4096)], 6, dev, outliers=0.01, w4a16=False, points=1024)
+
+
+# ----------------------------------------------------------------- quantiser fused into the linear
+@pytest.mark.parametrize("M,N,K,seed", [(1, 300, 1152, 30), (2, 4096, 4096, 31), (5, 96, 640, 32),
+                                        (8, 1000, 384, 33), (17, 64, 512, 34), (4, 19533, 1152, 35),
+                                        (40, 200, 256, 36), (1, 4096, 14336, 37)])
+def test_fused_quant_linear_equals_two_calls(M, N, K, seed):
+    """qspec_linear_w4a4_bf16 gives bit for bit what qspec_quant_act_int4 then
+    qspec_linear_w4a4 give (and the oracle), on every dispatch path."""
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100, outlier_frac=0.01).to(dev)
+    st = status(dev)
+    y, xq, sx, qs, I = q.linear_w4a4_bf16(x, packed, sz, want_I=True, dev_status=st)
+    assert read_status(st) == 0
+    xq2, sx2, qs2 = q.quant_act_int4(x)
+    y2, I2 = q.linear_w4a4(xq2, sx2, qs2, packed, sz, want_I=True)
+    assert torch.equal(xq, xq2) and torch.equal(qs, qs2) and torch.equal(sx, sx2)
+    assert torch.equal(I, I2) and np.array_equal(bits(y), bits(y2))
+    rc, xqo, sxo, qso = oracle.quant_act_int4(bits(x.cpu()))
+    y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert np.array_equal(xq.cpu().numpy(), xqo) and np.array_equal(I.cpu().numpy(), Io)
+    assert np.array_equal(bits(y), y4o)
+
+
+def test_fused_quant_linear_flags_nonfinite():
+    dev = need_gpu()
+    packed, sz, _, _ = make_layer(64, 256, 37, dev)
+    x = syn.activations(1, 256, 38).to(dev)
+    x[0, 5] = float("nan")
+    st = status(dev)
+    q.linear_w4a4_bf16(x, packed, sz, dev_status=st)
+    assert q.STATUS[read_status(st)] == "QSPEC_ERR_NONFINITE"
