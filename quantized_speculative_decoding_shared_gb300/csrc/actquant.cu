@@ -22,38 +22,46 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
     const int G = K / kGroup;
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4, hl = lane & 15;
-    const long long pairs_per_row = (G + 1) / 2;
-    long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-    const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int ppr = (G + 1) / 2;                             // group pairs per row
+    const int tasks = M * ppr;                               // one pair per warp-task
+    const int n_warps = (int)((gridDim.x * blockDim.x) >> 5);
+    int w0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    // (row, pair) of this warp's first task, then advanced by n_warps per task
+    // with one division per pass (no 64-bit division anywhere)
     bool bad = false;
     // kBatch pair-tasks per warp and pass, their loads issued first
     constexpr int kBatch = 4;
-    const long long tasks = (long long)M * pairs_per_row;
-    for (; warp < tasks; warp += kBatch * n_warps) {
+    for (; w0 < tasks; w0 += kBatch * n_warps) {
         uint4 v[kBatch];
+        int mm[kBatch], gg[kBatch];
+        int m = w0 / ppr, p = w0 - m * ppr;
+        const int dm = n_warps / ppr, dp = n_warps - dm * ppr;
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            const long long w = warp + j * n_warps;
-            const int m = (int)(w / pairs_per_row);
-            const int g = (int)(w % pairs_per_row) * 2 + half;
-            v[j] = w < tasks && g < G
-                       ? __ldcs(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup) + hl)
-                       : make_uint4(0, 0, 0, 0);
+            const int g = 2 * p + half;
+            const bool active = m < M && g < G;
+            mm[j] = active ? m : -1;
+            gg[j] = g;
+            v[j] = active ? __ldcs(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup) + hl)
+                          : make_uint4(0, 0, 0, 0);
+            m += dm;
+            p += dp;
+            if (p >= ppr) {
+                p -= ppr;
+                ++m;
+            }
         }
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            const long long w = warp + j * n_warps;
-            const int m = (int)(w / pairs_per_row);
-            const int g = (int)(w % pairs_per_row) * 2 + half;
-            const bool active = w < tasks && g < G;
             float scale;
             int sum;
             const uint32_t nib = quant_group_halfwarp(v[j], scale, sum, bad);
-            if (active) {
-                reinterpret_cast<uint32_t *>(xq + (size_t)m * (K / 2) + (size_t)g * (kGroup / 2))[hl] = nib;
+            if (mm[j] >= 0) {
+                const int mj = mm[j], g = gg[j];
+                reinterpret_cast<uint32_t *>(xq + (size_t)mj * (K / 2) + (size_t)g * (kGroup / 2))[hl] = nib;
                 if (hl == 0) {
-                    sx[(size_t)m * G + g] = scale;
-                    qs[(size_t)m * G + g] = sum;
+                    sx[(size_t)mj * G + g] = scale;
+                    qs[(size_t)mj * G + g] = sum;
                 }
             }
         }
@@ -70,6 +78,7 @@ extern "C" int qspec_quant_act_int4(const uint16_t *x_bf16, int M, int K, int ld
                                     qspec_stream_t stream) {
     if (!x_bf16 || !xq || !sx || !qs) return QSPEC_ERR_NULL;
     if (M < 1 || K < kGroup || K % kGroup || ldx < K) return QSPEC_ERR_SHAPE;
+    if ((long long)M * ((K / kGroup + 1) / 2) >= (1LL << 31)) return QSPEC_ERR_SHAPE;
     if (!aligned(x_bf16, 16) || ldx % 8 || !aligned(xq, 4) || !aligned(sx, 4) || !aligned(qs, 4))
         return QSPEC_ERR_ALIGN;
     int rc = check_device();

@@ -7,8 +7,9 @@
 // n_acc[b] are rewritten: the last confirmed token (whose K/V the first draft
 // step wrote) and the accepted drafts.
 //
-// Pure copy, HBM-bound: 16-byte loads and stores; consecutive threads walk one
-// D-row, then the heads of a position (contiguous in the verify-pass layout).
+// Pure copy, HBM-bound: 16-byte loads and stores; one CTA per (layer,
+// sequence, verify row), whose threads walk the H x D row (contiguous in the
+// verify-pass layout); rows past the accepted count return at once.
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -16,34 +17,34 @@
 
 namespace qspec {
 
-__global__ void __launch_bounds__(256) kv_overwrite_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
-                                                          const uint4 *__restrict__ kn,
-                                                          const uint4 *__restrict__ vn,
-                                                          const int32_t *__restrict__ base_pos,
-                                                          const int32_t *__restrict__ n_acc, int L, int B,
-                                                          int H, int T, int D, int gamma, int32_t *st) {
+// one CTA per (layer, sequence, verify row); its threads copy the H x D row
+// in 16-byte pieces (no per-element index arithmetic beyond one division)
+constexpr int kKvThreads = 128;
+
+__global__ void __launch_bounds__(kKvThreads) kv_overwrite_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
+                                                                 const uint4 *__restrict__ kn,
+                                                                 const uint4 *__restrict__ vn,
+                                                                 const int32_t *__restrict__ base_pos,
+                                                                 const int32_t *__restrict__ n_acc, int L, int B,
+                                                                 int H, int T, int D, int gamma, int32_t *st) {
     pdl_launch_dependents();
     pdl_wait();
-    const int D8 = D / 8;
-    const long long total = (long long)L * B * (gamma + 1) * H * D8;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        long long t = i;
-        const int c = (int)(t % D8); t /= D8;
-        const int h = (int)(t % H); t /= H;
-        const int r = (int)(t % (gamma + 1)); t /= (gamma + 1);
-        const int b = (int)(t % B);
-        const int l = (int)(t / B);
-        const int p0 = base_pos[b], a = n_acc[b];
-        if (p0 < 0 || a < 0 || a > gamma || p0 + a >= T) {
-            if (l == 0 && r == 0 && h == 0 && c == 0) flag(st, QSPEC_ERR_RANGE);
-            continue;
-        }
-        if (r > a) continue;
-        const size_t src = ((((size_t)l * B + b) * (gamma + 1) + r) * H + h) * D8 + c;
-        const size_t dst = ((((size_t)l * B + b) * H + h) * T + (size_t)(p0 + r)) * D8 + c;
-        kc[dst] = __ldcs(kn + src);
-        vc[dst] = __ldcs(vn + src);
+    const int D8 = D / 8, R = gamma + 1;
+    const int blk = blockIdx.x;                       // = (l * B + b) * R + r
+    const int r = blk % R, lb = blk / R, b = lb % B, l = lb / B;
+    const int p0 = base_pos[b], a = n_acc[b];
+    if (p0 < 0 || a < 0 || a > gamma || p0 + a >= T) {
+        if (l == 0 && r == 0 && threadIdx.x == 0) flag(st, QSPEC_ERR_RANGE);
+        return;
+    }
+    if (r > a) return;
+    const uint4 *ks = kn + (size_t)blk * H * D8, *vs = vn + (size_t)blk * H * D8;
+    const size_t head0 = ((size_t)l * B + b) * H;       // (l, b, h = 0) row of the cache
+    for (int e = threadIdx.x; e < H * D8; e += kKvThreads) {
+        const int h = e / D8, c = e - h * D8;
+        const size_t dst = ((head0 + h) * T + (size_t)(p0 + r)) * D8 + c;
+        kc[dst] = __ldcs(ks + e);
+        vc[dst] = __ldcs(vs + e);
     }
 }
 
@@ -63,9 +64,10 @@ extern "C" int qspec_kv_overwrite(uint16_t *k_cache, uint16_t *v_cache, const ui
         return QSPEC_ERR_ALIGN;
     int rc = check_device();
     if (rc) return rc;
-    long long total = (long long)L * B * (gamma + 1) * H * (D / 8);
-    unsigned grid = (unsigned)std::min<long long>((total + 255) / 256, (long long)sm_count() * 16);
-    return launch_pdl("qspec_kv_overwrite", kv_overwrite_kernel, dim3(grid), dim3(256), 0, as_cuda(stream),
+    const long long blocks = (long long)L * B * (gamma + 1);
+    if (blocks >= (1LL << 31) || (long long)H * (D / 8) >= (1LL << 31)) return QSPEC_ERR_SHAPE;
+    return launch_pdl("qspec_kv_overwrite", kv_overwrite_kernel, dim3((unsigned)blocks), dim3(kKvThreads), 0,
+                      as_cuda(stream),
                       reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
                       reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), base_pos,
                       n_acc, L, B, H, T, D, gamma, dev_status);
