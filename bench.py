@@ -104,7 +104,7 @@ def profile_case(name, reps):
         xq, sx, qs = q.quant_act_int4(x)
         for _ in range(reps):
             if name == "w4a4_m1":
-                q.linear_w4a4(xq, sx, qs, packed, sz)
+                q.linear_w4a4_bf16(x, packed, sz)
             elif name == "w4a16_m5":
                 q.linear_w4a16(x, packed, sz)
             else:
@@ -719,8 +719,11 @@ def main():
     peak, peak_kind = measured_peaks()
     ach4 = rnd_obj.bytes_draft_linears() / (t4 / 1e3) / 1e9
     ach16 = rnd_obj.bytes_verify_linears() / (t16 / 1e3) / 1e9
-    traffic = recorded_traffic("w4a4.cu")
-    roofline = {"bound": "hbm", "kernel": "w4a4_hmma_gemv_kernel (W4A4 linear, M = %d)" % wl["B"],
+    one_token = wl["B"] == 1
+    traffic = recorded_traffic("w4a4_dp4a.cu") if one_token else None
+    roofline = {"bound": "hbm",
+                "kernel": ("w4a4_dp4a_gemv_kernel (W4A4 linear, M = 1)" if one_token
+                           else "W4A4 linears, M = %d" % wl["B"]),
                 "achieved": round(ach4, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach4 / peak, 4), "peak_source": peak_kind,
                 "bytes_per_launch": rnd_obj.bytes_draft_linears() / n4,
@@ -729,7 +732,7 @@ def main():
                 # scaled by algorithmic bytes to the average launch above
                 "traffic": (round(traffic["dram_bytes_per_algorithmic_byte"] *
                                   rnd_obj.bytes_draft_linears() / n4)
-                            if traffic and wl["B"] == 1 else None)}
+                            if traffic else None)}
 
     # e2e: host buffers, copies inside the timed region
     host_in = [t.cpu().pin_memory() for t in rnd_obj.host_inputs()]

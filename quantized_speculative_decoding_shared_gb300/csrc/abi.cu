@@ -1,6 +1,7 @@
 // abi.cu -- version, status strings, error text, device checks.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "qspec_host.h"
 
@@ -48,19 +49,35 @@ int sm_count() {
     return g_sm_count[dev];
 }
 
-static unsigned char g_smem_set[kMaxDevices][64];
+// (device, kernel) pairs whose shared-memory limit is raised, with the
+// bytes set; guarded by a mutex (launches may come from several threads)
+struct SmemSet {
+    int dev;
+    const void *func;
+    int bytes;
+};
+static constexpr int kMaxSmemSets = 256;
+static SmemSet g_smem_set[kMaxSmemSets];
+static int g_n_smem_set = 0;
+static std::mutex g_smem_mu;
 
-int smem_limit_once(const void *func, int slot, int bytes) {
+int smem_limit_once(const void *func, int bytes) {
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= 64) return QSPEC_ERR_UNSUPPORTED;
-    if (g_smem_set[dev][slot]) return QSPEC_OK;
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    for (int i = 0; i < g_n_smem_set; ++i)
+        if (g_smem_set[i].dev == dev && g_smem_set[i].func == func && g_smem_set[i].bytes >= bytes) return QSPEC_OK;
     cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) {
         set_last_error("cudaFuncSetAttribute", e);
         return QSPEC_ERR_LAUNCH;
     }
-    g_smem_set[dev][slot] = 1;
+    for (int i = 0; i < g_n_smem_set; ++i)
+        if (g_smem_set[i].dev == dev && g_smem_set[i].func == func) {
+            g_smem_set[i].bytes = bytes;
+            return QSPEC_OK;
+        }
+    if (g_n_smem_set < kMaxSmemSets) g_smem_set[g_n_smem_set++] = {dev, func, bytes};
     return QSPEC_OK;
 }
 

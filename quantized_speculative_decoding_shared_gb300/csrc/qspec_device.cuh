@@ -142,57 +142,105 @@ __device__ __forceinline__ uint64_t fixed_weight(float l, float m) {
     return v >= 4294967296.0f ? (1ull << 32) : (uint64_t)__float2uint_rn(v);
 }
 
-// One activation code of the a2 quantiser, q = clamp(rint(x / sx), -7, 7),
-// with rs = 1 / sx rounded to nearest.  t = x * rs differs from the
-// correctly rounded quotient fl(x / sx) by at most |x / sx| * 2^-23 + 2^-24
-// relative, i.e. below 1.4e-6 since |x / sx| <= 7 (1 + 2^-23); so rint(t) and
-// rint(fl(x / sx)) can differ only when t lies within that distance of a
-// half-integer.  Within 1e-5 of one (or for a tiny sx, whose reciprocal may
-// overflow) the IEEE division decides, so the result is the division's.
-__device__ __forceinline__ int quant_code(float x, float sx, float rs) {
-    const float t = __fmul_rn(x, rs);
-    float n = rintf(t);
-    if (sx < 1.0e-30f || fabsf(fabsf(__fsub_rn(t, n)) - 0.5f) < 1.0e-5f) n = rintf(__fdiv_rn(x, sx));
-    return max(-7, min(7, (int)n));
+// Reciprocal of x within 1 ulp (the PTX rcp.approx instruction; subnormal x
+// flushes to zero and gives inf).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+    return r;
 }
 
-// a2 quantisation of one 128-element group by half a warp (16 lanes x 8
-// bf16 in one 16-byte word each; both halves of the warp take part, each
-// with its own group): amax over the group, sx = amax / 7 (IEEE division),
-// q = clamp(rint(x / sx), -7, 7) (0 when sx == 0), qs = sum q over the group.
-// Returns this lane's 8 codes as nibbles (two's complement, code i in bits
-// 4i..4i+3); `bad` is set by a NaN or inf input.  Shared by the quantiser and
-// the kernels that quantise their own activations, so all agree bit for bit.
-__device__ __forceinline__ uint32_t quant_group_halfwarp(uint4 v, float &scale, int &qsum, bool &bad) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float f[8];
+// a2 quantisation of one 128-element group by 16 / kVec lanes, each with
+// kVec 16-byte words of 8 bf16 (consecutive elements; the lanes of a group
+// are consecutive and aligned, and every lane of the warp takes part, each
+// group of lanes with its own group): amax over the group, sx = amax / 7
+// (IEEE division), q = clamp(rint(x / sx), -7, 7) (0 when sx == 0), qs =
+// sum q over the group.  nib[i] gets the codes of v[i] as nibbles (two's
+// complement, code e in bits 4e..4e+3); `bad` is set by a NaN or inf input.
+// Shared by the quantiser and the kernels that quantise their own
+// activations, so all agree bit for bit.
+//
+// The quotient x / sx is formed as t = x * rs with rs within 1 ulp of 1 / sx
+// (|rs sx - 1| <= 2^-23).  t then differs from the exact quotient by at
+// most |x / sx| (2^-23 + 2^-24 + 2^-47), below 1.3e-6 since |x / sx| <= 7
+// (1 + 2^-23), and the correctly rounded quotient fl(x / sx) lies within
+// 2^-24 |x / sx| < 4.2e-7 of the exact one; so rint(t) and rint(fl(x / sx))
+// can differ only when t lies within 1.7e-6 of a half-integer.  When any
+// element of a lane is within 1e-5 of one, or sx is below 1e-30 (its
+// reciprocal may overflow or flush), the lane redoes its elements with the
+// IEEE division, so the codes are always the division's.  rint(t) for |t| <
+// 2^22 is t + 1.5 * 2^23 rounded to nearest (even), whose low bits are then
+// the integer.
+template <int kVec>
+__device__ __forceinline__ void quant_group(const uint4 (&v)[kVec], float &scale, int &qsum, bool &bad,
+                                            uint32_t (&nib)[kVec]) {
+    static_assert(kVec == 1 || kVec == 2 || kVec == 4, "16, 8 or 4 lanes per group");
+    constexpr float kMagic = 12582912.0f;                  // 1.5 * 2^23
+    float f[kVec * 8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    for (int c = 0; c < kVec; ++c) {
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[8 * c + 2 * i] = __uint_as_float(w[i] << 16);
+            f[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
     }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kVec * 8; ++i) {
         bad |= !isfinite(f[i]);
         amax = fmaxf(amax, fabsf(f[i]));
     }
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    for (int o = 8 / kVec; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     scale = __fdiv_rn(amax, 7.0f);
-    const float rs = __frcp_rn(scale);
+    const bool tiny = scale < 1.0e-30f;                     // 0 included: then every x is 0
+    const float rs = tiny ? 0.0f : rcp_approx(scale);
+    bool redo = tiny && scale != 0.0f;
     int sum = 0;
-    uint32_t nib = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int q = scale != 0.0f ? quant_code(f[i], scale, rs) : 0;
-        sum += q;
-        nib |= (uint32_t)(q & 15) << (4 * i);
+    for (int c = 0; c < kVec; ++c) {
+        uint32_t n = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float t = __fmul_rn(f[8 * c + i], rs);
+            const float m = __fadd_rn(t, kMagic);
+            const float d = __fsub_rn(t, __fsub_rn(m, kMagic));  // t - rint(t)
+            redo |= fabsf(fabsf(d) - 0.5f) < 1.0e-5f;
+            const int q = max(-7, min(7, (int)(__float_as_uint(m) - 0x4B400000u)));
+            sum += q;
+            n |= (uint32_t)(q & 15) << (4 * i);
+        }
+        nib[c] = n;
+    }
+    if (__any_sync(0xffffffffu, redo)) {                     // rare: the IEEE division decides
+        if (redo) {
+            sum = 0;
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) {
+                uint32_t n = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int q = max(-7, min(7, (int)rintf(__fdiv_rn(f[8 * c + i], scale))));
+                    sum += q;
+                    n |= (uint32_t)(q & 15) << (4 * i);
+                }
+                nib[c] = n;
+            }
+        }
     }
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int o = 8 / kVec; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     qsum = sum;
-    return nib;
+}
+
+// The same by half a warp (16 lanes x one 16-byte word); returns the nibbles.
+__device__ __forceinline__ uint32_t quant_group_halfwarp(uint4 v, float &scale, int &qsum, bool &bad) {
+    const uint4 a[1] = {v};
+    uint32_t n[1];
+    quant_group<1>(a, scale, qsum, bad, n);
+    return n[0];
 }
 
 typedef unsigned __int128 u128;

@@ -27,10 +27,17 @@ inline cudaStream_t as_cuda(qspec_stream_t s) { return reinterpret_cast<cudaStre
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
-// Raise a kernel's dynamic shared-memory limit to `bytes`, once per device and
-// `slot` (each kernel variant passes its own slot < 64).  Call before a stream
-// capture: the first call on a device talks to the driver.
-int smem_limit_once(const void *func, int slot, int bytes);
+// Raise a kernel's dynamic shared-memory limit to at least `bytes`, once per
+// device and kernel.  Call before a stream capture: the first call for a
+// kernel on a device talks to the driver.
+int smem_limit_once(const void *func, int bytes);
+
+// One-token W4A4 on the byte dot-product unit (w4a4_dp4a.cu): xq, sx, qs as
+// input, or x (bf16) quantised in the kernel with xq_out, sx_out, qs_out
+// stored; QSPEC_ERR_SHAPE before any launch when K does not suit it.
+int launch_w4a4_dp4a(const uint8_t *xq, const float *sx, const int32_t *qs, const uint16_t *x, uint8_t *xq_out,
+                     float *sx_out, int32_t *qs_out, const uint8_t *packed, const uint32_t *sz, int N, int K,
+                     uint16_t *y, int32_t *dbg_I, int32_t *dev_status, cudaStream_t stream);
 
 // Large-M W4A16 on the tensor cores (w4a16_tc.cu).
 int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,

@@ -314,7 +314,7 @@ int launch_w4a16_w(const uint16_t *x, int ldx, const uint8_t *packed, const uint
                    uint16_t *y, int ldy, cudaStream_t st) {
     const size_t smem = smem_bytes(MT, M, K, kWarps);
     auto kern = w4a16_hmma_gemv_kernel<MT, 1, kWarps>;
-    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), (kWarps == 16 ? 48 : 24) + MT, 200 * 1024);
+    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 200 * 1024);
     if (rc) return rc;
     const int n_tiles = (N + 15) / 16, token_tiles = (M + MT - 1) / MT;
     const int per_col = std::max(1, (16 / kWarps) * sm_count() / token_tiles);

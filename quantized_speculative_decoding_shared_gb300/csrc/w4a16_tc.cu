@@ -317,7 +317,7 @@ int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t 
               uint16_t *y, int ldy, int32_t *st, cudaStream_t stream) {
     static_assert(sizeof(float) * BN * kTileN <= sizeof(Smem<BN>), "partials fit in the operand stages");
     const size_t smem = sizeof(Smem<BN>) + 1024;
-    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a16_umma_kernel<BN>), 32 + BN / 16, (int)smem);
+    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a16_umma_kernel<BN>), (int)smem);
     if (rc) return rc;
     const int n_tiles = (N + kTileN - 1) / kTileN, token_tiles = (M + BN - 1) / BN, G = K / kGroup;
     // split the groups over a cluster (2, 4 or 8 CTAs: sizes that pack into

@@ -12,9 +12,10 @@
 //   acc = 0; for g ascending: acc = fmaf((float) I, sx[m][g] * s[n][g], acc)
 //   y[m][n] = bf16_rn(acc)
 //
-// Small-M path (M <= 32, draft decode): f16 warp MMA on exact small
-// integers, described below; 3 <= M <= 8 with at least one 128-row tile per
-// SM: tensor-memory GEMV (w4a4_gemv_tc.cu).  Larger M: tcgen05 (w4a4_tc.cu).
+// One token (the B = 1 draft decode): byte dot products (w4a4_dp4a.cu).
+// Small M (2..32): f16 warp MMA on exact small integers, described below;
+// 3 <= M <= 8 with at least one 128-row tile per SM: tensor-memory GEMV
+// (w4a4_gemv_tc.cu).  Larger M: tcgen05 (w4a4_tc.cu).
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -404,7 +405,7 @@ int launch(const Act &a, const uint8_t *packed, const uint32_t *sz, int M, int N
            int32_t *dbg_I, int32_t *dev_status, cudaStream_t st, int ctas_per_sm = MINB) {
     const size_t smem = smem_bytes(MT, K);
     auto kern = w4a4_hmma_gemv_kernel<MT, PF, MINB>;
-    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 8 + MT, 200 * 1024);
+    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 200 * 1024);
     if (rc) return rc;
     const int n_tiles = (N + 15) / 16, token_tiles = (M + MT - 1) / MT;
     const int per_col = std::max(1, ctas_per_sm * sm_count() / token_tiles);
@@ -454,6 +455,11 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
     if (rc) return rc;
     cudaStream_t st = as_cuda(stream);
     if (M > 32) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
+    if (M == 1) {
+        rc = launch_w4a4_dp4a(xq, sx, qs, nullptr, nullptr, nullptr, nullptr, packed, sz, N, K, y_bf16, dbg_I,
+                              dev_status, st);
+        if (rc != QSPEC_ERR_SHAPE) return rc;
+    }
     // 3..8 tokens and at least one 128-row tile per SM: weights through TMA
     // and TMEM, MMAs async (at 1-2 tokens the warp-MMA kernel below is faster)
     if (hm::use_gemv_tc(M, N)) {
@@ -475,6 +481,11 @@ extern "C" int qspec_linear_w4a4_bf16(const uint16_t *x_bf16, int ldx, const uin
     int rc = check_device();
     if (rc) return rc;
     cudaStream_t st = as_cuda(stream);
+    if (M == 1) {
+        rc = launch_w4a4_dp4a(nullptr, nullptr, nullptr, x_bf16, xq, sx, qs, packed, sz, N, K, y_bf16, dbg_I,
+                              dev_status, st);
+        if (rc != QSPEC_ERR_SHAPE) return rc;
+    }
     if (M <= 32 && !hm::use_gemv_tc(M, N)) {
         const hm::Act act = {xq, sx, qs, x_bf16, ldx, xq, sx, qs};
         rc = hm::launch_small(act, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);

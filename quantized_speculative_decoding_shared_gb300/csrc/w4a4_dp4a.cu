@@ -1,0 +1,358 @@
+// w4a4_dp4a.cu -- a3 for a single token (M = 1, the draft decode shape):
+// the W4A4 linear on the integer byte dot-product unit.
+//
+// QSPEC summary page, background terms: W4A4 runs a low-precision kernel on
+// 4-bit weights and 4-bit activations with no dequantisation, accumulating in
+// INT32 before scaling to a 16-bit result.  Same bit-exact definition as the
+// other W4A4 paths:
+//   I[n][g] = sum_{k in g} q[k] (W[n][k] - z[n][g])
+//   acc = 0; for g ascending: acc = fmaf((float) I, sx[g] * s[n][g], acc)
+//   y[n] = bf16_rn(acc)
+//
+// At one token the f16 warp MMA wastes seven of its eight columns and the
+// kernel is bound by instruction issue, not by HBM.  Here a weight word (codes
+// c0..c7, low nibble = even k) feeds two 4-way byte dot products with no
+// unpacking beyond two masks:
+//   w & 0x0F0F0F0F = bytes (c0, c2, c4, c6)         times (16 q0, 16 q2, ...)
+//   w & 0xF0F0F0F0 = bytes (16 c1, 16 c3, ...)       times (q1, q3, ...)
+// so dp4a(lo, E) + dp4a(hi, O) = 16 sum_k c q exactly (unsigned weight bytes,
+// signed activation bytes: 16 q is in [-128, 112] even for the code -8).  The
+// activation bytes E, O are built once per CTA in shared memory.
+//
+// Work split: a unit is 512 contiguous bytes of one row (1024 codes = eight
+// groups), one 16-byte piece per lane.  Each CTA owns a contiguous, balanced
+// range of rows, walked in chunks of RC rows; in a chunk the warps take
+// units round-robin (at most kUnits each), with the next chunk's weights
+// loaded into registers while the current one is reduced.  After the four
+// lanes of a group combine their sums, each group's exact I and sx * s go to
+// shared memory, and one thread per row folds them in ascending group order
+// (overlapping the next chunk).  Every CTA builds the activation bytes of
+// the whole vector, quantising x itself when given.
+#include <algorithm>
+
+#include "qspec_device.cuh"
+#include "qspec_host.h"
+
+namespace qspec {
+
+namespace {
+
+namespace dq {
+
+constexpr int kSegGroups = 8;       // groups per unit (512 bytes of a row)
+constexpr int kUnits = 8;           // units per warp and chunk
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint8_t *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
+
+// activation word (codes q0..q7, two's complement nibbles) -> the byte
+// operands E' = (16 q0 - q1, 16 q2 - q3, ...) (mod 256) and O = (q1, q3, q5,
+// q7); `m8` is set when an even code is -8 (then 16 q0 - q1 may not fit a
+// signed byte)
+__device__ __forceinline__ void act_bytes(uint32_t nib, uint32_t &ep, uint32_t &o, bool &m8) {
+    const uint32_t lo = nib & 0x0F0F0F0Fu;
+    o = __vsub4(((nib >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u, 0x08080808u);
+    ep = __vsub4(lo << 4, o);
+    m8 |= __vcmpeq4(lo, 0x08080808u) != 0u;
+}
+
+// 16 x the dot product of one 16-byte weight piece with its activation
+// bytes, when no even code is -8:
+//   dp4a(w, O) + dp4a(w & 0x0F0F0F0F, E')
+//     = sum (c_e + 16 c_o) q_o + c_e (16 q_e - q_o) = 16 sum (c_e q_e + c_o q_o)
+__device__ __forceinline__ int piece_dot(const uint4 &w, const uint4 &ep, const uint4 &o) {
+    int p = 0;
+    p = dp4a_us(w.x, o.x, p);
+    p = dp4a_us(w.x & 0x0F0F0F0Fu, ep.x, p);
+    p = dp4a_us(w.y, o.y, p);
+    p = dp4a_us(w.y & 0x0F0F0F0Fu, ep.y, p);
+    p = dp4a_us(w.z, o.z, p);
+    p = dp4a_us(w.z & 0x0F0F0F0Fu, ep.z, p);
+    p = dp4a_us(w.w, o.w, p);
+    p = dp4a_us(w.w & 0x0F0F0F0Fu, ep.w, p);
+    return p;
+}
+
+// The same for any codes: E' + O = 16 q_e (mod 256, in [-128, 112]) against
+// the low nibbles, O against the high nibbles (16 c_o).
+__device__ __forceinline__ int piece_dot_any(const uint4 &w, const uint4 &ep, const uint4 &o) {
+    int p = 0;
+    p = dp4a_us(w.x & 0x0F0F0F0Fu, __vadd4(ep.x, o.x), p);
+    p = dp4a_us(w.x & 0xF0F0F0F0u, o.x, p);
+    p = dp4a_us(w.y & 0x0F0F0F0Fu, __vadd4(ep.y, o.y), p);
+    p = dp4a_us(w.y & 0xF0F0F0F0u, o.y, p);
+    p = dp4a_us(w.z & 0x0F0F0F0Fu, __vadd4(ep.z, o.z), p);
+    p = dp4a_us(w.z & 0xF0F0F0F0u, o.z, p);
+    p = dp4a_us(w.w & 0x0F0F0F0Fu, __vadd4(ep.w, o.w), p);
+    p = dp4a_us(w.w & 0xF0F0F0F0u, o.w, p);
+    return p;
+}
+
+// Shared memory: activation bytes uint4 [S][2][32] (E', O of each lane's
+// four words of a unit), sx float [G], qs float [G], (I, sx s) float2
+// [2][RC][G + 1].
+inline size_t smem_bytes(int K, int RC) {
+    const size_t G = (size_t)K / kGroup, S = (G + kSegGroups - 1) / kSegGroups;
+    return S * 64 * 16 + G * 8 + 2 * (size_t)RC * (G + 1) * 8;
+}
+
+// RC: rows per chunk (RC * S <= kWarps * kUnits).  x == nullptr: xq, sx, qs
+// are the quantised activations; else x (bf16) is quantised here and CTA 0
+// stores xq_out, sx_out, qs_out.  With 8 warps a CTA holds at most half of
+// an SM's registers, so the next launch's CTAs can start (and load their
+// weights) beside it.
+template <int kWarps>
+__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
+    w4a4_dp4a_gemv_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx,
+                          const int32_t *__restrict__ qs, const uint8_t *__restrict__ packed,
+                          const uint32_t *__restrict__ sz, int N, int K, int RC, uint16_t *__restrict__ y,
+                          int32_t *__restrict__ dbg_I, const uint16_t *__restrict__ x, uint8_t *__restrict__ xq_out,
+                          float *__restrict__ sx_out, int32_t *__restrict__ qs_out, int32_t *__restrict__ st) {
+    constexpr int kThreads = kWarps * 32;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int G = K / kGroup;
+    const int S = (G + kSegGroups - 1) / kSegGroups;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4 *act = reinterpret_cast<uint4 *>(smem_raw);
+    float *sxs = reinterpret_cast<float *>(act + (size_t)S * 64);
+    float *qss = sxs + G;
+    float2 *pairs = reinterpret_cast<float2 *>(qss + G);
+    const int pstride = G + 1;
+    const size_t row_bytes = (size_t)K / 2;
+
+    const int r_begin = (int)(((long long)blockIdx.x * N) / gridDim.x);
+    const int r_end = (int)(((long long)(blockIdx.x + 1) * N) / gridDim.x);
+    const int n_chunks = (r_end - r_begin + RC - 1) / RC;
+
+    // unit j of this warp in every chunk: u = warp + j * kWarps, row u / S,
+    // segment u % S (both below 128, kept as bytes); lanes whose group is
+    // past G load nothing
+    uint32_t rows_of[kUnits / 4] = {}, segs[kUnits / 4] = {};
+    uint32_t lane_ok = 0;
+#pragma unroll
+    for (int j = 0; j < kUnits; ++j) {
+        const int u = warp + j * kWarps, rl = u / S, sg = u - rl * S;
+        rows_of[j / 4] |= (uint32_t)(rl & 0xFF) << (8 * (j % 4));
+        segs[j / 4] |= (uint32_t)sg << (8 * (j % 4));
+        if (sg * kSegGroups + (lane >> 2) < G) lane_ok |= 1u << j;
+    }
+    const uint8_t *lane_base = packed + (size_t)lane * 16;
+    // after the reduction of batch b, lane 4 g' + i holds unit 4 b + i, group
+    // g' of its segment: the same unit, row slot and group in every chunk
+    int eu[2], erl[2], eg[2];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        eu[b] = warp + (4 * b + (lane & 3)) * kWarps;
+        erl[b] = eu[b] / S;
+        eg[b] = (eu[b] - erl[b] * S) * kSegGroups + (lane >> 2);
+        if (eg[b] >= G) eu[b] = 1 << 30;                  // never valid
+    }
+
+    // weights are read once: first out of L2
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(policy));
+    auto chunk_rows = [&](int c) { return min(RC, r_end - (r_begin + c * RC)); };
+    auto load = [&](int c, uint4 (&v)[kUnits], uint32_t (&zw)[2]) {
+        const int row0 = r_begin + c * RC, n_units = chunk_rows(c) * S;
+        const uint8_t *base = lane_base + (size_t)row0 * row_bytes;
+#pragma unroll
+        for (int j = 0; j < kUnits; ++j) {
+            const uint32_t off = ((rows_of[j / 4] >> (8 * (j % 4))) & 0xFFu) * (uint32_t)row_bytes +
+                                 ((segs[j / 4] >> (8 * (j % 4))) & 0xFFu) * 512u;
+            if (warp + j * kWarps < n_units && (lane_ok >> j & 1u)) {
+                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;\n"
+                             : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
+                             : "l"(base + off), "l"(policy));
+            } else {
+                v[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+            zw[b] = eu[b] < n_units ? __ldg(sz + (size_t)(row0 + erl[b]) * G + eg[b]) : 0u;
+    };
+
+    pdl_launch_dependents();
+    uint4 va[kUnits], vb[kUnits];
+    uint32_t za[2], zb[2];
+    if (n_chunks > 0) load(0, va, za);                   // immutable weights before the wait
+    pdl_wait();
+
+    // activation bytes, per-group sx and qs; all of a pass's loads first
+    bool bad = false, m8 = false;
+    const int words = K / 8;
+    auto put_word = [&](int wi, uint32_t nib) {
+        uint32_t ep, o;
+        act_bytes(nib, ep, o, m8);
+        uint32_t *a = reinterpret_cast<uint32_t *>(act + (size_t)(wi >> 7) * 64 + ((wi >> 2) & 31));
+        a[wi & 3] = ep;
+        a[128 + (wi & 3)] = o;
+    };
+    if (x == nullptr) {
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
+        constexpr int kB = 4;
+        for (int w0 = threadIdx.x; w0 < S * 128; w0 += kB * kThreads) {
+            uint32_t nw[kB];
+#pragma unroll
+            for (int i = 0; i < kB; ++i) nw[i] = w0 + i * kThreads < words ? xw[w0 + i * kThreads] : 0u;
+#pragma unroll
+            for (int i = 0; i < kB; ++i)
+                if (w0 + i * kThreads < S * 128) put_word(w0 + i * kThreads, nw[i]);
+        }
+        for (int g = threadIdx.x; g < G; g += kThreads) {
+            sxs[g] = sx[g];
+            qss[g] = (float)qs[g];
+        }
+    } else {
+        // eight lanes per group, 16 elements each (two 16-byte words); CTA 0
+        // also stores xq, sx, qs
+        const int sub = lane >> 3, l8 = lane & 7;
+        constexpr int kPer = 4 * kWarps;                  // groups per pass
+        for (int g0 = 4 * warp; g0 < G; g0 += 2 * kPer) {
+            uint4 v[2][2];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int g = g0 + p * kPer + sub;
+                const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)g * kGroup) + 2 * l8;
+                v[p][0] = g < G ? src[0] : make_uint4(0u, 0u, 0u, 0u);
+                v[p][1] = g < G ? src[1] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int g = g0 + p * kPer + sub;
+                if (g0 + p * kPer >= G) break;            // warp-uniform
+                float scale;
+                int qsum;
+                uint32_t nib[2];
+                quant_group<2>(v[p], scale, qsum, bad, nib);
+                if (g < G) {
+                    const int wi = g * 16 + 2 * l8;
+                    put_word(wi, nib[0]);
+                    put_word(wi + 1, nib[1]);
+                    if (l8 == 0) {
+                        sxs[g] = scale;
+                        qss[g] = (float)qsum;
+                    }
+                    if (blockIdx.x == 0) {
+                        *reinterpret_cast<uint2 *>(xq_out + (size_t)wi * 4) = make_uint2(nib[0], nib[1]);
+                        if (l8 == 0) {
+                            sx_out[g] = scale;
+                            qs_out[g] = qsum;
+                        }
+                    }
+                }
+            }
+        }
+        // words of a partial last unit: zero (their weights load as zeros too)
+        for (int wi = words + threadIdx.x; wi < S * 128; wi += kThreads) put_word(wi, 0u);
+    }
+    if (bad) flag(st, QSPEC_ERR_NONFINITE);
+    const bool any_m8 = __syncthreads_or(m8);
+    // this lane's epilogue constants: sx and qs of its two groups, pair slots
+    float esx[2], eqs[2];
+    int pidx[2];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const int g = eg[b] < G ? eg[b] : 0;
+        esx[b] = sxs[g];
+        eqs[b] = qss[g];
+        pidx[b] = erl[b] * pstride + eg[b];
+    }
+
+    // one thread per row folds the groups of chunk c in ascending order
+    auto fold = [&](int c) {
+        const int row0 = r_begin + c * RC, rows = chunk_rows(c);
+        const float2 *pb = pairs + (size_t)(c & 1) * RC * pstride;
+        for (int t = threadIdx.x; t < rows; t += kThreads) {
+            const float2 *pp = pb + (size_t)t * pstride;
+            float acc = 0.0f;
+#pragma unroll 4
+            for (int g = 0; g < G; ++g) {
+                const float2 v = pp[g];
+                acc = __fmaf_rn(v.x, v.y, acc);
+            }
+            y[row0 + t] = float_to_bf16_bits(acc);
+        }
+    };
+    // one chunk: the next chunk's loads, the previous chunk's fold, then the
+    // dot products and the group epilogue
+    auto step = [&](int c, uint4 (&cur)[kUnits], uint32_t (&zc)[2], uint4 (&nxt)[kUnits], uint32_t (&zn)[2]) {
+        if (c + 1 < n_chunks) load(c + 1, nxt, zn);
+        if (c > 0) fold(c - 1);
+        const int row0 = r_begin + c * RC, n_units = chunk_rows(c) * S;
+        float2 *pb = pairs + (size_t)(c & 1) * RC * pstride;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            int part[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * b + i;
+                const uint32_t a = ((segs[b] >> (8 * i)) & 0xFFu) * 64u + (uint32_t)lane;
+                const uint4 e = act[a], o = act[a + 32];
+                part[i] = any_m8 ? piece_dot_any(cur[j], e, o) : piece_dot(cur[j], e, o);
+            }
+            // quad transpose-reduce: lane 4 g' + i ends with unit 4 b + i
+            const int qi = lane & 3;
+            const bool odd = qi & 1, upper = qi & 2;
+            int k0 = odd ? part[1] : part[0], k1 = odd ? part[3] : part[2];
+            const int s0 = odd ? part[0] : part[1], s1 = odd ? part[2] : part[3];
+            k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+            k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+            int d16 = upper ? k1 : k0;
+            d16 += __shfl_xor_sync(0xffffffffu, upper ? k0 : k1, 2);
+            if (eu[b] < n_units) {
+                const float I = __fmaf_rn(-half_hi(zc[b]), eqs[b], (float)(d16 >> 4));
+                pb[pidx[b]] = make_float2(I, __fmul_rn(esx[b], half_lo(zc[b])));
+                if (dbg_I) dbg_I[(size_t)(row0 + erl[b]) * G + eg[b]] = (int32_t)I;
+            }
+        }
+        __syncthreads();
+    };
+    for (int c = 0; c < n_chunks; c += 2) {
+        step(c, va, za, vb, zb);
+        if (c + 1 < n_chunks) step(c + 1, vb, zb, va, za);
+    }
+    if (n_chunks > 0) fold(n_chunks - 1);
+}
+
+}  // namespace dq
+
+}  // namespace
+
+// One token: QSPEC_ERR_SHAPE before any launch when K is too long for a chunk
+// of one row (more than 128 units of 1024 codes).
+int launch_w4a4_dp4a(const uint8_t *xq, const float *sx, const int32_t *qs, const uint16_t *x, uint8_t *xq_out,
+                     float *sx_out, int32_t *qs_out, const uint8_t *packed, const uint32_t *sz, int N, int K,
+                     uint16_t *y, int32_t *dbg_I, int32_t *dev_status, cudaStream_t stream) {
+    const int G = K / kGroup, S = (G + dq::kSegGroups - 1) / dq::kSegGroups;
+    // up to 8 units per row: two 8-warp CTAs per SM; longer rows: one
+    // 16-warp CTA per SM (more rows per chunk, fewer chunk boundaries)
+    const int warps = S > 8 ? 16 : 8, per_sm = S > 8 ? 1 : 2;
+    if (S > warps * dq::kUnits) return QSPEC_ERR_SHAPE;
+    const int ctas = std::min(sm_count() * per_sm, N);
+    const int rows_per_cta = (N + ctas - 1) / ctas;
+    const int RC = std::min(warps * dq::kUnits / S, rows_per_cta);
+    const size_t smem = dq::smem_bytes(K, RC);
+    if (smem > 200 * 1024) return QSPEC_ERR_SHAPE;
+    auto kern = warps == 16 ? dq::w4a4_dp4a_gemv_kernel<16> : dq::w4a4_dp4a_gemv_kernel<8>;
+    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 200 * 1024);
+    if (rc) return rc;
+    return launch_pdl("qspec_linear_w4a4", kern, dim3((unsigned)ctas), dim3(warps * 32), smem, stream, xq, sx, qs,
+                      packed, sz, N, K, RC, y, dbg_I, x, xq_out, sx_out, qs_out, dev_status);
+}
+
+}  // namespace qspec

@@ -327,7 +327,7 @@ int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t 
     int rc = weight_tmap(&tmap, packed, N, K, 128);
     if (rc) return QSPEC_ERR_SHAPE;
     auto kern = w4a4_gemv_tc_kernel<MT>;
-    rc = smem_limit_once(reinterpret_cast<const void *>(kern), 40 + MT, (int)kBudget);
+    rc = smem_limit_once(reinterpret_cast<const void *>(kern), (int)kBudget);
     if (rc) return rc;
     const int n_tiles = (N + 127) / 128, token_tiles = (M + MT - 1) / MT;
     const int per_col = std::max(1, sm_count() / token_tiles);

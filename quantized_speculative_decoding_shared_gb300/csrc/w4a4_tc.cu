@@ -289,7 +289,7 @@ template <int BN>
 int launch_bn(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed, const uint32_t *sz,
               int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st, cudaStream_t stream) {
     const size_t smem = sizeof(Smem<BN>) + 1024;
-    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN>), 16 + BN / 32, (int)smem);
+    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN>), (int)smem);
     if (rc) return rc;
     dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + BN - 1) / BN));
     return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, xq, sx, qs,

@@ -201,3 +201,75 @@ def test_fused_quant_linear_flags_nonfinite():
     st = status(dev)
     q.linear_w4a4_bf16(x, packed, sz, dev_status=st)
     assert q.STATUS[read_status(st)] == "QSPEC_ERR_NONFINITE"
+
+
+# ----------------------------------------------------------------- one token: byte dot products
+# Rows split over every SM in balanced ranges, walked in chunks of up to
+# 64 / S or 128 / S rows (S = units of 1024 codes per row); clusters of 8,
+# 4 or 1 CTAs share the activations.  Covered: fewer rows than SMs, one and
+# several chunks per CTA, a partial last unit (K % 1024 != 0), fewer groups
+# than CTAs in a cluster, S = 64 and the largest S = 128.
+@pytest.mark.parametrize("N,K,seed", [(5, 128, 40), (151, 1024, 41), (6083, 4096, 42), (300, 1152, 43),
+                                      (40, 65536, 44), (24, 131072, 45), (152 * 33 + 7, 14336, 46),
+                                      (16, 128, 49), (24, 768, 50)])
+def test_one_token_full_compare(N, K, seed):
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(1, K, seed + 100, outlier_frac=0.01)
+    (y4, I), xqo, sxo = run_w4a4(x, packed, sz, dev)
+    y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert np.array_equal(I.cpu().numpy(), Io)
+    assert np.array_equal(bits(y4), y4o)
+    y, xq, sx, qs, I2 = q.linear_w4a4_bf16(x.to(dev), packed, sz, want_I=True)
+    assert np.array_equal(xq.cpu().numpy(), xqo) and np.array_equal(I2.cpu().numpy(), Io)
+    assert np.array_equal(bits(y), y4o)
+
+
+@pytest.mark.parametrize("where", ["everywhere", "last_group_only", "none"])
+def test_one_token_every_activation_code(where):
+    """Quantised activations given directly with every nibble value, -8
+    included (the quantiser never emits it; the definition covers it): -8 at
+    random places, once in the last group only (the CTA that builds that
+    group must tell the others of its cluster), or nowhere."""
+    dev = need_gpu()
+    N, K = 700, 2048
+    G = K // 128
+    packed, sz, po, szo = make_layer(N, K, 47, dev)
+    rng = np.random.default_rng(47)
+    if where == "everywhere":
+        xq = rng.integers(0, 256, (1, K // 2), dtype=np.uint8)
+        xq[0, :8] = 0x88                              # a run of -8 codes
+    else:
+        c = rng.integers(-7, 8, (1, K)).astype(np.int64) & 15
+        xq = (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+        if where == "last_group_only":
+            xq[0, K // 2 - 10] = (xq[0, K // 2 - 10] & 0xF0) | 0x08     # even code -8, group G - 1
+    lo, hi = (xq & 15).astype(np.int32), (xq >> 4).astype(np.int32)
+    codes = np.stack([lo, hi], axis=-1).reshape(1, K)
+    codes = np.where(codes >= 8, codes - 16, codes)
+    qs = codes.reshape(1, G, 128).sum(-1).astype(np.int32)
+    sx = rng.uniform(0.01, 2.0, (1, G)).astype(np.float32)
+    y, I = q.linear_w4a4(torch.from_numpy(xq).to(dev), torch.from_numpy(sx).to(dev),
+                         torch.from_numpy(qs).to(dev), packed, sz, want_I=True)
+    yo, Io = oracle.linear_w4a4(xq, sx, po, szo, want_I=True)
+    assert np.array_equal(I.cpu().numpy(), Io) and np.array_equal(bits(y), yo)
+
+
+def test_one_token_extreme():
+    """|I| = 128 * 7 * 15 in both signs at one token."""
+    dev = need_gpu()
+    N, K = 333, 1152
+    G = K // 128
+    rng = np.random.default_rng(48)
+    codes = torch.from_numpy(rng.choice([0, 15], (N, K)).astype(np.uint8))
+    z = torch.from_numpy(rng.choice([0.0, 15.0], (N, G))).to(torch.float16)
+    s = torch.ones((N, G), dtype=torch.float16)
+    codes[0], codes[1], codes[N - 1] = 15, 0, 15
+    z[0], z[1], z[N - 1] = 0.0, 15.0, 0.0
+    x = torch.full((1, K), 7.0).to(torch.bfloat16)
+    packed, sz = q.pack_weights(codes.to(dev), s.to(dev), z.to(dev))
+    rc, po, szo = oracle.pack_weights(codes.numpy(), bits(s), bits(z))
+    (y4, I), xqo, sxo = run_w4a4(x, packed, sz, dev)
+    y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert Io[0, 0].max() == 128 * 7 * 15 and Io[0, 1].min() == -128 * 7 * 15
+    assert np.array_equal(I.cpu().numpy(), Io) and np.array_equal(bits(y4), y4o)

@@ -72,6 +72,8 @@ def test_quant_act_edge_values():
     x[3, :128] = 3.0                             # constant group: every q = 7
     x[4, ::2] = 0.5                              # many exact ties after scaling
     x[4, 0] = 3.5
+    x[4, 128] = 7.0                              # sx = 1: every other element an exact
+    x[4, 129:256] = (torch.arange(1, 128) % 14) - 6.5   # half-integer tie (to even)
     x[5, :128] = torch.arange(128) - 64.0        # exact integers
     xb = x.to(torch.bfloat16)
     st = status(dev)
