@@ -61,13 +61,17 @@ static SmemSet g_smem_set[kMaxSmemSets];
 static int g_n_smem_set = 0;
 static std::mutex g_smem_mu;
 
-int smem_limit_once(const void *func, int bytes) {
+int smem_limit_once(const void *func, int bytes, bool max_carveout) {
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(g_smem_mu);
     for (int i = 0; i < g_n_smem_set; ++i)
         if (g_smem_set[i].dev == dev && g_smem_set[i].func == func && g_smem_set[i].bytes >= bytes) return QSPEC_OK;
     cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    // optionally all of the unified L1 / shared array as shared memory, so
+    // that as many CTAs as the shared memory allows can be resident
+    if (e == cudaSuccess && max_carveout)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) {
         set_last_error("cudaFuncSetAttribute", e);
         return QSPEC_ERR_LAUNCH;

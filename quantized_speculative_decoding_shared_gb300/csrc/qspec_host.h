@@ -27,10 +27,11 @@ inline cudaStream_t as_cuda(qspec_stream_t s) { return reinterpret_cast<cudaStre
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
-// Raise a kernel's dynamic shared-memory limit to at least `bytes`, once per
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` (with
+// max_carveout, also prefer the largest shared-memory carveout), once per
 // device and kernel.  Call before a stream capture: the first call for a
 // kernel on a device talks to the driver.
-int smem_limit_once(const void *func, int bytes);
+int smem_limit_once(const void *func, int bytes, bool max_carveout = false);
 
 // One-token W4A4 on the byte dot-product unit (w4a4_dp4a.cu): xq, sx, qs as
 // input, or x (bf16) quantised in the kernel with xq_out, sx_out, qs_out

@@ -22,13 +22,15 @@
 // Work split: a unit is 512 contiguous bytes of one row (1024 codes = eight
 // groups), one 16-byte piece per lane.  Each CTA owns a contiguous, balanced
 // range of rows, walked in chunks of RC rows; in a chunk the warps take
-// units round-robin (at most kUnits each), with the next chunk's weights
-// loaded into registers while the current one is reduced.  After the four
+// units round-robin (at most kUnits each).  Each thread streams its pieces
+// into its own slots of a shared-memory ring with asynchronous copies, two
+// chunks ahead of the one being reduced.  After the four
 // lanes of a group combine their sums, each group's exact I and sx * s go to
 // shared memory, and one thread per row folds them in ascending group order
 // (overlapping the next chunk).  Every CTA builds the activation bytes of
 // the whole vector, quantising x itself when given.
 #include <algorithm>
+#include <type_traits>
 
 #include "qspec_device.cuh"
 #include "qspec_host.h"
@@ -48,12 +50,12 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const uint8_t *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
+// 16 bytes global -> shared, asynchronous; src_bytes 0 writes zeros and reads nothing
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, uint32_t src_bytes, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc), "r"(src_bytes), "l"(policy)
+                 : "memory");
 }
 
 __device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
@@ -102,53 +104,68 @@ __device__ __forceinline__ int piece_dot_any(const uint4 &w, const uint4 &ep, co
     return p;
 }
 
-// Shared memory: activation bytes uint4 [S][2][32] (E', O of each lane's
-// four words of a unit), sx float [G], qs float [G], (I, sx s) float2
-// [2][RC][G + 1].
-inline size_t smem_bytes(int K, int RC) {
+// Shared memory: the weight ring uint4 [P][kUnits][unit threads] (each
+// thread's own pieces of P chunks), activation bytes uint4 [S][2][32] (E', O
+// of each lane's four words of a unit), (I, sx s) float2 [2][RC][pstride >
+// G], sx float [G], qs float [G].
+inline size_t smem_bytes(int K, int RC, int unit_threads, int P) {
     const size_t G = (size_t)K / kGroup, S = (G + kSegGroups - 1) / kSegGroups;
-    return S * 64 * 16 + G * 8 + 2 * (size_t)RC * (G + 1) * 8;
+    const size_t pstride = (G + 13) / 16 * 16 + 2;
+    return (size_t)P * kUnits * unit_threads * 16 + S * 64 * 16 + G * 8 + 2 * (size_t)RC * pstride * 8;
 }
 
-// RC: rows per chunk (RC * S <= kWarps * kUnits).  x == nullptr: xq, sx, qs
-// are the quantised activations; else x (bf16) is quantised here and CTA 0
-// stores xq_out, sx_out, qs_out.  With 8 warps a CTA holds at most half of
-// an SM's registers, so the next launch's CTAs can start (and load their
-// weights) beside it.
-template <int kWarps>
-__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
+// blockDim.x / 32 <= kMaxWarps warps, the first nw of which reduce units
+// (the rest, if any, fold the groups); RC: rows per chunk (RC * S <= nw *
+// kUnits).  x == nullptr: xq, sx, qs are the quantised activations; else x
+// (bf16) is quantised here and CTA 0 stores xq_out, sx_out, qs_out.
+// kFixed: S divides nw, so every unit of a warp has the same segment
+// (warp % S) and the next unit's row is nw / S further; the warp keeps that
+// segment's activation bytes in registers.  kP: chunks of weights in the
+// shared-memory ring (kP - 1 in flight while one is reduced).
+template <int kMaxWarps, bool kFixed, int kP>
+__global__ void __launch_bounds__(kMaxWarps * 32, 16 / kMaxWarps)
     w4a4_dp4a_gemv_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx,
                           const int32_t *__restrict__ qs, const uint8_t *__restrict__ packed,
-                          const uint32_t *__restrict__ sz, int N, int K, int RC, uint16_t *__restrict__ y,
+                          const uint32_t *__restrict__ sz, int N, int K, int nw, int RC, uint16_t *__restrict__ y,
                           int32_t *__restrict__ dbg_I, const uint16_t *__restrict__ x, uint8_t *__restrict__ xq_out,
                           float *__restrict__ sx_out, int32_t *__restrict__ qs_out, int32_t *__restrict__ st) {
-    constexpr int kThreads = kWarps * 32;
+    const int kThreads = (int)blockDim.x, kCThreads = nw * 32;   // all threads, unit threads
+    const bool fold_warps = kThreads > kCThreads;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int G = K / kGroup;
     const int S = (G + kSegGroups - 1) / kSegGroups;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint4 *act = reinterpret_cast<uint4 *>(smem_raw);
-    float *sxs = reinterpret_cast<float *>(act + (size_t)S * 64);
+    uint4 *ring = reinterpret_cast<uint4 *>(smem_raw);
+    uint4 *act = ring + (size_t)kP * kUnits * kCThreads;
+    // (I, sx s) row stride: 16-byte aligned rows, consecutive rows 16 bytes
+    // apart modulo 128 (conflict-free 16-byte reads by consecutive threads)
+    const int pstride = (G + 13) / 16 * 16 + 2;
+    float2 *pairs = reinterpret_cast<float2 *>(act + (size_t)S * 64);
+    float *sxs = reinterpret_cast<float *>(pairs + (size_t)2 * RC * pstride);
     float *qss = sxs + G;
-    float2 *pairs = reinterpret_cast<float2 *>(qss + G);
-    const int pstride = G + 1;
     const size_t row_bytes = (size_t)K / 2;
 
     const int r_begin = (int)(((long long)blockIdx.x * N) / gridDim.x);
     const int r_end = (int)(((long long)(blockIdx.x + 1) * N) / gridDim.x);
     const int n_chunks = (r_end - r_begin + RC - 1) / RC;
 
-    // unit j of this warp in every chunk: u = warp + j * kWarps, row u / S,
+    // unit j of this warp in every chunk: u = warp + j * nw, row u / S,
     // segment u % S (both below 128, kept as bytes); lanes whose group is
     // past G load nothing
     uint32_t rows_of[kUnits / 4] = {}, segs[kUnits / 4] = {};
-    uint32_t lane_ok = 0;
+    uint32_t lane_ok = 0, off0 = 0, dj = 0;
+    if constexpr (kFixed) {
+        off0 = (uint32_t)(warp / S) * (uint32_t)row_bytes + (uint32_t)(warp % S) * 512u;
+        dj = (uint32_t)(nw / S) * (uint32_t)row_bytes;
+        lane_ok = ((warp % S) * kSegGroups + (lane >> 2) < G) ? 0xFFu : 0u;
+    } else {
 #pragma unroll
-    for (int j = 0; j < kUnits; ++j) {
-        const int u = warp + j * kWarps, rl = u / S, sg = u - rl * S;
-        rows_of[j / 4] |= (uint32_t)(rl & 0xFF) << (8 * (j % 4));
-        segs[j / 4] |= (uint32_t)sg << (8 * (j % 4));
-        if (sg * kSegGroups + (lane >> 2) < G) lane_ok |= 1u << j;
+        for (int j = 0; j < kUnits; ++j) {
+            const int u = warp + j * nw, rl = u / S, sg = u - rl * S;
+            rows_of[j / 4] |= (uint32_t)(rl & 0xFF) << (8 * (j % 4));
+            segs[j / 4] |= (uint32_t)sg << (8 * (j % 4));
+            if (sg * kSegGroups + (lane >> 2) < G) lane_ok |= 1u << j;
+        }
     }
     const uint8_t *lane_base = packed + (size_t)lane * 16;
     // after the reduction of batch b, lane 4 g' + i holds unit 4 b + i, group
@@ -156,7 +173,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
     int eu[2], erl[2], eg[2];
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
-        eu[b] = warp + (4 * b + (lane & 3)) * kWarps;
+        eu[b] = warp + (4 * b + (lane & 3)) * nw;
         erl[b] = eu[b] / S;
         eg[b] = (eu[b] - erl[b] * S) * kSegGroups + (lane >> 2);
         if (eg[b] >= G) eu[b] = 1 << 30;                  // never valid
@@ -166,30 +183,40 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(policy));
     auto chunk_rows = [&](int c) { return min(RC, r_end - (r_begin + c * RC)); };
-    auto load = [&](int c, uint4 (&v)[kUnits], uint32_t (&zw)[2]) {
-        const int row0 = r_begin + c * RC, n_units = chunk_rows(c) * S;
-        const uint8_t *base = lane_base + (size_t)row0 * row_bytes;
+    // chunk c's weight pieces into ring stage c % kP (each thread its own),
+    // one commit group per call, empty past the last chunk
+    auto issue = [&](int c) {
+        if (c < n_chunks) {
+            const int row0 = r_begin + c * RC, n_units = chunk_rows(c) * S;
+            const uint8_t *base = lane_base + (size_t)row0 * row_bytes;
+            uint4 *dst = ring + (size_t)(c % kP) * kUnits * kCThreads + threadIdx.x;
 #pragma unroll
-        for (int j = 0; j < kUnits; ++j) {
-            const uint32_t off = ((rows_of[j / 4] >> (8 * (j % 4))) & 0xFFu) * (uint32_t)row_bytes +
-                                 ((segs[j / 4] >> (8 * (j % 4))) & 0xFFu) * 512u;
-            if (warp + j * kWarps < n_units && (lane_ok >> j & 1u)) {
-                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;\n"
-                             : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
-                             : "l"(base + off), "l"(policy));
-            } else {
-                v[j] = make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < kUnits; ++j) {
+                const uint32_t off = kFixed ? off0 + (uint32_t)j * dj
+                                            : ((rows_of[j / 4] >> (8 * (j % 4))) & 0xFFu) * (uint32_t)row_bytes +
+                                                  ((segs[j / 4] >> (8 * (j % 4))) & 0xFFu) * 512u;
+                const bool ok = warp + j * nw < n_units && (lane_ok >> j & 1u);
+                cp_async16(dst + (size_t)j * kCThreads, ok ? base + off : packed, ok ? 16u : 0u, policy);
             }
         }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+    auto load_sz = [&](int c, uint32_t (&zw)[2]) {
+        const int row0 = r_begin + c * RC, n_units = chunk_rows(c) * S;
 #pragma unroll
         for (int b = 0; b < 2; ++b)
             zw[b] = eu[b] < n_units ? __ldg(sz + (size_t)(row0 + erl[b]) * G + eg[b]) : 0u;
     };
 
     pdl_launch_dependents();
-    uint4 va[kUnits], vb[kUnits];
-    uint32_t za[2], zb[2];
-    if (n_chunks > 0) load(0, va, za);                   // immutable weights before the wait
+    // immutable weights before the wait: the first kP - 1 chunks
+    const bool unit_warp = warp < nw;
+    uint32_t za[2] = {0u, 0u}, zb[2] = {0u, 0u};
+    if (unit_warp) {
+#pragma unroll
+        for (int c = 0; c < kP - 1; ++c) issue(c);
+        if (n_chunks > 0) load_sz(0, za);
+    }
     pdl_wait();
 
     // activation bytes, per-group sx and qs; all of a pass's loads first
@@ -206,12 +233,12 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
         const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
         constexpr int kB = 4;
         for (int w0 = threadIdx.x; w0 < S * 128; w0 += kB * kThreads) {
-            uint32_t nw[kB];
+            uint32_t xw4[kB];
 #pragma unroll
-            for (int i = 0; i < kB; ++i) nw[i] = w0 + i * kThreads < words ? xw[w0 + i * kThreads] : 0u;
+            for (int i = 0; i < kB; ++i) xw4[i] = w0 + i * kThreads < words ? xw[w0 + i * kThreads] : 0u;
 #pragma unroll
             for (int i = 0; i < kB; ++i)
-                if (w0 + i * kThreads < S * 128) put_word(w0 + i * kThreads, nw[i]);
+                if (w0 + i * kThreads < S * 128) put_word(w0 + i * kThreads, xw4[i]);
         }
         for (int g = threadIdx.x; g < G; g += kThreads) {
             sxs[g] = sx[g];
@@ -221,7 +248,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
         // eight lanes per group, 16 elements each (two 16-byte words); CTA 0
         // also stores xq, sx, qs
         const int sub = lane >> 3, l8 = lane & 7;
-        constexpr int kPer = 4 * kWarps;                  // groups per pass
+        const int kPer = kThreads / 8;                    // groups per pass: 4 per warp
         for (int g0 = 4 * warp; g0 < G; g0 += 2 * kPer) {
             uint4 v[2][2];
 #pragma unroll
@@ -262,6 +289,12 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
     }
     if (bad) flag(st, QSPEC_ERR_NONFINITE);
     const bool any_m8 = __syncthreads_or(m8);
+    // with a fixed segment, this lane's activation bytes for every unit
+    uint4 fe = make_uint4(0u, 0u, 0u, 0u), fo = fe;
+    if (kFixed && unit_warp) {
+        fe = act[(warp % S) * 64 + lane];
+        fo = act[(warp % S) * 64 + 32 + lane];
+    }
     // this lane's epilogue constants: sx and qs of its two groups, pair slots
     float esx[2], eqs[2];
     int pidx[2];
@@ -274,36 +307,64 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
     }
 
     // one thread per row folds the groups of chunk c in ascending order
+    // (the fold warps' threads when there are any, else every thread)
+    // (unit threads start past the last row when fold warps exist)
+    const int f0 = !fold_warps ? (int)threadIdx.x : unit_warp ? RC : (int)threadIdx.x - kCThreads;
+    const int fstep = fold_warps ? kThreads - kCThreads : kThreads;
     auto fold = [&](int c) {
         const int row0 = r_begin + c * RC, rows = chunk_rows(c);
         const float2 *pb = pairs + (size_t)(c & 1) * RC * pstride;
-        for (int t = threadIdx.x; t < rows; t += kThreads) {
-            const float2 *pp = pb + (size_t)t * pstride;
+        for (int t = f0; t < rows; t += fstep) {
+            const float4 *pp = reinterpret_cast<const float4 *>(pb + (size_t)t * pstride);
             float acc = 0.0f;
-#pragma unroll 4
-            for (int g = 0; g < G; ++g) {
-                const float2 v = pp[g];
+#pragma unroll 8
+            for (int h = 0; h < G / 2; ++h) {
+                const float4 v = pp[h];
+                acc = __fmaf_rn(v.x, v.y, acc);
+                acc = __fmaf_rn(v.z, v.w, acc);
+            }
+            if (G & 1) {
+                const float4 v = pp[G / 2];
                 acc = __fmaf_rn(v.x, v.y, acc);
             }
             y[row0 + t] = float_to_bf16_bits(acc);
         }
     };
-    // one chunk: the next chunk's loads, the previous chunk's fold, then the
-    // dot products and the group epilogue
-    auto step = [&](int c, uint4 (&cur)[kUnits], uint32_t (&zc)[2], uint4 (&nxt)[kUnits], uint32_t (&zn)[2]) {
-        if (c + 1 < n_chunks) load(c + 1, nxt, zn);
-        if (c > 0) fold(c - 1);
+    // one chunk: chunk c + kP - 1 into the stage chunk c - 1 left, the next
+    // chunk's scale words, the previous chunk's fold, then (once chunk c's
+    // pieces have landed) the dot products and the group epilogue
+    // (two copies of the loop: codes -8 present or not, decided once)
+    auto step = [&](auto any_tag, int c, uint32_t (&zc)[2], uint32_t (&zn)[2]) {
+        constexpr bool kAny = decltype(any_tag)::value;
+        if (!unit_warp) {
+            if (c > 0) fold(c - 1);
+            __syncthreads();
+            return;
+        }
+        issue(c + kP - 1);
+        if (c + 1 < n_chunks) load_sz(c + 1, zn);
+        if (c > 0 && !fold_warps) fold(c - 1);
+        asm volatile("cp.async.wait_group %0;\n" ::"n"(kP - 1) : "memory");
         const int row0 = r_begin + c * RC, n_units = chunk_rows(c) * S;
         float2 *pb = pairs + (size_t)(c & 1) * RC * pstride;
+        const uint4 *cur = ring + (size_t)(c % kP) * kUnits * kCThreads + threadIdx.x;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             int part[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int j = 4 * b + i;
-                const uint32_t a = ((segs[b] >> (8 * i)) & 0xFFu) * 64u + (uint32_t)lane;
-                const uint4 e = act[a], o = act[a + 32];
-                part[i] = any_m8 ? piece_dot_any(cur[j], e, o) : piece_dot(cur[j], e, o);
+                uint4 e = fe, o = fo;
+                if constexpr (!kFixed) {
+                    const uint32_t a = ((segs[b] >> (8 * i)) & 0xFFu) * 64u + (uint32_t)lane;
+                    e = act[a];
+                    o = act[a + 32];
+                }
+                const uint4 w = cur[(size_t)j * kCThreads];
+                if constexpr (kAny)
+                    part[i] = piece_dot_any(w, e, o);
+                else
+                    part[i] = piece_dot(w, e, o);
             }
             // quad transpose-reduce: lane 4 g' + i ends with unit 4 b + i
             const int qi = lane & 3;
@@ -322,11 +383,18 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
         }
         __syncthreads();
     };
-    for (int c = 0; c < n_chunks; c += 2) {
-        step(c, va, za, vb, zb);
-        if (c + 1 < n_chunks) step(c + 1, vb, zb, va, za);
-    }
+    auto run = [&](auto any_tag) {
+        for (int c = 0; c < n_chunks; c += 2) {
+            step(any_tag, c, za, zb);
+            if (c + 1 < n_chunks) step(any_tag, c + 1, zb, za);
+        }
+    };
+    if (any_m8)
+        run(std::true_type{});
+    else
+        run(std::false_type{});
     if (n_chunks > 0) fold(n_chunks - 1);
+    asm volatile("cp.async.wait_all;\n" ::: "memory");    // the empty tail groups
 }
 
 }  // namespace dq
@@ -339,20 +407,37 @@ int launch_w4a4_dp4a(const uint8_t *xq, const float *sx, const int32_t *qs, cons
                      float *sx_out, int32_t *qs_out, const uint8_t *packed, const uint32_t *sz, int N, int K,
                      uint16_t *y, int32_t *dbg_I, int32_t *dev_status, cudaStream_t stream) {
     const int G = K / kGroup, S = (G + dq::kSegGroups - 1) / dq::kSegGroups;
-    // up to 8 units per row: two 8-warp CTAs per SM; longer rows: one
-    // 16-warp CTA per SM (more rows per chunk, fewer chunk boundaries)
-    const int warps = S > 8 ? 16 : 8, per_sm = S > 8 ? 1 : 2;
+    // up to 8 units per row: two 8-warp CTAs per SM; longer rows: one 16-warp
+    // CTA.  When S <= warps, the unit warps are the largest multiple of S
+    // (each warp's segment fixed) and the others fold the groups.
+    const int max_w = S > 8 ? 16 : 8, per_sm = S > 8 ? 1 : 2;
+    const bool fixed = S <= max_w;
+    const int warps = fixed ? (max_w / S) * S : max_w;
     if (S > warps * dq::kUnits) return QSPEC_ERR_SHAPE;
     const int ctas = std::min(sm_count() * per_sm, N);
     const int rows_per_cta = (N + ctas - 1) / ctas;
     const int RC = std::min(warps * dq::kUnits / S, rows_per_cta);
-    const size_t smem = dq::smem_bytes(K, RC);
-    if (smem > 200 * 1024) return QSPEC_ERR_SHAPE;
-    auto kern = warps == 16 ? dq::w4a4_dp4a_gemv_kernel<16> : dq::w4a4_dp4a_gemv_kernel<8>;
-    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 200 * 1024);
+    // a ring of 3 chunks when it fits (two CTAs per SM: half the SM each);
+    // very long rows: 2, or 1 (no prefetch)
+    const size_t budget = per_sm == 2 ? 112 * 1024 : 227 * 1024;
+    int P = 3;
+    while (P > 1 && dq::smem_bytes(K, RC, warps * 32, P) > budget) --P;
+    const size_t smem = dq::smem_bytes(K, RC, warps * 32, P);
+    if (smem > budget || (P < 2 && (max_w == 8 || fixed))) return QSPEC_ERR_SHAPE;
+    void (*kern)(const uint8_t *, const float *, const int32_t *, const uint8_t *, const uint32_t *, int, int, int,
+                 int, uint16_t *, int32_t *, const uint16_t *, uint8_t *, float *, int32_t *, int32_t *);
+    if (max_w == 8)
+        kern = P == 3 ? dq::w4a4_dp4a_gemv_kernel<8, true, 3> : dq::w4a4_dp4a_gemv_kernel<8, true, 2>;
+    else if (fixed)
+        kern = P == 3 ? dq::w4a4_dp4a_gemv_kernel<16, true, 3> : dq::w4a4_dp4a_gemv_kernel<16, true, 2>;
+    else
+        kern = P == 3 ? dq::w4a4_dp4a_gemv_kernel<16, false, 3>
+               : P == 2 ? dq::w4a4_dp4a_gemv_kernel<16, false, 2>
+                        : dq::w4a4_dp4a_gemv_kernel<16, false, 1>;
+    int rc = smem_limit_once(reinterpret_cast<const void *>(kern), (int)smem, true);
     if (rc) return rc;
-    return launch_pdl("qspec_linear_w4a4", kern, dim3((unsigned)ctas), dim3(warps * 32), smem, stream, xq, sx, qs,
-                      packed, sz, N, K, RC, y, dbg_I, x, xq_out, sx_out, qs_out, dev_status);
+    return launch_pdl("qspec_linear_w4a4", kern, dim3((unsigned)ctas), dim3(max_w * 32), smem, stream, xq, sx, qs,
+                      packed, sz, N, K, warps, RC, y, dbg_I, x, xq_out, sx_out, qs_out, dev_status);
 }
 
 }  // namespace qspec

@@ -211,7 +211,12 @@ def test_fused_quant_linear_flags_nonfinite():
 # than CTAs in a cluster, S = 64 and the largest S = 128.
 @pytest.mark.parametrize("N,K,seed", [(5, 128, 40), (151, 1024, 41), (6083, 4096, 42), (300, 1152, 43),
                                       (40, 65536, 44), (24, 131072, 45), (152 * 33 + 7, 14336, 46),
-                                      (16, 128, 49), (24, 768, 50)])
+                                      (16, 128, 49), (24, 768, 50),
+                                      # warps per CTA a multiple of S: 6 (S = 3), 5 (S = 5),
+                                      # 9 (S = 9); S = 19 (Qwen2.5-7B down projection) takes
+                                      # the mixed-segment mapping
+                                      (700, 2560, 51), (333, 5120, 52), (200, 9216, 54),
+                                      (500, 18944, 53)])
 def test_one_token_full_compare(N, K, seed):
     dev = need_gpu()
     packed, sz, po, szo = make_layer(N, K, seed, dev)
