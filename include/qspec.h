@@ -95,6 +95,7 @@ int qspec_pack_weights(const uint8_t *codes, const uint16_t *s_fp16, const uint1
  *
  *   x_bf16 uint16 [M][ldx]  input rows (ldx >= K, ldx % 8 == 0, 16-byte aligned)
  *   xq     uint8  [M][K/2]  out: two's-complement nibbles, byte j = q[2j] | q[2j+1] << 4
+ *                           (8-byte aligned)
  *   sx     float  [M][G]    out: scales
  *   qs     int32  [M][G]    out: group sums of q
  * Device errors: QSPEC_ERR_NONFINITE (a NaN or inf input).

@@ -5,9 +5,9 @@
 // Per (m, g): amax = max |x|, sx = amax / 7 (IEEE fp32 division),
 // q = clamp(rint(x / sx), -7, 7) (0 when sx == 0; the quotient through the
 // rounded reciprocal, the division itself near rounding ties), qs = sum q.
-// Half a warp per group: 16 lanes x 8 bf16 (one 16-byte load each), amax and
-// qs by shuffles over the half warp.  HBM-bound: 2 bytes read and ~0.53
-// bytes written per element.
+// Eight lanes per group, four groups per warp: 8 lanes x 16 bf16 (two
+// 16-byte loads each), amax and qs by shuffles over the eight lanes.
+// HBM-bound: 2 bytes read and ~0.53 bytes written per element.
 #include "qspec_device.cuh"
 #include "qspec_host.h"
 
@@ -21,33 +21,33 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
     pdl_wait();
     const int G = K / kGroup;
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, hl = lane & 15;
-    const int ppr = (G + 1) / 2;                             // group pairs per row
-    const int tasks = M * ppr;                               // one pair per warp-task
+    const int sub = lane >> 3, l8 = lane & 7;               // group of the quad, lane in the group
+    const int qpr = (G + 3) / 4;                             // group quads per row
+    const int tasks = M * qpr;                               // one quad per warp-task
     const int n_warps = (int)((gridDim.x * blockDim.x) >> 5);
     int w0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    // (row, pair) of this warp's first task, then advanced by n_warps per task
-    // with one division per pass (no 64-bit division anywhere)
     bool bad = false;
-    // kBatch pair-tasks per warp and pass, their loads issued first
-    constexpr int kBatch = 4;
+    // kBatch quad-tasks per warp and pass, their loads issued first; (row,
+    // quad) stepped by n_warps per task with one division per pass
+    constexpr int kBatch = 2;
     for (; w0 < tasks; w0 += kBatch * n_warps) {
-        uint4 v[kBatch];
+        uint4 v[kBatch][2];
         int mm[kBatch], gg[kBatch];
-        int m = w0 / ppr, p = w0 - m * ppr;
-        const int dm = n_warps / ppr, dp = n_warps - dm * ppr;
+        int m = w0 / qpr, p = w0 - m * qpr;
+        const int dm = n_warps / qpr, dp = n_warps - dm * qpr;
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            const int g = 2 * p + half;
+            const int g = 4 * p + sub;
             const bool active = m < M && g < G;
             mm[j] = active ? m : -1;
             gg[j] = g;
-            v[j] = active ? __ldcs(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup) + hl)
-                          : make_uint4(0, 0, 0, 0);
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + (size_t)g * kGroup) + 2 * l8;
+            v[j][0] = active ? __ldcs(src) : make_uint4(0u, 0u, 0u, 0u);
+            v[j][1] = active ? __ldcs(src + 1) : make_uint4(0u, 0u, 0u, 0u);
             m += dm;
             p += dp;
-            if (p >= ppr) {
-                p -= ppr;
+            if (p >= qpr) {
+                p -= qpr;
                 ++m;
             }
         }
@@ -55,11 +55,13 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
         for (int j = 0; j < kBatch; ++j) {
             float scale;
             int sum;
-            const uint32_t nib = quant_group_halfwarp(v[j], scale, sum, bad);
+            uint32_t nib[2];
+            quant_group<2>(v[j], scale, sum, bad, nib);
             if (mm[j] >= 0) {
                 const int mj = mm[j], g = gg[j];
-                reinterpret_cast<uint32_t *>(xq + (size_t)mj * (K / 2) + (size_t)g * (kGroup / 2))[hl] = nib;
-                if (hl == 0) {
+                *reinterpret_cast<uint2 *>(xq + (size_t)mj * (K / 2) + (size_t)g * (kGroup / 2) + 8 * l8) =
+                    make_uint2(nib[0], nib[1]);
+                if (l8 == 0) {
                     sx[(size_t)mj * G + g] = scale;
                     qs[(size_t)mj * G + g] = sum;
                 }
@@ -78,12 +80,12 @@ extern "C" int qspec_quant_act_int4(const uint16_t *x_bf16, int M, int K, int ld
                                     qspec_stream_t stream) {
     if (!x_bf16 || !xq || !sx || !qs) return QSPEC_ERR_NULL;
     if (M < 1 || K < kGroup || K % kGroup || ldx < K) return QSPEC_ERR_SHAPE;
-    if ((long long)M * ((K / kGroup + 1) / 2) >= (1LL << 31)) return QSPEC_ERR_SHAPE;
-    if (!aligned(x_bf16, 16) || ldx % 8 || !aligned(xq, 4) || !aligned(sx, 4) || !aligned(qs, 4))
+    if ((long long)M * ((K / kGroup + 3) / 4) >= (1LL << 31)) return QSPEC_ERR_SHAPE;
+    if (!aligned(x_bf16, 16) || ldx % 8 || !aligned(xq, 8) || !aligned(sx, 4) || !aligned(qs, 4))
         return QSPEC_ERR_ALIGN;
     int rc = check_device();
     if (rc) return rc;
-    long long warps = (long long)M * ((K / kGroup + 1) / 2);
+    long long warps = (long long)M * ((K / kGroup + 3) / 4);
     long long blocks = (warps * 32 + 255) / 256;
     unsigned grid = (unsigned)std::min<long long>(blocks, (long long)sm_count() * 16);
     return launch_pdl("qspec_quant_act_int4", quant_act_kernel, dim3(grid), dim3(256), 0, as_cuda(stream),

@@ -166,11 +166,13 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // (1 + 2^-23), and the correctly rounded quotient fl(x / sx) lies within
 // 2^-24 |x / sx| < 4.2e-7 of the exact one; so rint(t) and rint(fl(x / sx))
 // can differ only when t lies within 1.7e-6 of a half-integer.  When any
-// element of a lane is within 1e-5 of one, or sx is below 1e-30 (its
-// reciprocal may overflow or flush), the lane redoes its elements with the
-// IEEE division, so the codes are always the division's.  rint(t) for |t| <
-// 2^22 is t + 1.5 * 2^23 rounded to nearest (even), whose low bits are then
-// the integer.
+// element of a lane is within 1e-5 of one (|t - rint(t)| >= 0.49999), or sx
+// is below 1e-30 (its reciprocal may overflow or flush), the lane redoes its
+// elements with the IEEE division, so the codes are always the division's.
+// Otherwise |t| <= 7.000002 and no clamp is needed.  rint(t) is t + 1.5 *
+// 2^23 rounded to nearest (even), whose low four bits are then the code; the
+// sum of the rounded values is exact, and not finite exactly when some
+// input is not (a NaN or inf x makes its t a NaN or inf).
 template <int kVec>
 __device__ __forceinline__ void quant_group(const uint4 (&v)[kVec], float &scale, int &qsum, bool &bad,
                                             uint32_t (&nib)[kVec]) {
@@ -186,34 +188,49 @@ __device__ __forceinline__ void quant_group(const uint4 (&v)[kVec], float &scale
             f[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         }
     }
-    float amax = 0.0f;
+    // (maxima, sums and nibble packing as trees: short dependency chains)
+    float a[kVec * 8];
 #pragma unroll
-    for (int i = 0; i < kVec * 8; ++i) {
-        bad |= !isfinite(f[i]);
-        amax = fmaxf(amax, fabsf(f[i]));
-    }
+    for (int i = 0; i < kVec * 8; ++i) a[i] = fabsf(f[i]);
+#pragma unroll
+    for (int w = kVec * 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) a[i] = fmaxf(a[i], a[i + w]);
+    float amax = a[0];
 #pragma unroll
     for (int o = 8 / kVec; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     scale = __fdiv_rn(amax, 7.0f);
     const bool tiny = scale < 1.0e-30f;                     // 0 included: then every x is 0
     const float rs = tiny ? 0.0f : rcp_approx(scale);
-    bool redo = tiny && scale != 0.0f;
-    int sum = 0;
+    float d[kVec * 8], r[kVec * 8];
+    uint32_t e[kVec * 8];
+#pragma unroll
+    for (int i = 0; i < kVec * 8; ++i) {
+        const float t = __fmul_rn(f[i], rs);
+        const float m = __fadd_rn(t, kMagic);
+        r[i] = __fsub_rn(m, kMagic);                          // rint(t)
+        d[i] = fabsf(__fsub_rn(t, r[i]));
+        e[i] = (__float_as_uint(m) & 15u) << (4 * (i & 7));
+    }
+#pragma unroll
+    for (int w = kVec * 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            d[i] = fmaxf(d[i], d[i + w]);
+            r[i] = __fadd_rn(r[i], r[i + w]);                 // integers: exact in any order
+        }
 #pragma unroll
     for (int c = 0; c < kVec; ++c) {
-        uint32_t n = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float t = __fmul_rn(f[8 * c + i], rs);
-            const float m = __fadd_rn(t, kMagic);
-            const float d = __fsub_rn(t, __fsub_rn(m, kMagic));  // t - rint(t)
-            redo |= fabsf(fabsf(d) - 0.5f) < 1.0e-5f;
-            const int q = max(-7, min(7, (int)(__float_as_uint(m) - 0x4B400000u)));
-            sum += q;
-            n |= (uint32_t)(q & 15) << (4 * i);
-        }
-        nib[c] = n;
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) e[8 * c + i] |= e[8 * c + i + w];
+        nib[c] = e[8 * c];
     }
+    const float dmax = d[0], qf = r[0];
+    bad |= !isfinite(qf);
+    int sum = (int)qf;
+    const bool redo = (tiny && scale != 0.0f) || dmax >= 0.49999f;
     if (__any_sync(0xffffffffu, redo)) {                     // rare: the IEEE division decides
         if (redo) {
             sum = 0;

@@ -58,6 +58,11 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, uin
                  : "memory");
 }
 
+// Block-wide barrier that warps may reach from different places in the code
+// (the non-aligned form): unit warps, fold warps and the two copies of the
+// chunk loop each meet it once per chunk.
+__device__ __forceinline__ void cta_barrier() { asm volatile("barrier.sync 0;\n" ::: "memory"); }
+
 __device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
 __device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
 
@@ -219,92 +224,145 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 16 / kMaxWarps)
     }
     pdl_wait();
 
-    // activation bytes, per-group sx and qs; all of a pass's loads first
-    bool bad = false, m8 = false;
-    const int words = K / 8;
-    auto put_word = [&](int wi, uint32_t nib) {
-        uint32_t ep, o;
-        act_bytes(nib, ep, o, m8);
-        uint32_t *a = reinterpret_cast<uint32_t *>(act + (size_t)(wi >> 7) * 64 + ((wi >> 2) & 31));
-        a[wi & 3] = ep;
-        a[128 + (wi & 3)] = o;
-    };
-    if (x == nullptr) {
-        const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
-        constexpr int kB = 4;
-        for (int w0 = threadIdx.x; w0 < S * 128; w0 += kB * kThreads) {
-            uint32_t xw4[kB];
+    // Activation bytes, and sx, qs of the epilogue groups.
+    //  kFixed, with the quantised activations given or one unit warp per
+    //   segment (nw == S): a warp's units all lie in segment warp % S, and
+    //   lane l's 16-byte pieces are codes 32 l .. 32 l + 31 of the segment,
+    //   a quarter of group l / 4: each unit warp builds (quantising x when
+    //   given, four lanes per group) exactly the bytes its lanes need, in
+    //   registers, with no block-wide step; its epilogue groups are its
+    //   lanes' own groups.
+    //  Otherwise (where quantising that way would repeat work): the CTA
+    //   builds the whole vector in shared memory, each group once.
+    bool bad = false, m8 = false, any_m8 = false;
+    uint4 fe = make_uint4(0u, 0u, 0u, 0u), fo = fe;
+    float esx[2] = {0.0f, 0.0f}, eqs[2] = {0.0f, 0.0f};
+    if (kFixed && (x == nullptr || nw == S)) {
+        if (unit_warp) {
+            const int sg = warp % S, g = sg * kSegGroups + (lane >> 2);
+            const bool live = g < G;
+            uint32_t nib[4] = {0u, 0u, 0u, 0u};
+            float scale = 0.0f, qsf = 0.0f;
+            if (x == nullptr) {
+                if (live) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(xq + (size_t)sg * 512 + lane * 16);
+                    nib[0] = w.x;
+                    nib[1] = w.y;
+                    nib[2] = w.z;
+                    nib[3] = w.w;
+                    scale = sx[g];
+                    qsf = (float)qs[g];
+                }
+            } else {
+                uint4 v[4];
+                const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)sg * 1024 + lane * 32);
 #pragma unroll
-            for (int i = 0; i < kB; ++i) xw4[i] = w0 + i * kThreads < words ? xw[w0 + i * kThreads] : 0u;
-#pragma unroll
-            for (int i = 0; i < kB; ++i)
-                if (w0 + i * kThreads < S * 128) put_word(w0 + i * kThreads, xw4[i]);
-        }
-        for (int g = threadIdx.x; g < G; g += kThreads) {
-            sxs[g] = sx[g];
-            qss[g] = (float)qs[g];
-        }
-    } else {
-        // eight lanes per group, 16 elements each (two 16-byte words); CTA 0
-        // also stores xq, sx, qs
-        const int sub = lane >> 3, l8 = lane & 7;
-        const int kPer = kThreads / 8;                    // groups per pass: 4 per warp
-        for (int g0 = 4 * warp; g0 < G; g0 += 2 * kPer) {
-            uint4 v[2][2];
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int g = g0 + p * kPer + sub;
-                const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)g * kGroup) + 2 * l8;
-                v[p][0] = g < G ? src[0] : make_uint4(0u, 0u, 0u, 0u);
-                v[p][1] = g < G ? src[1] : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int g = g0 + p * kPer + sub;
-                if (g0 + p * kPer >= G) break;            // warp-uniform
-                float scale;
+                for (int i = 0; i < 4; ++i) v[i] = live ? src[i] : make_uint4(0u, 0u, 0u, 0u);
                 int qsum;
-                uint32_t nib[2];
-                quant_group<2>(v[p], scale, qsum, bad, nib);
-                if (g < G) {
-                    const int wi = g * 16 + 2 * l8;
-                    put_word(wi, nib[0]);
-                    put_word(wi + 1, nib[1]);
-                    if (l8 == 0) {
-                        sxs[g] = scale;
-                        qss[g] = (float)qsum;
+                quant_group<4>(v, scale, qsum, bad, nib);
+                qsf = (float)qsum;
+                if (blockIdx.x == 0 && warp < S && live) {
+                    *reinterpret_cast<uint4 *>(xq_out + (size_t)sg * 512 + lane * 16) =
+                        make_uint4(nib[0], nib[1], nib[2], nib[3]);
+                    if ((lane & 3) == 0) {
+                        sx_out[g] = scale;
+                        qs_out[g] = qsum;
                     }
-                    if (blockIdx.x == 0) {
-                        *reinterpret_cast<uint2 *>(xq_out + (size_t)wi * 4) = make_uint2(nib[0], nib[1]);
+                }
+            }
+            act_bytes(nib[0], fe.x, fo.x, m8);
+            act_bytes(nib[1], fe.y, fo.y, m8);
+            act_bytes(nib[2], fe.z, fo.z, m8);
+            act_bytes(nib[3], fe.w, fo.w, m8);
+            any_m8 = __any_sync(0xffffffffu, m8);
+            esx[0] = esx[1] = scale;
+            eqs[0] = eqs[1] = qsf;
+        }
+        if (bad) flag(st, QSPEC_ERR_NONFINITE);
+    } else {
+        const int words = K / 8;
+        auto put_word = [&](int wi, uint32_t nib) {
+            uint32_t ep, o;
+            act_bytes(nib, ep, o, m8);
+            uint32_t *a = reinterpret_cast<uint32_t *>(act + (size_t)(wi >> 7) * 64 + ((wi >> 2) & 31));
+            a[wi & 3] = ep;
+            a[128 + (wi & 3)] = o;
+        };
+        if (x == nullptr) {
+            const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
+            constexpr int kB = 4;
+            for (int w0 = threadIdx.x; w0 < S * 128; w0 += kB * kThreads) {
+                uint32_t xw4[kB];
+#pragma unroll
+                for (int i = 0; i < kB; ++i) xw4[i] = w0 + i * kThreads < words ? xw[w0 + i * kThreads] : 0u;
+#pragma unroll
+                for (int i = 0; i < kB; ++i)
+                    if (w0 + i * kThreads < S * 128) put_word(w0 + i * kThreads, xw4[i]);
+            }
+            for (int g = threadIdx.x; g < G; g += kThreads) {
+                sxs[g] = sx[g];
+                qss[g] = (float)qs[g];
+            }
+        } else {
+            // eight lanes per group, 16 elements each (two 16-byte words); CTA 0
+            // also stores xq, sx, qs
+            const int sub = lane >> 3, l8 = lane & 7;
+            const int kPer = kThreads / 8;                    // groups per pass: 4 per warp
+            for (int g0 = 4 * warp; g0 < G; g0 += 2 * kPer) {
+                uint4 v[2][2];
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int g = g0 + p * kPer + sub;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)g * kGroup) + 2 * l8;
+                    v[p][0] = g < G ? src[0] : make_uint4(0u, 0u, 0u, 0u);
+                    v[p][1] = g < G ? src[1] : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int g = g0 + p * kPer + sub;
+                    if (g0 + p * kPer >= G) break;            // warp-uniform
+                    float scale;
+                    int qsum;
+                    uint32_t nib[2];
+                    quant_group<2>(v[p], scale, qsum, bad, nib);
+                    if (g < G) {
+                        const int wi = g * 16 + 2 * l8;
+                        put_word(wi, nib[0]);
+                        put_word(wi + 1, nib[1]);
                         if (l8 == 0) {
-                            sx_out[g] = scale;
-                            qs_out[g] = qsum;
+                            sxs[g] = scale;
+                            qss[g] = (float)qsum;
+                        }
+                        if (blockIdx.x == 0) {
+                            *reinterpret_cast<uint2 *>(xq_out + (size_t)wi * 4) = make_uint2(nib[0], nib[1]);
+                            if (l8 == 0) {
+                                sx_out[g] = scale;
+                                qs_out[g] = qsum;
+                            }
                         }
                     }
                 }
             }
+            // words of a partial last unit: zero (their weights load as zeros too)
+            for (int wi = words + threadIdx.x; wi < S * 128; wi += kThreads) put_word(wi, 0u);
         }
-        // words of a partial last unit: zero (their weights load as zeros too)
-        for (int wi = words + threadIdx.x; wi < S * 128; wi += kThreads) put_word(wi, 0u);
+        if (bad) flag(st, QSPEC_ERR_NONFINITE);
+        any_m8 = __syncthreads_or(m8);
+        if (kFixed && unit_warp) {
+            fe = act[(warp % S) * 64 + lane];
+            fo = act[(warp % S) * 64 + 32 + lane];
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int g = eg[b] < G ? eg[b] : 0;
+            esx[b] = sxs[g];
+            eqs[b] = qss[g];
+        }
     }
-    if (bad) flag(st, QSPEC_ERR_NONFINITE);
-    const bool any_m8 = __syncthreads_or(m8);
-    // with a fixed segment, this lane's activation bytes for every unit
-    uint4 fe = make_uint4(0u, 0u, 0u, 0u), fo = fe;
-    if (kFixed && unit_warp) {
-        fe = act[(warp % S) * 64 + lane];
-        fo = act[(warp % S) * 64 + 32 + lane];
-    }
-    // this lane's epilogue constants: sx and qs of its two groups, pair slots
-    float esx[2], eqs[2];
+    // this lane's pair slots
     int pidx[2];
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-        const int g = eg[b] < G ? eg[b] : 0;
-        esx[b] = sxs[g];
-        eqs[b] = qss[g];
-        pidx[b] = erl[b] * pstride + eg[b];
-    }
+    for (int b = 0; b < 2; ++b) pidx[b] = erl[b] * pstride + eg[b];
 
     // one thread per row folds the groups of chunk c in ascending order
     // (the fold warps' threads when there are any, else every thread)
@@ -338,7 +396,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 16 / kMaxWarps)
         constexpr bool kAny = decltype(any_tag)::value;
         if (!unit_warp) {
             if (c > 0) fold(c - 1);
-            __syncthreads();
+            cta_barrier();
             return;
         }
         issue(c + kP - 1);
@@ -381,7 +439,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 16 / kMaxWarps)
                 if (dbg_I) dbg_I[(size_t)(row0 + erl[b]) * G + eg[b]] = (int32_t)I;
             }
         }
-        __syncthreads();
+        cta_barrier();
     };
     auto run = [&](auto any_tag) {
         for (int c = 0; c < n_chunks; c += 2) {

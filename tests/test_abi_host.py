@@ -88,6 +88,7 @@ def test_alignment_and_workspace_rejected_on_host(lib):
     assert lib.qspec_pack_weights(fake(0x1001), fake(), fake(), 4, 128, fake(), fake(), None,
                                   st) == 3
     assert lib.qspec_quant_act_int4(fake(), 1, 128, 132, fake(), fake(), fake(), None, st) == 3
+    assert lib.qspec_quant_act_int4(fake(), 1, 128, 128, fake(0x1004), fake(), fake(), None, st) == 3
     assert lib.qspec_linear_w4a4_bf16(fake(), 132, fake(), fake(), 1, 8, 128, fake(), 8, fake(),
                                       fake(), fake(), None, None, st) == 3
     assert lib.qspec_kv_overwrite(fake(0x1008), fake(), fake(), fake(), fake(), fake(), 1, 1, 1,
