@@ -278,3 +278,19 @@ def test_one_token_extreme():
     y4o, Io = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
     assert Io[0, 0].max() == 128 * 7 * 15 and Io[0, 1].min() == -128 * 7 * 15
     assert np.array_equal(I.cpu().numpy(), Io) and np.array_equal(bits(y4), y4o)
+
+
+# ----------------------------------------------------------------- W4A16, one token tile
+# Up to 8 tokens in one MMA column block: fewer rows than SMs, ragged tiles,
+# K = 14336 with 5 and 8 tokens (the token fragments then halve the tokens
+# per CTA), an odd group count.
+@pytest.mark.parametrize("M,N,K,seed", [(1, 300, 1152, 60), (5, 6083, 4096, 61), (5, 1000, 14336, 62),
+                                        (8, 777, 4096, 63), (3, 19533, 1152, 64), (7, 5, 640, 65),
+                                        (8, 300, 14336, 66), (2, 151, 256, 67)])
+def test_w4a16_one_token_tile(M, N, K, seed):
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100, outlier_frac=0.01)
+    y16 = q.linear_w4a16(x.to(dev), packed, sz)
+    ref = oracle.linear_w4a16(bits(x), po, szo)
+    assert_w4a16_close(y16, ref, "w4a16 M=%d N=%d K=%d" % (M, N, K))
