@@ -139,6 +139,12 @@ def bytes_w4a4(M, N, K):
     return K * N // 2 + 4 * N * K // GROUP + M * K // 2 + 8 * M * K // GROUP + 2 * M * N
 
 
+def bytes_w4a4_bf16(M, N, K):
+    """The draft call with the quantiser inside: bf16 activations read, the
+    quantised activations (xq, sx, qs) written once."""
+    return K * N // 2 + 4 * N * K // GROUP + 2 * M * K + M * K // 2 + 8 * M * K // GROUP + 2 * M * N
+
+
 def bytes_quant(M, K):
     return 2 * M * K + M * K // 2 + 8 * M * K // GROUP
 
@@ -317,17 +323,12 @@ class GpuRound:
                                              self.status), "w4a4_bf16")
 
     def draft_linears_only(self, j=0):
-        """One draft step's W4A4 launches without the quantiser (kernel timing)."""
-        q = self.q
+        """One draft step's W4A4 launches, exactly as the round makes them
+        (kernel timing)."""
         for l in range(self.L):
             for name, N, K in self.linears:
-                xq, sx, qs = self.qbuf[K]
-                self._check(q.qspec_linear_w4a4(xq, sx, qs, self.w[l][name][0], self.w[l][name][1],
-                                                self.B, N, K, self.yd[name], N, None, self.status),
-                            "w4a4")
-        xq, sx, qs = self.qbuf[self.hidden]
-        self._check(q.qspec_linear_w4a4(xq, sx, qs, self.lm[0], self.lm[1], self.B, self.V,
-                                        self.hidden, self.yd_lm, self.V, None, self.status), "w4a4")
+                self._w4a4(self.xd[name][j, l], self.w[l][name], N, K, self.yd[name])
+        self._w4a4(self.xd_lm[j], self.lm, self.V, self.hidden, self.yd_lm)
 
     def verify_linears_only(self):
         q = self.q
@@ -342,8 +343,8 @@ class GpuRound:
                     "w4a16")
 
     def bytes_draft_linears(self):
-        b = sum(bytes_w4a4(self.B, N, K) for _, N, K in self.linears) * self.L
-        return b + bytes_w4a4(self.B, self.V, self.hidden)
+        b = sum(bytes_w4a4_bf16(self.B, N, K) for _, N, K in self.linears) * self.L
+        return b + bytes_w4a4_bf16(self.B, self.V, self.hidden)
 
     def bytes_verify_linears(self):
         Mv = self.B * (self.gamma + 1)
@@ -387,10 +388,12 @@ def aggregate_over_ranks(seconds, tokens, device):
     return float(mx[0]), int(round(float(t[1])))
 
 
-def row_kernels(dev, stream, reps=5):
+def row_kernels(dev, stream, reps=5, calls=10):
     """Every hot-path row timed on its own at a representative size (CUDA
-    graph replays, CUDA events): algorithmic bytes per call, GB/s, fraction
-    of the measured HBM bandwidth."""
+    graph replays of `calls` back-to-back calls, CUDA events; per call, so the
+    graph launch is spread over the calls as in a longer pipeline):
+    algorithmic bytes per call, GB/s, fraction of the measured HBM
+    bandwidth."""
     from quantized_speculative_decoding_shared_gb300 import binding as q
     peak, _ = measured_peaks()
     out = {}
@@ -398,8 +401,12 @@ def row_kernels(dev, stream, reps=5):
     def rec(name, fn, nbytes, note):
         fn()
         torch.cuda.synchronize()
-        g = capture(fn, stream)
-        t = time_graph(g, reps, stream)
+
+        def many():
+            for _ in range(calls):
+                fn()
+        g = capture(many, stream)
+        t = time_graph(g, reps, stream) / calls
         out[name] = {"case": note, "us": round(t * 1e3, 2), "bytes": int(nbytes),
                      "GB/s": round(nbytes / (t / 1e3) / 1e9, 1),
                      "frac_hbm": round(nbytes / (t / 1e3) / 1e9 / peak, 4)}

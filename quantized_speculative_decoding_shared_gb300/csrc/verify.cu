@@ -17,9 +17,9 @@
 // many CTAs and combined with atomics without changing a single bit.
 //
 // Launch sequence (one stream, no host synchronisation):
-//   greedy : argmax (one CTA per row when there are at least two rows per
-//            SM; else memset, chunk x row with atomics), finalize (per
-//            sequence)
+//   greedy : argmax (chunk x row, one chunk per row when there are at
+//            least two rows per SM; one key per chunk), finalize (per
+//            sequence: max over the chunk keys, first mismatch)
 //   sampled: row max and row sums (one CTA per row, the second pass over the
 //            row hitting L2; else memset, then chunk x row kernels for each
 //            with atomics), decisions + residual chunk sums (chunk x
@@ -38,6 +38,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kSub = kThreads * 8;    // elements one CTA covers per pass (8 per thread)
 constexpr int kMaxChunks = 256;
+// greedy: rows x chunks keys, with chunks sized for about two CTAs per SM,
+// fit in rows + kGreedyExtraKeys slots (for up to 512 SMs)
+constexpr int kGreedyExtraKeys = 1024;
 
 struct Layout {
     int chunk;        // elements per chunk (multiple of kSub)
@@ -55,7 +58,7 @@ Layout make_layout(int B, int gamma, int V) {
     L.n_chunks = (V + L.chunk - 1) / L.chunk;
     size_t rows_g = (size_t)B * (gamma + 1), rows_s = (size_t)B * (2 * gamma + 1);
     size_t o = 0;
-    L.off_key = o;  o = align16(o + rows_g * 8);                 // greedy argmax keys
+    L.off_key = o;  o = align16(o + (rows_g + kGreedyExtraKeys) * 8); // greedy (row, chunk) argmax keys
     L.off_max = o;  o = align16(o + rows_s * 4);                 // row max, ordered bits
     L.off_sum = o;  o = align16(o + rows_s * 8);                 // row sums S
     L.off_rsum = o; o = align16(o + (size_t)B * L.n_chunks * 16); // residual chunk sums
@@ -139,6 +142,12 @@ __device__ __forceinline__ u128 block_scan_u128(u128 v, u128 *buf) {
 // -------------------------------------------------------------------------
 // greedy
 // -------------------------------------------------------------------------
+// CTA (row, chunk): the argmax key of P[row][chunk], written to
+// keys[row * gridDim.y + chunk]; four 8-logit loads per thread in flight.
+// Each thread keeps the first of its largest logits (strict >, increasing
+// index, so -0 and +0 tie as in float comparison and NaN never wins),
+// starting from its first logit; the key (value with -0 made +0, then the
+// lowest index) picks the CTA's winner.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) greedy_argmax_kernel(const uint16_t *__restrict__ P, int V,
                                                                 int chunk,
@@ -150,59 +159,35 @@ __global__ void __launch_bounds__(kThreads) greedy_argmax_kernel(const uint16_t 
     const int row = blockIdx.x;
     const uint16_t *rp = P + (size_t)row * V;
     const int c0 = blockIdx.y * chunk, c1 = min(V, c0 + chunk);
-    unsigned long long best = 0;
+    float bv = -INFINITY;
+    int bi = c0 + threadIdx.x * 8;                          // its first logit (or none)
     bool bad = false;
-    for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
-        float f[8];
-        load8<VEC>(rp, v0, c1, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (v0 + i >= c1) break;
-            bad |= isnan(f[i]);
-            unsigned long long key = ((unsigned long long)ordered_bits(f[i]) << 32) |
-                                     (0xFFFFFFFFu - (uint32_t)(v0 + i));
-            best = key > best ? key : best;
-        }
-    }
-    if (bad) flag(st, QSPEC_ERR_NONFINITE);
-    best = block_reduce_max(best, sh);
-    if (threadIdx.x == 0) atomicMax(keys + row, best);
-}
-
-// one CTA per row: the row's argmax key written directly
-template <bool VEC>
-__global__ void __launch_bounds__(kThreads) greedy_rowargmax_kernel(const uint16_t *__restrict__ P, int V,
-                                                                   unsigned long long *__restrict__ keys,
-                                                                   int32_t *st) {
-    pdl_launch_dependents();
-    pdl_wait();
-    __shared__ unsigned long long sh[kThreads / 32];
-    const int row = blockIdx.x;
-    const uint16_t *rp = P + (size_t)row * V;
-    unsigned long long best = 0;
-    bool bad = false;
-    for (int v0 = threadIdx.x * 8; v0 < V; v0 += kSub * 4) {
+    for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub * 4) {
         float f[4][8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) load8<VEC>(rp, v0 + u * kSub, V, f[u]);
+        for (int u = 0; u < 4; ++u) load8<VEC>(rp, v0 + u * kSub, c1, f[u]);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int v = v0 + u * kSub + i;
-                if (v >= V) break;
-                bad |= isnan(f[u][i]);
-                const unsigned long long key =
-                    ((unsigned long long)ordered_bits(f[u][i]) << 32) | (0xFFFFFFFFu - (uint32_t)v);
-                best = key > best ? key : best;
+                bad |= isnan(f[u][i]);                    // (missing logits read as -inf)
+                if (f[u][i] > bv) {
+                    bv = f[u][i];
+                    bi = v0 + u * kSub + i;
+                }
             }
     }
     if (bad) flag(st, QSPEC_ERR_NONFINITE);
+    unsigned long long best = 0;
+    if (bi < c1)
+        best = ((unsigned long long)ordered_bits(__fadd_rn(bv, 0.0f)) << 32) | (0xFFFFFFFFu - (uint32_t)bi);
     best = block_reduce_max(best, sh);
-    if (threadIdx.x == 0) keys[row] = best;
+    if (threadIdx.x == 0) keys[(size_t)row * gridDim.y + blockIdx.y] = best;
 }
 
-__global__ void greedy_finalize_kernel(const unsigned long long *__restrict__ keys,
+// per sequence: the row argmaxes (max over the row's nch chunk keys), the
+// first mismatch, the emitted tokens
+__global__ void greedy_finalize_kernel(const unsigned long long *__restrict__ keys, int nch,
                                        const int32_t *__restrict__ draft, int B, int gamma, int V,
                                        int32_t *__restrict__ n_acc, int32_t *__restrict__ out,
                                        int32_t *st) {
@@ -210,20 +195,24 @@ __global__ void greedy_finalize_kernel(const unsigned long long *__restrict__ ke
     pdl_wait();
     int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
-    const unsigned long long *k = keys + (size_t)b * (gamma + 1);
+    auto row_arg = [&](int i) {
+        const unsigned long long *k = keys + ((size_t)b * (gamma + 1) + i) * nch;
+        unsigned long long best = 0;
+        for (int c = 0; c < nch; ++c) best = k[c] > best ? k[c] : best;
+        return (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    };
     const int32_t *d = draft + (size_t)b * gamma;
     int A = gamma;
     bool bad = false;
     for (int i = 0; i < gamma; ++i) {
         int t = d[i];
         bad |= (t < 0 || t >= V);
-        int arg = (int)(0xFFFFFFFFu - (uint32_t)(k[i] & 0xFFFFFFFFull));
-        if (A == gamma && t != arg) A = i;
+        if (A == gamma && t != row_arg(i)) A = i;
     }
     if (bad) flag(st, QSPEC_ERR_RANGE);
     int32_t *o = out + (size_t)b * (gamma + 1);
     for (int i = 0; i <= gamma; ++i) o[i] = i < A ? d[i] : -1;
-    o[A] = (int)(0xFFFFFFFFu - (uint32_t)(k[A] & 0xFFFFFFFFull));
+    o[A] = row_arg(A);
     n_acc[b] = A;
 }
 
@@ -624,28 +613,23 @@ extern "C" int qspec_verify_greedy(const uint16_t *p_logits, const int32_t *draf
     auto *keys = reinterpret_cast<unsigned long long *>(ws + L.off_key);
     const int rows = B * (gamma + 1);
     bool vec = (V % 8 == 0) && aligned(p_logits, 16);
-    if (rows >= 2 * sm_count()) {
-        // enough rows: one CTA per row
-        rc = vec ? launch_pdl("qspec_verify_greedy", greedy_rowargmax_kernel<true>, dim3(rows), dim3(kThreads), 0,
-                              st, p_logits, V, keys, dev_status)
-                 : launch_pdl("qspec_verify_greedy", greedy_rowargmax_kernel<false>, dim3(rows), dim3(kThreads), 0,
-                              st, p_logits, V, keys, dev_status);
-    } else {
-        // few rows: chunks of every row combined with atomics
-        cudaError_t e = cudaMemsetAsync(keys, 0, (size_t)rows * 8, st);
-        if (e != cudaSuccess) {
-            set_last_error("qspec_verify_greedy memset", e);
-            return QSPEC_ERR_LAUNCH;
-        }
-        dim3 grid((unsigned)rows, (unsigned)L.n_chunks);
-        rc = vec ? launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<true>, grid, dim3(kThreads), 0, st,
-                              p_logits, V, L.chunk, keys, dev_status)
-                 : launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<false>, grid, dim3(kThreads), 0, st,
-                              p_logits, V, L.chunk, keys, dev_status);
-    }
+    // one CTA per row when there are at least two rows per SM, else each row
+    // split into chunks so that the grid covers about two CTAs per SM; one
+    // key per (row, chunk), no atomics and no clearing
+    const int target = 2 * sm_count();
+    int nch = rows >= target ? 1 : std::min(kMaxChunks, (target + rows - 1) / rows);
+    const int subs = (V + kSub - 1) / kSub;
+    const int chunk = ((subs + nch - 1) / nch) * kSub;
+    nch = (V + chunk - 1) / chunk;
+    if ((size_t)rows * nch > (size_t)rows + kGreedyExtraKeys) return QSPEC_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)rows, (unsigned)nch);
+    rc = vec ? launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<true>, grid, dim3(kThreads), 0, st, p_logits,
+                          V, chunk, keys, dev_status)
+             : launch_pdl("qspec_verify_greedy", greedy_argmax_kernel<false>, grid, dim3(kThreads), 0, st, p_logits,
+                          V, chunk, keys, dev_status);
     if (rc) return rc;
     return launch_pdl("qspec_verify_greedy", greedy_finalize_kernel, dim3((B + 127) / 128), dim3(128), 0, st,
-                      keys, draft, B, gamma, V, n_acc, out, dev_status);
+                      keys, nch, draft, B, gamma, V, n_acc, out, dev_status);
 }
 
 template <bool VEC>

@@ -95,7 +95,7 @@ def test_row_statistics_in_workspace(B):
     wsb = ws.cpu().numpy()
     rows = B * (2 * gamma + 1)
     rows_g = B * (gamma + 1)
-    off_max = ((rows_g * 8 + 15) // 16) * 16
+    off_max = (((rows_g + 1024) * 8 + 15) // 16) * 16      # after the (row, chunk) argmax keys
     off_sum = off_max + ((rows * 4 + 15) // 16) * 16
     enc = wsb[off_max:off_max + rows * 4].view(np.uint32)
     S = wsb[off_sum:off_sum + rows * 8].view(np.uint64)
@@ -209,3 +209,24 @@ def test_expected_accept_length_on_gpu():
     L = n + 1
     EL = (1 - a ** (gamma + 1)) / (1 - a)
     assert abs(L.mean() - EL) < 4 * L.std() / math.sqrt(B)
+
+
+@pytest.mark.parametrize("B", [1, 64])
+def test_greedy_signed_zero_tie(B):
+    """A row whose largest logit is zero with -0 before +0: float comparison
+    ties them, so the lower index wins (the oracle's reading), whether the two
+    fall in different chunks of the row (B = 1) or one CTA scans the row
+    (B = 64)."""
+    dev = need_gpu()
+    gamma, V = 4, 50000
+    P = torch.full((B, gamma + 1, V), -5.0)
+    P[:, :, 100] = -0.0
+    P[:, :, 40000] = 0.0
+    P[:, 1, 7] = 0.0                                       # row 1: +0 first, then -0 at 100
+    P = P.to(torch.bfloat16)
+    d = torch.full((B, gamma), 100, dtype=torch.int32)
+    rc, n, out = gpu_greedy(P, d, dev)
+    rco, no, outo = oracle.verify_greedy(bits(P), d.numpy())
+    assert rc == rco == 0
+    assert np.array_equal(n, no) and np.array_equal(out, outo)
+    assert n[0] == 1 and out[0, 1] == 7                    # row 0 argmax 100 (accepted), row 1 argmax 7
