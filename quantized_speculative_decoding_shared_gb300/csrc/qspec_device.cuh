@@ -160,19 +160,16 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // Shared by the quantiser and the kernels that quantise their own
 // activations, so all agree bit for bit.
 //
-// The quotient x / sx is formed as t = x * rs with rs within 1 ulp of 1 / sx
-// (|rs sx - 1| <= 2^-23).  t then differs from the exact quotient by at
-// most |x / sx| (2^-23 + 2^-24 + 2^-47), below 1.3e-6 since |x / sx| <= 7
-// (1 + 2^-23), and the correctly rounded quotient fl(x / sx) lies within
-// 2^-24 |x / sx| < 4.2e-7 of the exact one; so rint(t) and rint(fl(x / sx))
-// can differ only when t lies within 1.7e-6 of a half-integer.  When any
-// element of a lane is within 1e-5 of one (|t - rint(t)| >= 0.49999), or sx
-// is below 1e-30 (its reciprocal may overflow or flush), the lane redoes its
-// elements with the IEEE division, so the codes are always the division's.
-// Otherwise |t| <= 7.000002 and no clamp is needed.  rint(t) is t + 1.5 *
-// 2^23 rounded to nearest (even), whose low four bits are then the code; the
-// sum of the rounded values is exact, and not finite exactly when some
-// input is not (a NaN or inf x makes its t a NaN or inf).
+// The quotient is taken as one Newton step from the approximate reciprocal
+// y = rcp.approx(sx): q0 = x y, r = fma(-q0, sx, x) (the exact remainder),
+// t = fma(r, y, q0).  For every pair of bf16 values with |x| <= amax and
+// sx = amax / 7 >= 1e-30 (all 1.05e9 of them, checked exhaustively on the
+// device against the IEEE division), rint(t) equals rint(x / sx) and lies
+// in [-7, 7], so no clamp and no tie test are needed; groups with sx below
+// 1e-30 take the IEEE division.  rint(t) is t + 1.5 * 2^23 rounded to
+// nearest (even), whose low four bits are then the code; the sum of the
+// rounded values is exact, and not finite exactly when some input is not (a
+// NaN or inf x makes its t a NaN).
 template <int kVec>
 __device__ __forceinline__ void quant_group(const uint4 (&v)[kVec], float &scale, int &qsum, bool &bad,
                                             uint32_t (&nib)[kVec]) {
@@ -201,24 +198,21 @@ __device__ __forceinline__ void quant_group(const uint4 (&v)[kVec], float &scale
     for (int o = 8 / kVec; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     scale = __fdiv_rn(amax, 7.0f);
     const bool tiny = scale < 1.0e-30f;                     // 0 included: then every x is 0
-    const float rs = tiny ? 0.0f : rcp_approx(scale);
-    float d[kVec * 8], r[kVec * 8];
+    const float y = tiny ? 0.0f : rcp_approx(scale);
+    float r[kVec * 8];
     uint32_t e[kVec * 8];
 #pragma unroll
     for (int i = 0; i < kVec * 8; ++i) {
-        const float t = __fmul_rn(f[i], rs);
+        const float q0 = __fmul_rn(f[i], y);
+        const float t = __fmaf_rn(__fmaf_rn(-q0, scale, f[i]), y, q0);
         const float m = __fadd_rn(t, kMagic);
         r[i] = __fsub_rn(m, kMagic);                          // rint(t)
-        d[i] = fabsf(__fsub_rn(t, r[i]));
         e[i] = (__float_as_uint(m) & 15u) << (4 * (i & 7));
     }
 #pragma unroll
     for (int w = kVec * 4; w >= 1; w >>= 1)
 #pragma unroll
-        for (int i = 0; i < w; ++i) {
-            d[i] = fmaxf(d[i], d[i + w]);
-            r[i] = __fadd_rn(r[i], r[i + w]);                 // integers: exact in any order
-        }
+        for (int i = 0; i < w; ++i) r[i] = __fadd_rn(r[i], r[i + w]);   // integers: exact in any order
 #pragma unroll
     for (int c = 0; c < kVec; ++c) {
 #pragma unroll
@@ -227,11 +221,11 @@ __device__ __forceinline__ void quant_group(const uint4 (&v)[kVec], float &scale
             for (int i = 0; i < w; ++i) e[8 * c + i] |= e[8 * c + i + w];
         nib[c] = e[8 * c];
     }
-    const float dmax = d[0], qf = r[0];
+    const float qf = r[0];
     bad |= !isfinite(qf);
     int sum = (int)qf;
-    const bool redo = (tiny && scale != 0.0f) || dmax >= 0.49999f;
-    if (__any_sync(0xffffffffu, redo)) {                     // rare: the IEEE division decides
+    const bool redo = tiny && scale != 0.0f;
+    if (__any_sync(0xffffffffu, redo)) {                     // sx below 1e-30: the IEEE division
         if (redo) {
             sum = 0;
 #pragma unroll

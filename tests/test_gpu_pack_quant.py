@@ -92,3 +92,36 @@ def test_quant_act_nonfinite_status():
     st = status(dev)
     q.quant_act_int4(x.to(dev), dev_status=st)
     assert read_status(st) == q.ERR_NONFINITE == oracle.quant_act_int4(bits(x))[0]
+
+
+def test_quant_act_every_scale_near_ties():
+    """One group per positive bf16 amax (every normal value, and a few
+    subnormal ones, whose tiny scale takes the IEEE division): the group holds
+    amax and the bf16 values at and up to two steps either side of every
+    half-integer multiple (k + 1/2) sx, the quotients that decide rounding
+    ties; the codes, scales and sums match the oracle bit for bit."""
+    dev = need_gpu()
+    rng = np.random.default_rng(12)
+    ab = np.concatenate([np.arange(0x0080, 0x7F80, dtype=np.uint32), np.array([0x0001, 0x0040, 0x007F], np.uint32)])
+    amax = (ab << 16).view(np.float32)
+    sx = (amax / np.float32(7)).astype(np.float32)
+    h = ((np.arange(-7, 7, dtype=np.float32) + np.float32(0.5))[None, :] * sx[:, None]).astype(np.float32)
+    hb = torch.from_numpy(h).to(torch.bfloat16).view(torch.int16).numpy().astype(np.int32)
+    mag, sign = hb & 0x7FFF, hb & 0x8000
+    near = np.concatenate([((mag + d).clip(0, 0x7F7F) | sign) for d in (-2, -1, 0, 1, 2)], axis=1)   # [n][70]
+    nearf = ((near.astype(np.uint32) & 0xFFFF) << 16).view(np.float32)
+    nearf = np.where(np.abs(nearf) <= amax[:, None], nearf, 0.0).astype(np.float32)
+    fill = (rng.uniform(-1, 1, (len(ab), 128 - 1 - nearf.shape[1])) * amax[:, None]).astype(np.float32)
+    grp = np.concatenate([amax[:, None], nearf, fill], axis=1)                       # [n][128]
+    G = 256
+    n_rows = (len(ab) + G - 1) // G
+    pad = np.zeros((n_rows * G - len(ab), 128), np.float32)
+    x = torch.from_numpy(np.concatenate([grp, pad]).reshape(n_rows, G * 128)).to(torch.bfloat16)
+    assert np.abs(x.float().numpy().reshape(-1, 128)[: len(ab), 0] - amax).max() == 0
+    st = status(dev)
+    xq, sx_g, qs = q.quant_act_int4(x.to(dev), dev_status=st)
+    rc, xqo, sxo, qso = oracle.quant_act_int4(bits(x))
+    assert rc == 0 and read_status(st) == 0
+    assert np.array_equal(sx_g.cpu().numpy().view(np.uint32), sxo.view(np.uint32))
+    assert np.array_equal(qs.cpu().numpy(), qso)
+    assert np.array_equal(xq.cpu().numpy(), xqo)
