@@ -160,8 +160,12 @@ def measured_peaks():
 
 
 def kernel_source_hash(name):
-    p = os.path.join(ROOT, "quantized_speculative_decoding_shared_gb300", "csrc", name)
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """The kernel's source file with the library headers it compiles in."""
+    d = os.path.join(ROOT, "quantized_speculative_decoding_shared_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (name, "qspec_device.cuh", "qspec_host.h"):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel_file):
