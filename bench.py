@@ -81,7 +81,7 @@ def parse_args():
                     default="llama3-8b-decode-b1-g4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rounds", type=int, default=16, help="distinct captured rounds (RNG round ids)")
-    ap.add_argument("--profile-case", choices=["w4a4_m1", "w4a16_m5", "quant", "verify_sample",
+    ap.add_argument("--profile-case", choices=["w4a4_m1", "w4a16_m5", "w4a16_m80", "quant", "verify_sample",
                                                "verify_greedy", "kv"],
                     help="run one kernel a few times on a single LM-head-sized case (for ncu)")
     ap.add_argument("--profile-reps", type=int, default=3)
@@ -95,17 +95,17 @@ def profile_case(name, reps):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     N, K = 128256, 4096
-    if name in ("w4a4_m1", "w4a16_m5", "quant"):
+    if name in ("w4a4_m1", "w4a16_m5", "w4a16_m80", "quant"):
         codes, s, z = syn.weights(N, K, 5, device=dev)
         packed, sz = q.pack_weights(codes, s, z)
         del codes
-        M = 1 if name != "w4a16_m5" else 5
+        M = {"w4a16_m5": 5, "w4a16_m80": 80}.get(name, 1)
         x = syn.activations(M, K, 6, device=dev, outlier_frac=0.01)
         xq, sx, qs = q.quant_act_int4(x)
         for _ in range(reps):
             if name == "w4a4_m1":
                 q.linear_w4a4_bf16(x, packed, sz)
-            elif name == "w4a16_m5":
+            elif name in ("w4a16_m5", "w4a16_m80"):
                 q.linear_w4a16(x, packed, sz)
             else:
                 q.quant_act_int4(syn.activations(4096, 14336, 7, device=dev))

@@ -14,7 +14,7 @@
 //
 // One token (the B = 1 draft decode): byte dot products (w4a4_dp4a.cu).
 // Small M (2..32): f16 warp MMA on exact small integers, described below;
-// 3 <= M <= 8 with at least one 128-row tile per SM: tensor-memory GEMV
+// 3 <= M <= 16 with at least one 128-row tile per SM: tensor-memory GEMV
 // (w4a4_gemv_tc.cu).  Larger M: tcgen05 (w4a4_tc.cu).
 #include <algorithm>
 
@@ -431,8 +431,8 @@ int launch_small(const Act &a, const uint8_t *packed, const uint32_t *sz, int M,
     }
 }
 
-// the tensor-memory GEMV takes 3..8 tokens when every SM gets a 128-row tile
-bool use_gemv_tc(int M, int N) { return M >= 3 && M <= 8 && (N + 127) / 128 >= sm_count(); }
+// the tensor-memory GEMV takes 3..16 tokens when every SM gets a 128-row tile
+bool use_gemv_tc(int M, int N) { return M >= 3 && M <= 16 && (N + 127) / 128 >= sm_count(); }
 
 }  // namespace hm
 
@@ -460,7 +460,7 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
                               dev_status, st);
         if (rc != QSPEC_ERR_SHAPE) return rc;
     }
-    // 3..8 tokens and at least one 128-row tile per SM: weights through TMA
+    // 3..16 tokens and at least one 128-row tile per SM: weights through TMA
     // and TMEM, MMAs async (at 1-2 tokens the warp-MMA kernel below is faster)
     if (hm::use_gemv_tc(M, N)) {
         rc = launch_w4a4_gemv_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);

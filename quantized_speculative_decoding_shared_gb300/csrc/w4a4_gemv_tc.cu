@@ -56,8 +56,11 @@ constexpr uint32_t kDcol = 256;            // D of pair slot s: columns 256 + 32
 constexpr int kStageBytes = 128 * 128;     // one box: 128 rows x 128 bytes (a group pair)
 constexpr int kMaxStages = 8;
 
+// token operand bytes per group: 128 k x 8 token rows, or x 16 rows for 16 tokens
+constexpr size_t token_group_bytes(int MT) { return MT > 8 ? 2048 : 1024; }
 inline size_t tail_bytes(int MT, int G, int stages) {
-    return (size_t)G * 1024 + (((size_t)G * MT * 8 + 15) / 16) * 16 + (size_t)(2 * stages + 3 * kPSlots) * 8 + 16;
+    return (size_t)G * token_group_bytes(MT) + (((size_t)G * MT * 8 + 15) / 16) * 16 +
+           (size_t)(2 * stages + 3 * kPSlots) * 8 + 16;
 }
 inline size_t smem_bytes(int MT, int K, int stages) {
     return (size_t)stages * kStageBytes + tail_bytes(MT, K / kGroup, stages);
@@ -87,12 +90,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float *__restrict__ sx, const int32_t *__restrict__ qs,
                         const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
                         int32_t *__restrict__ dbg_I, int32_t *__restrict__ st, int S) {
-    static_assert(MT == 1 || MT == 2 || MT == 4 || MT == 8, "token columns per CTA");
+    static_assert(MT == 1 || MT == 2 || MT == 4 || MT == 8 || MT == 16, "token columns per CTA");
+    constexpr uint32_t kTokBytes = (uint32_t)token_group_bytes(MT);
     extern __shared__ __align__(1024) unsigned char smem[];
     const int G = K / kGroup, P = (G + 1) / 2;
     uint8_t *stages = smem;
     uint8_t *bsm = smem + (size_t)S * kStageBytes;
-    float2 *sxq = reinterpret_cast<float2 *>(bsm + (size_t)G * 1024);
+    float2 *sxq = reinterpret_cast<float2 *>(bsm + (size_t)G * kTokBytes);
     uint64_t *bars =
         reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sxq) + (((size_t)G * MT * 8 + 15) / 16) * 16);
     uint64_t *st_full = bars, *st_empty = bars + S;
@@ -151,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
 
     // token operand: zero rows, then the real tokens' words
-    for (int i = threadIdx.x; i < G * 64; i += kThreads) reinterpret_cast<uint4 *>(bsm)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < G * (int)(kTokBytes / 16); i += kThreads)
+        reinterpret_cast<uint4 *>(bsm)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     const int mt_real = min(MT, M - tok0);
     const uint32_t *xw = reinterpret_cast<const uint32_t *>(xq);
@@ -162,7 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = 4 * kc + j;                         // 4-byte column of the group row
         const int u = c >> 3, v = (c & 7) >> 1, h = c & 1;
         const uint32_t w = xw[(size_t)(tok0 + t) * (K / 8) + g * 16 + 4 * v + u];
-        reinterpret_cast<uint32_t *>(bsm + (size_t)g * 1024 + kc * 128 + t * 16)[j] = e4m3_of_signed_nibbles(w, h);
+        // rows 0..7 of the chunk's core matrix, rows 8..15 in a second one 1024 bytes on
+        reinterpret_cast<uint32_t *>(bsm + (size_t)g * kTokBytes + (t >> 3) * 1024 + kc * 128 + (t & 7) * 16)[j] =
+            e4m3_of_signed_nibbles(w, h);
     }
     for (int i = threadIdx.x; i < G * MT; i += kThreads) {
         const int g = i / MT, t = i - g * MT, m = tok0 + t;
@@ -190,11 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma::fence_after_sync();
                 const int ng = 2 * pp + 1 < G ? 2 : 1;
                 for (int gi = 0; gi < ng; ++gi) {
-                    const uint32_t bg = b0 + (uint32_t)(2 * pp + gi) * 1024;
+                    const uint32_t bg = b0 + (uint32_t)(2 * pp + gi) * kTokBytes;
+                    // token rows 8..15: the second core-matrix row (16 tokens), else
+                    // rows 0..7 again through a zero stride (ignored)
+                    constexpr uint32_t kSbo = MT > 8 ? 1024 : 0;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma::mma_e4m3_ta(tbase + kDcol + 32 * s + 16 * gi, tbase + kAcol + 64 * s + 32 * gi + 8 * kk,
-                                          umma::smem_desc(bg + kk * 256, 128, 0), idesc, kk > 0 ? 1u : 0u);
+                                          umma::smem_desc(bg + kk * 256, 128, kSbo), idesc, kk > 0 ? 1u : 0u);
                 }
                 umma::mma_commit(&done[s]);
                 if (++pp == P) pp = 0;
@@ -261,26 +271,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ng = 2 * pp + 1 < G ? 2 : 1;
             wait(&done[s], (uint32_t)((p / kPSlots) & 1));
             umma::fence_after_sync();
-            uint32_t d0[MT], d1[MT];
-            umma::tmem_ld_cols<MT>(tbase + kDcol + 32 * s + lane_base, d0);
-            umma::tmem_ld_cols<MT>(tbase + kDcol + 32 * s + 16 + lane_base, d1);
-            umma::tmem_ld_wait();
-            umma::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) umma::mbar_arrive(&freed[s]);
             const uint32_t zw[2] = {za, zb};
             if (p + 1 < n_pairs) zload(za, zb);
             const int n = (blockIdx.x + step * gridDim.x) * 128 + erow;
+            // the two groups' columns one after the other (registers for 16
+            // tokens); the slot is freed once both are read
 #pragma unroll
             for (int gi = 0; gi < 2; ++gi) {
                 if (gi == 1 && ng == 1) break;
+                uint32_t dg[MT];
+                umma::tmem_ld_cols<MT>(tbase + kDcol + 32 * s + 16 * gi + lane_base, dg);
+                umma::tmem_ld_wait();
+                if (gi == ng - 1) {                        // once per pair, after its last read
+                    umma::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) umma::mbar_arrive(&freed[s]);
+                }
                 const int g = 2 * pp + gi;
                 const float zf = __half2float(__ushort_as_half((uint16_t)(zw[gi] >> 16)));
                 const float sf = __half2float(__ushort_as_half((uint16_t)(zw[gi] & 0xFFFF)));
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
                     const float2 xv = sxq[g * MT + t];
-                    const float I = __fmaf_rn(__uint_as_float(gi ? d1[t] : d0[t]), 262144.0f, -(zf * xv.y));
+                    const float I = __fmaf_rn(__uint_as_float(dg[t]), 262144.0f, -(zf * xv.y));
                     acc[t] = __fmaf_rn(I, __fmul_rn(xv.x, sf), acc[t]);
                     if (dbg_I && n < N && tok0 + t < M) dbg_I[((size_t)(tok0 + t) * N + n) * G + g] = (int32_t)I;
                 }
@@ -340,16 +353,17 @@ int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t 
 
 }  // namespace
 
-// Decode-sized W4A4 on the tensor cores (M <= 8): QSPEC_OK, or
+// Decode-sized W4A4 on the tensor cores (M <= 16): QSPEC_OK, or
 // QSPEC_ERR_SHAPE before any launch when the shape does not suit the kernel.
 int launch_w4a4_gemv_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                         const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I,
                         int32_t *dev_status, cudaStream_t stream) {
-    if (M > 8) return QSPEC_ERR_SHAPE;
+    if (M > 16) return QSPEC_ERR_SHAPE;
     if (M == 1) return tg::launch<1>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
     if (M == 2) return tg::launch<2>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
     if (M <= 4) return tg::launch<4>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
-    return tg::launch<8>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
+    if (M <= 8) return tg::launch<8>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
+    return tg::launch<16>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
 }
 
 }  // namespace qspec

@@ -128,9 +128,11 @@ def test_prefill_m4096():
 
 # ----------------------------------------------------------------- decode M, many row tiles
 # Shapes with at least one 128-row tile per SM take the tensor-memory GEMV
-# path at 3 <= M <= 8 (the warp-MMA kernel below that); a ragged last tile,
-# an odd group count and every token count class are covered.
-@pytest.mark.parametrize("M,K,seed", [(1, 1152, 20), (2, 2048, 21), (3, 1152, 22), (5, 2048, 23), (8, 1152, 24)])
+# path at 3 <= M <= 16 (the one-token kernel and the warp-MMA kernel below
+# that); a ragged last tile, an odd group count and every token count class
+# (1, 2, 4, 8 and 16 token columns) are covered.
+@pytest.mark.parametrize("M,K,seed", [(1, 1152, 20), (2, 2048, 21), (3, 1152, 22), (5, 2048, 23), (8, 1152, 24),
+                                      (12, 1152, 25), (16, 2048, 26)])
 def test_decode_many_tiles_full_compare(M, K, seed):
     dev = need_gpu()
     N = 19456 + 77
@@ -173,7 +175,7 @@ def test_lm_head_decode_m1_m4():
 # ----------------------------------------------------------------- quantiser fused into the linear
 @pytest.mark.parametrize("M,N,K,seed", [(1, 300, 1152, 30), (2, 4096, 4096, 31), (5, 96, 640, 32),
                                         (8, 1000, 384, 33), (17, 64, 512, 34), (4, 19533, 1152, 35),
-                                        (40, 200, 256, 36), (1, 4096, 14336, 37)])
+                                        (40, 200, 256, 36), (1, 4096, 14336, 37), (16, 19533, 2048, 38)])
 def test_fused_quant_linear_equals_two_calls(M, N, K, seed):
     """qspec_linear_w4a4_bf16 gives bit for bit what qspec_quant_act_int4 then
     qspec_linear_w4a4 give (and the oracle), on every dispatch path."""
