@@ -414,14 +414,31 @@ int launch(const Act &a, const uint8_t *packed, const uint32_t *sz, int M, int N
                       K, y, ldy, dbg_I, a.x, a.ldx, a.xq_out, a.sx_out, a.qs_out, dev_status);
 }
 
+// tokens per CTA of the warp-MMA path: up to 8 (one MMA column block),
+// halved while two CTAs would not fit on an SM
+int tokens_per_cta(int M, int K) {
+    constexpr size_t kTwoPerSm = 112 * 1024;
+    int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
+    while (mt > 1 && smem_bytes(mt, K) > kTwoPerSm) mt /= 2;
+    return mt;
+}
+
+// up to 32 tokens go to the tensor-core kernel (all tokens of a 128-row tile
+// in one CTA) when the warp-MMA path would read the weights more than 12
+// times: large K leaves room for one token per warp-MMA CTA, whose time grows
+// by ~7 us per token tile on a 4096 x 14336 layer, while the tensor-core
+// kernel takes 100-150 us at any token count up to 32 (measured crossover
+// near 13 tiles)
+bool use_tc(int M, int K) {
+    const int mt = tokens_per_cta(M, K);
+    return (M + mt - 1) / mt > 12;
+}
+
 // warp-MMA path for M <= 32: QSPEC_ERR_SHAPE when the shape does not fit
 int launch_small(const Act &a, const uint8_t *packed, const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy,
                  int32_t *dbg_I, int32_t *dev_status, cudaStream_t st) {
-    // tokens per CTA: up to 8 (one MMA column block), halved while two CTAs
-    // would not fit on an SM
-    constexpr size_t kTwoPerSm = 112 * 1024, kMaxSmem = 200 * 1024;
-    int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
-    while (mt > 1 && smem_bytes(mt, K) > kTwoPerSm) mt /= 2;
+    constexpr size_t kMaxSmem = 200 * 1024;
+    const int mt = tokens_per_cta(M, K);
     if (smem_bytes(mt, K) > kMaxSmem) return QSPEC_ERR_SHAPE;
     switch (mt) {
         case 1: return launch<1>(a, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, st);
@@ -466,6 +483,7 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
         rc = launch_w4a4_gemv_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
         if (rc != QSPEC_ERR_SHAPE) return rc;
     }
+    if (hm::use_tc(M, K)) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
     const hm::Act act = {xq, sx, qs, nullptr, 0, nullptr, nullptr, nullptr};
     return hm::launch_small(act, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
 }
@@ -486,7 +504,7 @@ extern "C" int qspec_linear_w4a4_bf16(const uint16_t *x_bf16, int ldx, const uin
                               dev_status, st);
         if (rc != QSPEC_ERR_SHAPE) return rc;
     }
-    if (M <= 32 && !hm::use_gemv_tc(M, N)) {
+    if (M <= 32 && !hm::use_gemv_tc(M, N) && !hm::use_tc(M, K)) {
         const hm::Act act = {xq, sx, qs, x_bf16, ldx, xq, sx, qs};
         rc = hm::launch_small(act, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
         if (rc != QSPEC_ERR_SHAPE) return rc;

@@ -38,7 +38,11 @@ def run_w4a4(x, packed, sz, dev, want_I=True):
     (33, 31, 1152, 10),
     # W4A16 with the groups of a tile split over a cluster of 4 or 8 CTAs
     # (uneven splits included), W4A4 on the tensor cores
-    (80, 300, 1024, 11), (50, 1000, 2048, 12), (24, 130, 1152, 13), (128, 257, 4096, 14)])
+    (80, 300, 1024, 11), (50, 1000, 2048, 12), (24, 130, 1152, 13), (128, 257, 4096, 14),
+    # large K (one token per warp-MMA CTA): W4A4 at 13..32 tokens on the
+    # tensor cores, fewer on the warp-MMA kernel with one CTA column per token
+    (5, 150, 14336, 15), (16, 200, 14336, 16), (32, 130, 18944, 17), (4, 70, 14336, 18),
+    (12, 90, 14336, 19), (13, 90, 18944, 20)])
 def test_small_full_compare(M, N, K, seed):
     dev = need_gpu()
     packed, sz, po, szo = make_layer(N, K, seed, dev)
