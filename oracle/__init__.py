@@ -15,6 +15,8 @@ Pages cited:
   QSPEC summary   -- "QSPEC: Speculative Decoding with Complementary
                      Quantization Schemes", summary page (molayo1419.me);
                      sections: background terms, QSPEC structure.
+  SpecKV blog     -- "SpecKV: compression-aware gamma selection";
+                     architecture section (the controller's draft features).
 
 Parity pins: every function here is checked by ``tests/test_oracle_pins.py``
 against closed forms, brute force or special cases.  The W4A16 reference is
@@ -98,6 +100,8 @@ def _load():
         lib.orc_verify_sample.argtypes = [_P(u16), _P(u16), _P(i32), I, I, I, u64, u64,
                                           _P(i32), _P(i32)]
         lib.orc_verify_sample.restype = I
+        lib.orc_draft_sample.argtypes = [_P(u16), I, I, u64, u64, I, _P(i32), _P(f32), _P(f64)]
+        lib.orc_draft_sample.restype = I
         lib.orc_kv_overwrite.argtypes = [_P(u16), _P(u16), _P(u16), _P(u16), _P(i32), _P(i32),
                                          I, I, I, I, I, I]
         lib.orc_kv_overwrite.restype = I
@@ -287,6 +291,27 @@ def verify_sample(p_bits, q_bits, draft, seed, rnd):
                                    ctypes.c_uint64(seed), ctypes.c_uint64(rnd),
                                    _ptr(n_acc, ctypes.c_int32), _ptr(out, ctypes.c_int32))
     return st, n_acc, out
+
+
+# ---------------------------------------------------------------------------
+# draft-side sampling -- QSPEC summary, background: the draft model proposes
+# x ~ q(x|h); SpecKV blog, architecture (feature extraction): the gamma
+# controller reads the draft softmax's confidence (largest probability) and
+# entropy -sum p log(p + 1e-9).
+# ---------------------------------------------------------------------------
+def draft_sample(q_bits, seed, rnd, step):
+    """q_bits: uint16 bf16 logits [B][V]; step: draft position 1..16.
+    Returns (status, token int32 [B], confidence float32 [B], entropy float64 [B])."""
+    q_bits = _c(q_bits, np.uint16)
+    B, V = q_bits.shape
+    assert 1 <= step <= 16
+    token = np.zeros(B, np.int32)
+    conf = np.zeros(B, np.float32)
+    ent = np.zeros(B, np.float64)
+    st = _load().orc_draft_sample(_ptr(q_bits, ctypes.c_uint16), B, V, ctypes.c_uint64(seed),
+                                  ctypes.c_uint64(rnd), step, _ptr(token, ctypes.c_int32),
+                                  _ptr(conf, ctypes.c_float), _ptr(ent, ctypes.c_double))
+    return st, token, conf, ent
 
 
 # ---------------------------------------------------------------------------

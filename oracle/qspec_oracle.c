@@ -16,6 +16,9 @@
  *   [QS-design] same page, "QSPEC structure": W4A4 draft, W4A16 verify on
  *             T<=i ++ T^_{i+1:i+gamma} giving gamma+1 distributions, one
  *             shared 4-bit weight set, KV overwrite for accepted tokens.
+ *   [SK]      "SpecKV: compression-aware gamma selection" blog, architecture
+ *             section: the controller's draft features, confidence (largest
+ *             probability) and entropy -sum p log(p + 1e-9).
  *
  * Where the pages are silent the readings below are taken (each one is also
  * listed in the design notes of the repository):
@@ -39,7 +42,11 @@
  *   - random numbers: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11),
  *     key = (seed lo, seed hi), counter = (slot, b, round lo, round hi),
  *     U = word0 >> 8; slot i-1 for the test at draft position i, slot gamma
- *     for the correction / bonus draw.
+ *     for the correction / bonus draw, slot 16 + i for drawing the draft
+ *     token at position i (1 <= i <= 16) from the draft distribution;
+ *   - draft statistics: confidence = largest fixed-point probability,
+ *     (float)((double) max_v E_v / (double) S); entropy = -sum_v p_v
+ *     log(p_v + 1e-9) with p_v = E_v / S, in fp64.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fopenmp -shared
  * -fPIC.  fp-contract must stay off: every fused multiply-add below is an
@@ -528,6 +535,62 @@ int orc_verify_sample(const uint16_t *P, const uint16_t *Q, const int32_t *draft
         n_acc[b] = A;
     }
     free(Ep);
+    free(w);
+    return st;
+}
+
+/* ------------------------------------------------------------------ */
+/* draft-side sampling and the draft statistics                         */
+/* ------------------------------------------------------------------ */
+
+/*
+ * [QS-bg] the draft model proposes x ~ q(x|h), the distribution the
+ * acceptance test divides by.  [SK] "SpecKV: compression-aware gamma
+ * selection" blog, architecture section (feature extraction step): the gamma
+ * controller reads two statistics of the draft model's softmax over the
+ * vocabulary, its confidence (the largest probability) and its entropy,
+ * -sum_v p_v log(p_v + 1e-9).  Per row b of Q [B][V]: the fixed-point
+ * weights E_v and S of the verification above; the token drawn from E with
+ * the uniform of slot 16 + step; confidence and entropy of p_v = E_v / S.
+ * Returns ORC_ERR_NONFINITE for a NaN or +inf logit or a row without mass
+ * (that row's outputs are then unspecified).
+ */
+int orc_draft_sample(const uint16_t *Q, int B, int V, uint64_t seed, uint64_t round, int step,
+                     int32_t *token, float *confidence, double *entropy)
+{
+    int st = ORC_OK;
+    uint64_t *E = malloc(sizeof(uint64_t) * (size_t)V);
+    u128 *w = malloc(sizeof(u128) * (size_t)V);
+    for (int b = 0; b < B; b++) {
+        uint64_t S;
+        float m;
+        int rs = orc_fixed_softmax_row(Q + (size_t)b * V, V, E, &S, &m);
+        if (rs != ORC_OK) {
+            st = rs;
+            token[b] = -1;
+            confidence[b] = 0.0f;
+            entropy[b] = 0.0;
+            continue;
+        }
+        uint64_t Emax = 0;
+        u128 W = 0;
+        for (int v = 0; v < V; v++) {
+            w[v] = E[v];
+            W += E[v];
+            if (E[v] > Emax)
+                Emax = E[v];
+        }
+        uint32_t U = orc_uniform24(seed, round, (uint32_t)(16 + step), (uint32_t)b);
+        token[b] = draw_index(w, V, W, U);
+        confidence[b] = (float)((double)Emax / (double)S);
+        double h = 0.0;
+        for (int v = 0; v < V; v++) {
+            double p = (double)E[v] / (double)S;
+            h += p * log(p + 1e-9);
+        }
+        entropy[b] = -h;
+    }
+    free(E);
     free(w);
     return st;
 }

@@ -6,7 +6,9 @@ plain integer algebra, and statistical laws the method must obey.
 Pages: "QSPEC: Speculative Decoding with Complementary Quantization Schemes"
 summary (molayo1419.me) -- background terms (dequantisation, W4A4 INT32
 accumulation, min(1, p/q) acceptance, greedy acceptance, first rejection,
-E[A] and E[L]) and "QSPEC structure" (shared weights, KV overwrite).
+E[A] and E[L]) and "QSPEC structure" (shared weights, KV overwrite);
+"SpecKV: compression-aware gamma selection" blog, architecture section (the
+draft statistics: confidence and entropy of the draft softmax).
 """
 import math
 import os
@@ -576,6 +578,105 @@ def test_sampled_status():
     P2 = P.copy()
     P2[0, 1, 2] = 0x7F80
     assert oracle.verify_sample(P2, Q, np.array([[0]], np.int32), 0, 0)[0] == oracle.ERR_NONFINITE
+
+
+# ---------------------------------------------------------------------------
+# draft-side sampling and the draft statistics (SpecKV blog, architecture:
+# confidence = largest probability, entropy = -sum p log(p + 1e-9))
+# ---------------------------------------------------------------------------
+NEG_INF_BF16 = 0xFF80
+
+
+def test_draft_statistics_closed_forms():
+    """Uniform rows have p = 1/V exactly: confidence 1/V and entropy
+    -log(1/V + 1e-9) (the 1e-9 moves it by ~V * 1e-9, far above the
+    tolerance); k equal logits and the rest -inf give 1/k; a single finite
+    logit gives confidence 1, entropy -log(1 + 1e-9) < 0 and that token."""
+    half = bf16_bits_of([0.5])[0]
+    for V in (1, 2, 7, 1000, 128256):
+        st, tok, conf, ent = oracle.draft_sample(np.full((1, V), half, np.uint16), 3, 4, 1)
+        assert st == 0 and 0 <= tok[0] < V
+        assert conf[0] == np.float32(1.0 / V)
+        assert abs(ent[0] + math.log(1.0 / V + 1e-9)) <= 1e-9
+    for V, k in ((10, 3), (5000, 17), (128256, 1000)):
+        row = np.full(V, NEG_INF_BF16, np.uint16)
+        hot = np.random.default_rng(V).choice(V, k, replace=False)
+        row[hot] = bf16_bits_of([-1.25])[0]
+        st, tok, conf, ent = oracle.draft_sample(row[None], 5, 6, 2)
+        assert st == 0 and tok[0] in hot
+        assert conf[0] == np.float32(1.0 / k)
+        assert abs(ent[0] + math.log(1.0 / k + 1e-9)) <= 1e-9
+    row = np.full(300, bf16_bits_of([-40.0])[0], np.uint16)     # e^-40 is below the fixed-point grid
+    row[123] = bf16_bits_of([2.0])[0]
+    st, tok, conf, ent = oracle.draft_sample(row[None], 7, 8, 16)
+    assert st == 0 and tok[0] == 123 and conf[0] == 1.0
+    assert abs(ent[0] + math.log(1.0 + 1e-9)) <= 1e-15 and ent[0] < 0
+
+
+def test_draft_statistics_match_float64_softmax():
+    """Random rows (N(0, 2^2), some -inf): confidence and entropy against the
+    float64 softmax computed with numpy, within the fixed-point weights'
+    error (own exp within 4 ulp of fp32, E rounded to 2^-32)."""
+    rng = np.random.default_rng(31)
+    B, V = 6, 5000
+    l = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+    bits = (l.view(np.uint32) >> 16).astype(np.uint16)        # truncate to bf16
+    bits[:, rng.choice(V, 50, replace=False)] = NEG_INF_BF16
+    st, tok, conf, ent = oracle.draft_sample(bits, 11, 12, 3)
+    assert st == 0
+    lf = bf16_to_f64(bits)
+    p = np.exp(lf - lf.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    H = -(p * np.log(p + 1e-9)).sum(1)
+    np.testing.assert_allclose(conf, p.max(1), rtol=1e-6)
+    assert np.all(np.abs(ent - H) <= 1e-5 * (1 + H))
+    assert np.all(p[np.arange(B), tok] > 0)                   # never a -inf token
+
+
+def test_draft_draw_rule_and_slot():
+    """Two equal logits: E = (2^32, 2^32), so T = floor(U 2^33 / 2^24) and
+    token 1 is drawn exactly when U >= 2^23, U the Philox uniform of slot
+    16 + step for row b (Philox pinned by its known answers)."""
+    B = 64
+    q = np.tile(bf16_bits_of([0.75, 0.75]), (B, 1))
+    for step in (1, 7, 16):
+        st, tok, _, _ = oracle.draft_sample(q, 2024, 99, step)
+        assert st == 0
+        want = [int(oracle.uniform24(2024, 99, 16 + step, b) >= (1 << 23)) for b in range(B)]
+        assert tok.tolist() == want
+
+
+def test_draft_tokens_follow_softmax_chi_square():
+    """Over many rows of the same logits (independent uniforms per row) the
+    drawn token follows the softmax of the row, and the draws of two draft
+    positions differ."""
+    from scipy.stats import chi2 as chi2dist
+    V, B = 8, 200000
+    lv = np.array([1.0, 0.5, 0.0, -1.0, 2.0, -0.5, 0.25, 1.5], np.float32)
+    row = bf16_bits_of(lv)
+    p = np.exp(lv.astype(np.float64) - lv.max())
+    p /= p.sum()
+    draws = []
+    for step in (1, 2):
+        st, tok, _, _ = oracle.draft_sample(np.tile(row, (B, 1)), 5, 0, step)
+        assert st == 0
+        counts = np.bincount(tok, minlength=V)
+        exp = p * B
+        assert chi2dist.sf(((counts - exp) ** 2 / exp).sum(), V - 1) > 1e-3
+        draws.append(tok)
+    assert (draws[0] != draws[1]).mean() > 0.5
+
+
+def test_draft_status():
+    q = np.tile(bf16_bits_of([0.0, 1.0, 2.0]), (3, 1))
+    assert oracle.draft_sample(q, 0, 0, 1)[0] == 0
+    for bad in (0x7FC0, 0x7F80):                               # NaN, +inf
+        q2 = q.copy()
+        q2[1, 2] = bad
+        assert oracle.draft_sample(q2, 0, 0, 1)[0] == oracle.ERR_NONFINITE
+    q3 = q.copy()
+    q3[2, :] = NEG_INF_BF16                                    # a row without mass
+    assert oracle.draft_sample(q3, 0, 0, 1)[0] == oracle.ERR_NONFINITE
 
 
 # ---------------------------------------------------------------------------
