@@ -444,6 +444,15 @@ def row_kernels(dev, stream, reps=5, calls=10):
     rec("a6_verify_sample", lambda: q.qspec_verify_sample(P, Q, d, B, g, V, 5, 0, n_acc, o, ws, ws.numel()),
         2 * B * (2 * g + 1) * V, "B 256, gamma 4, V 128256")
     del P, Q, d, ws
+    B = 16
+    Qd = syn.logits_noisy_draft(B, 1, V, 98, device=dev)[1][:, 0, :].contiguous()
+    dws = q.draft_workspace(B, V, dev)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    conf = torch.empty(B, dtype=torch.float32, device=dev)
+    ent = torch.empty(B, dtype=torch.float32, device=dev)
+    rec("next_draft_sample", lambda: q.qspec_draft_sample(Qd, B, V, 5, 0, 1, tok, conf, ent, dws, dws.numel()),
+        2 * B * V, "B 16, V 128256, one draft position: token, confidence, entropy")
+    del Qd, dws
     L, B, H, T, D = 32, 16, 8, 4096, 128
     kc, vc = syn.kv_cache(L, B, H, T, D, 95, device=dev)
     kn, vn = syn.kv_new(L, B, g, H, D, 96, device=dev)

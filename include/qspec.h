@@ -235,6 +235,39 @@ int qspec_verify_sample_noalloc(const uint16_t *p_logits, const uint16_t *q_logi
                                 uint64_t round, int32_t *n_acc, int32_t *out, int32_t *dev_status,
                                 qspec_stream_t stream);
 
+/* Bytes of workspace qspec_draft_sample needs for (B, V). */
+size_t qspec_draft_workspace_bytes(int B, int V);
+
+/*
+ * Draft-side sampling with the draft statistics.  [QS-bg] the draft model
+ * proposes x ~ q(x|h), the distribution the acceptance test of
+ * qspec_verify_sample divides by.  SpecKV blog ("SpecKV: compression-aware
+ * gamma selection"), architecture section, feature extraction: a gamma
+ * controller reads the confidence (the largest probability) and the entropy
+ * -sum_v p_v log(p_v + 1e-9) of the draft model's softmax.  Per row b, with
+ * the fixed-point weights of qspec_verify_sample (E_v, S = sum_v E_v):
+ *   token[b]      = min{v : sum_{u<=v} E_u > floor(U * S / 2^24)}, U the
+ *                   24-bit Philox uniform of slot 16 + step (slots 0..16 are
+ *                   the verification's), so a draft drawn here is
+ *                   distributed as the q' the acceptance test uses;
+ *   confidence[b] = max_v E_v / S, the fp64 quotient rounded to fp32
+ *                   (bit-exact);
+ *   entropy[b]    = -sum_v p_v log(p_v + 1e-9), p_v = E_v / S, summed in
+ *                   fp32 (within 1e-4 (1 + H) of the fp64 value).
+ *
+ *   q_logits   uint16 [B][V]   draft logits of one draft position, bf16
+ *   step       1..16           the draft position (selects the uniform)
+ *   token      int32  [B]      out
+ *   confidence float  [B]      out
+ *   entropy    float  [B]      out
+ *   workspace, ws_bytes        device scratch of qspec_draft_workspace_bytes(B, V)
+ * Device errors: QSPEC_ERR_NONFINITE (NaN or +inf logit, or a row that is
+ * all -inf; that row's outputs are unspecified).
+ */
+int qspec_draft_sample(const uint16_t *q_logits, int B, int V, uint64_t seed, uint64_t round, int step,
+                       int32_t *token, float *confidence, float *entropy, void *workspace, size_t ws_bytes,
+                       int32_t *dev_status, qspec_stream_t stream);
+
 /*
  * a7. KV overwrite.  [QS-design] for accepted tokens the low-precision (W4A4)
  * KV-cache entries are replaced with the W4A16 ones, so later steps read the

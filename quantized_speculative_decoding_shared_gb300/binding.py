@@ -32,7 +32,8 @@ ERR_RANGE, ERR_ZERO_POINT, ERR_NONFINITE, ERR_TIMEOUT, ERR_UNSUPPORTED = 6, 7, 8
 EXPORTED = ["qspec_version", "qspec_status_string", "qspec_last_cuda_error", "qspec_pack_weights",
             "qspec_quant_act_int4", "qspec_linear_w4a4", "qspec_linear_w4a4_bf16", "qspec_linear_w4a16",
             "qspec_verify_workspace_bytes", "qspec_verify_greedy", "qspec_verify_sample",
-            "qspec_kv_overwrite", "qspec_verify_sample_noalloc"]
+            "qspec_kv_overwrite", "qspec_verify_sample_noalloc", "qspec_draft_workspace_bytes",
+            "qspec_draft_sample"]
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
@@ -79,6 +80,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                    i32),
             "qspec_verify_sample_noalloc": ([vp, vp, vp, i32, i32, i32, u64, u64, vp, vp, vp, vp],
                                             i32),
+            "qspec_draft_workspace_bytes": ([i32, i32], sz_t),
+            "qspec_draft_sample": ([vp, i32, i32, u64, u64, i32, vp, vp, vp, vp, sz_t, vp, vp], i32),
         }
         for name, (args, res) in proto.items():
             f = getattr(lib, name)
@@ -179,6 +182,17 @@ def qspec_verify_sample_noalloc(p, q, draft, B, gamma, V, seed, rnd, n_acc, out,
                                                       _stream(stream))
 
 
+def qspec_draft_workspace_bytes(B, V):
+    return int(load_library().qspec_draft_workspace_bytes(B, V))
+
+
+def qspec_draft_sample(q, B, V, seed, rnd, step, token, confidence, entropy, workspace, ws_bytes,
+                       dev_status=None, stream=None):
+    return load_library().qspec_draft_sample(_ptr(q), B, V, ctypes.c_uint64(seed), ctypes.c_uint64(rnd),
+                                             step, _ptr(token), _ptr(confidence), _ptr(entropy),
+                                             _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+
+
 def qspec_kv_overwrite(k_cache, v_cache, k_new, v_new, base_pos, n_acc, L, B, H, T, D, gamma,
                        dev_status=None, stream=None):
     return load_library().qspec_kv_overwrite(_ptr(k_cache), _ptr(v_cache), _ptr(k_new),
@@ -277,6 +291,27 @@ def verify_sample(p, q, draft, seed, rnd, workspace=None, dev_status=None, strea
     _check(qspec_verify_sample(p, q, draft, B, gamma, V, seed, rnd, n_acc, out, ws, ws.numel(),
                                dev_status, stream), "qspec_verify_sample")
     return n_acc, out
+
+
+def draft_workspace(B, V, device="cuda"):
+    n = qspec_draft_workspace_bytes(B, V)
+    if n == 0:
+        raise QspecError(ERR_SHAPE, "qspec_draft_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def draft_sample(q, seed, rnd, step, workspace=None, dev_status=None, stream=None):
+    """q bf16 [B][V] draft logits of draft position step (1..16) ->
+    (token int32 [B], confidence fp32 [B], entropy fp32 [B])."""
+    _need(q, torch.bfloat16, "q")
+    B, V = q.shape
+    ws = workspace if workspace is not None else draft_workspace(B, V, q.device)
+    token = torch.empty(B, dtype=torch.int32, device=q.device)
+    conf = torch.empty(B, dtype=torch.float32, device=q.device)
+    ent = torch.empty(B, dtype=torch.float32, device=q.device)
+    _check(qspec_draft_sample(q, B, V, seed, rnd, step, token, conf, ent, ws, ws.numel(), dev_status,
+                              stream), "qspec_draft_sample")
+    return token, conf, ent
 
 
 def kv_overwrite(k_cache, v_cache, k_new, v_new, base_pos, n_acc, dev_status=None, stream=None):

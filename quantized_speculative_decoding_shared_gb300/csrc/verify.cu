@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(kThreads) sample_residual_kernel(
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) sample_draw_kernel(
     const uint16_t *__restrict__ P, const uint16_t *__restrict__ Q, int B, int gamma, int V,
-    int chunk, int n_chunks, uint64_t seed, uint64_t round, const uint32_t *__restrict__ maxenc,
+    int chunk, int n_chunks, uint64_t seed, uint64_t round, uint32_t slot, const uint32_t *__restrict__ maxenc,
     const unsigned long long *__restrict__ sums, const u128 *__restrict__ rsum,
     const unsigned long long *__restrict__ esum, const int32_t *__restrict__ accbuf,
     int32_t *__restrict__ out) {
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads) sample_draw_kernel(
         W = buf[kThreads - 1];
         __syncthreads();
     }
-    const uint32_t U = uniform24(seed, round, (uint32_t)gamma, (uint32_t)b);
+    const uint32_t U = uniform24(seed, round, slot, (uint32_t)b);
     const u128 T = ((u128)U * W) >> 24;
     // the first chunk whose inclusive prefix exceeds T
     if (threadIdx.x == 0) s_chunk = n_chunks - 1;
@@ -531,8 +531,8 @@ __global__ void __launch_bounds__(kThreads) sample_draw_kernel(
     const float mp = from_ordered_bits(maxenc[rp]);
     const uint64_t Sp = sums[rp];
     const int rq = B * (gamma + 1) + b * gamma + (residual ? A : 0);
-    const float mq = from_ordered_bits(maxenc[rq]);
-    const uint64_t Sq = sums[rq];
+    const float mq = residual ? from_ordered_bits(maxenc[rq]) : 0.0f;
+    const uint64_t Sq = residual ? sums[rq] : 0;
     const uint16_t *prow = P + (size_t)rp * V;
     const uint16_t *qrow = Q + ((size_t)b * gamma + (residual ? A : 0)) * V;
     const int c0 = c * chunk, c1 = min(V, c0 + chunk);
@@ -576,6 +576,85 @@ __global__ void __launch_bounds__(kThreads) sample_draw_kernel(
         running += total;
     }
     if (threadIdx.x == 0) out[(size_t)b * (gamma + 1) + A] = s_mode >= 0 ? s_mode : c1 - 1;
+}
+
+// -------------------------------------------------------------------------
+// draft-side sampling: the rows are Q[b] (B rows, gamma = 0 in the row
+// kernels above, A_b = 0 so the draw kernel draws from the row's own E)
+// -------------------------------------------------------------------------
+// grid (b, chunk): this chunk's sum of E_v and its part of the entropy sum
+// sum_v p_v log(p_v + 1e-9) (p_v = E_v / S in fp32); A_b = 0 for the draw.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) draft_chunk_kernel(const uint16_t *__restrict__ Q, int V, int chunk,
+                                                               const uint32_t *__restrict__ maxenc,
+                                                               const unsigned long long *__restrict__ sums,
+                                                               unsigned long long *__restrict__ esum,
+                                                               float *__restrict__ hpart,
+                                                               int32_t *__restrict__ accbuf) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ unsigned long long she[kThreads / 32];
+    __shared__ float shh[kThreads / 32];
+    const int b = blockIdx.x, n_chunks = gridDim.y;
+    const uint64_t S = sums[b];
+    const float m = from_ordered_bits(maxenc[b]);
+    const float inv = S ? (float)(1.0 / (double)S) : 0.0f;
+    const uint16_t *row = Q + (size_t)b * V;
+    const int c0 = blockIdx.y * chunk, c1 = min(V, c0 + chunk);
+    unsigned long long e = 0;
+    float h = 0.0f;
+    if (S) {                                   // a row without mass has no weights
+        for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
+            float f[8];
+            load8<VEC>(row, v0, c1, f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint64_t E = fixed_weight(f[i], m);
+                const float p = (float)E * inv;
+                e += E;
+                h += p * logf(p + 1e-9f);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        e += __shfl_xor_sync(0xffffffffu, e, o);
+        h += __shfl_xor_sync(0xffffffffu, h, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        she[threadIdx.x >> 5] = e;
+        shh[threadIdx.x >> 5] = h;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long et = 0;
+        float ht = 0.0f;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            et += she[w];
+            ht += shh[w];
+        }
+        esum[(size_t)b * n_chunks + blockIdx.y] = et;
+        hpart[(size_t)b * n_chunks + blockIdx.y] = ht;
+        if (blockIdx.y == 0) accbuf[b] = 0;
+    }
+}
+
+// one thread per row: entropy from the chunk parts (in chunk order) and the
+// confidence max_v E_v / S (the row maximum's weight, rint(qexp(0) 2^32))
+__global__ void draft_features_kernel(int B, int n_chunks, const uint32_t *__restrict__ maxenc,
+                                      const unsigned long long *__restrict__ sums,
+                                      const float *__restrict__ hpart, float *__restrict__ confidence,
+                                      float *__restrict__ entropy) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const uint64_t S = sums[b];
+    float h = 0.0f;
+    for (int c = 0; c < n_chunks; ++c) h += hpart[(size_t)b * n_chunks + c];
+    entropy[b] = -h;
+    const float m = from_ordered_bits(maxenc[b]);
+    confidence[b] = S ? (float)((double)fixed_weight(m, m) / (double)S) : 0.0f;
 }
 
 }  // namespace
@@ -670,7 +749,7 @@ static int launch_sample(const uint16_t *P, const uint16_t *Q, const int32_t *dr
                     L.chunk, seed, round, maxenc, sums, rsum, esum, accbuf, n_acc, out, dev_status);
     if (rc) return rc;
     return launch_pdl(w, sample_draw_kernel<VEC>, dim3(B), dim3(kThreads), 0, st, P, Q, B, gamma, V, L.chunk,
-                      L.n_chunks, seed, round, maxenc, sums, rsum, esum, accbuf, out);
+                      L.n_chunks, seed, round, (uint32_t)gamma, maxenc, sums, rsum, esum, accbuf, out);
 }
 
 extern "C" int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_logits,
@@ -746,4 +825,78 @@ extern "C" int qspec_verify_sample_noalloc(const uint16_t *p_logits, const uint1
     if (rc) return rc;
     return qspec_verify_sample(p_logits, q_logits, draft, B, gamma, V, seed, round, n_acc, out, scratch,
                                QSPEC_VERIFY_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Draft-side sampling with the draft statistics: the row statistics of the
+// sampled verification over the B draft rows (gamma = 0), per-chunk weight
+// sums and entropy parts, the draw of the verification's bonus path with the
+// uniform of slot 16 + step, then the features.  The workspace is the
+// verification layout for gamma = 0; the residual chunk sums (unused here)
+// hold the entropy parts.
+// ---------------------------------------------------------------------------
+extern "C" size_t qspec_draft_workspace_bytes(int B, int V) {
+    if (B < 1 || V < 1) return 0;
+    return make_layout(B, 0, V).total;
+}
+
+template <bool VEC>
+static int launch_draft(const uint16_t *Q, int B, int V, uint64_t seed, uint64_t round, int step, int32_t *token,
+                        float *confidence, float *entropy, const Layout &L, char *ws, int32_t *dev_status,
+                        cudaStream_t st) {
+    auto *maxenc = reinterpret_cast<uint32_t *>(ws + L.off_max);
+    auto *sums = reinterpret_cast<unsigned long long *>(ws + L.off_sum);
+    auto *rsum = reinterpret_cast<u128 *>(ws + L.off_rsum);
+    auto *hpart = reinterpret_cast<float *>(ws + L.off_rsum);
+    auto *esum = reinterpret_cast<unsigned long long *>(ws + L.off_esum);
+    auto *accbuf = reinterpret_cast<int32_t *>(ws + L.off_acc);
+    const char *w = "qspec_draft_sample";
+    int rc;
+    if (B >= 2 * sm_count()) {
+        rc = launch_pdl(w, sample_rowstats_kernel<VEC>, dim3(B), dim3(kRowThreads), 0, st, Q, Q, B, 0, V, maxenc,
+                        sums, dev_status);
+        if (rc) return rc;
+    } else {
+        cudaError_t e = cudaMemsetAsync(ws + L.off_max, 0, L.off_rsum - L.off_max, st);
+        if (e != cudaSuccess) {
+            set_last_error("qspec_draft_sample memset", e);
+            return QSPEC_ERR_LAUNCH;
+        }
+        dim3 grid_rows((unsigned)B, (unsigned)L.n_chunks);
+        rc = launch_pdl(w, sample_rowmax_kernel<VEC>, grid_rows, dim3(kThreads), 0, st, Q, Q, B, 0, V, L.chunk,
+                        maxenc, dev_status);
+        if (rc) return rc;
+        rc = launch_pdl(w, sample_rowsum_kernel<VEC>, grid_rows, dim3(kThreads), 0, st, Q, Q, B, 0, V, L.chunk,
+                        maxenc, sums, dev_status);
+        if (rc) return rc;
+    }
+    rc = launch_pdl(w, draft_chunk_kernel<VEC>, dim3((unsigned)B, (unsigned)L.n_chunks), dim3(kThreads), 0, st, Q, V,
+                    L.chunk, maxenc, sums, esum, hpart, accbuf);
+    if (rc) return rc;
+    rc = launch_pdl(w, sample_draw_kernel<VEC>, dim3(B), dim3(kThreads), 0, st, Q, Q, B, 0, V, L.chunk, L.n_chunks,
+                    seed, round, (uint32_t)(QSPEC_MAX_GAMMA + step), maxenc, sums, rsum, esum, accbuf, token);
+    if (rc) return rc;
+    return launch_pdl(w, draft_features_kernel, dim3((B + 127) / 128), dim3(128), 0, st, B, L.n_chunks, maxenc, sums,
+                      hpart, confidence, entropy);
+}
+
+extern "C" int qspec_draft_sample(const uint16_t *q_logits, int B, int V, uint64_t seed, uint64_t round, int step,
+                                  int32_t *token, float *confidence, float *entropy, void *workspace,
+                                  size_t ws_bytes, int32_t *dev_status, qspec_stream_t stream) {
+    if (!q_logits || !token || !confidence || !entropy || !workspace) return QSPEC_ERR_NULL;
+    if (B < 1 || V < 1 || step < 1 || step > QSPEC_MAX_GAMMA) return QSPEC_ERR_SHAPE;
+    if (!aligned(q_logits, 2) || !aligned(token, 4) || !aligned(confidence, 4) || !aligned(entropy, 4) ||
+        !aligned(workspace, 16))
+        return QSPEC_ERR_ALIGN;
+    const Layout L = make_layout(B, 0, V);
+    if (ws_bytes < L.total) return QSPEC_ERR_WORKSPACE;
+    int rc = check_device();
+    if (rc) return rc;
+    cudaStream_t st = as_cuda(stream);
+    char *ws = static_cast<char *>(workspace);
+    const bool vec = (V % 8 == 0) && aligned(q_logits, 16);
+    return vec ? launch_draft<true>(q_logits, B, V, seed, round, step, token, confidence, entropy, L, ws, dev_status,
+                                    st)
+               : launch_draft<false>(q_logits, B, V, seed, round, step, token, confidence, entropy, L, ws,
+                                     dev_status, st);
 }

@@ -98,3 +98,21 @@ def test_alignment_and_workspace_rejected_on_host(lib):
                                    fake(), need - 16, None, st) == 5
     assert lib.qspec_verify_greedy(fake(), fake(), 2, 3, 1000, fake(), fake(), fake(),
                                    need - 16, None, st) == 5
+
+
+def test_draft_sample_rejected_on_host(lib):
+    st = V(None)
+    need = binding.qspec_draft_workspace_bytes(4, 1000)
+    assert need > 0 and need % 16 == 0
+    assert binding.qspec_draft_workspace_bytes(0, 1000) == 0
+    ok = dict(q=fake(), B=4, Vv=1000, step=1, tok=fake(), conf=fake(), ent=fake(), ws=fake(), n=need)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.qspec_draft_sample(a["q"], a["B"], a["Vv"], 0, 0, a["step"], a["tok"], a["conf"],
+                                      a["ent"], a["ws"], a["n"], None, st)
+    assert call(q=V(None)) == 1 and call(tok=V(None)) == 1 and call(ws=V(None)) == 1
+    assert call(B=0) == 2 and call(Vv=0) == 2
+    assert call(step=0) == 2 and call(step=17) == 2           # draft positions 1..16
+    assert call(q=fake(0x1001)) == 3 and call(conf=fake(0x1002)) == 3 and call(ws=fake(0x1008)) == 3
+    assert call(n=need - 16) == 5
