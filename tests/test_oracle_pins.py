@@ -646,6 +646,38 @@ def test_draft_draw_rule_and_slot():
         assert tok.tolist() == want
 
 
+def test_draft_draw_rule_exact_on_uniform_rows():
+    """Uniform rows: E_v = 2^32, W = V 2^32, T = floor(U V 2^8) and the first
+    prefix (v + 1) 2^32 above T gives token floor(U V / 2^24) exactly.  With
+    V = 4096 the threshold equals a prefix sum (U V a multiple of 2^24) about
+    once in 4096 rows; the sample below holds such rows, where a >= in place
+    of > would pick the token before."""
+    V, B, seed, rnd, step = 4096, 16384, 606, 17, 5
+    q = np.full((B, V), bf16_bits_of([1.0])[0], np.uint16)
+    st, tok, conf, _ = oracle.draft_sample(q, seed, rnd, step)
+    assert st == 0 and np.all(conf == np.float32(1.0 / V))
+    U = np.array([oracle.uniform24(seed, rnd, 16 + step, b) for b in range(B)], np.int64)
+    assert np.array_equal(tok, (U * V) >> 24)
+    assert ((U * V) % (1 << 24) == 0).sum() >= 1                # ties present in the sample
+
+
+def test_draft_confidence_is_rounded_exact_quotient():
+    """confidence = max E / S (max E = 2^32, the weight of the row maximum)
+    as the fp64 quotient rounded to fp32: checked bit for bit against exact
+    rational arithmetic on random rows (S from the fixed-point row sums)."""
+    rng = np.random.default_rng(47)
+    B, V = 40, 3000
+    l = (rng.standard_normal((B, V)) * 1.5).astype(np.float32)
+    bits = (l.view(np.uint32) >> 16).astype(np.uint16)
+    st, _, conf, _ = oracle.draft_sample(bits, 1, 2, 3)
+    assert st == 0
+    for b in range(B):
+        st_r, E, S, _ = oracle.fixed_softmax_row(bits[b])
+        assert st_r == 0 and int(E.max()) == 1 << 32
+        want = round_to_mantissa(round_to_mantissa(Fraction(1 << 32, int(S)), 52), 23)
+        assert Fraction(float(conf[b])) == want
+
+
 def test_draft_tokens_follow_softmax_chi_square():
     """Over many rows of the same logits (independent uniforms per row) the
     drawn token follows the softmax of the row, and the draws of two draft
