@@ -179,7 +179,8 @@ def test_lm_head_decode_m1_m4():
 # ----------------------------------------------------------------- quantiser fused into the linear
 @pytest.mark.parametrize("M,N,K,seed", [(1, 300, 1152, 30), (2, 4096, 4096, 31), (5, 96, 640, 32),
                                         (8, 1000, 384, 33), (17, 64, 512, 34), (4, 19533, 1152, 35),
-                                        (40, 200, 256, 36), (1, 4096, 14336, 37), (16, 19533, 2048, 38)])
+                                        (40, 200, 256, 36), (1, 4096, 14336, 37), (16, 19533, 2048, 38),
+                                        (16, 300, 14336, 39), (32, 130, 18944, 40)])
 def test_fused_quant_linear_equals_two_calls(M, N, K, seed):
     """qspec_linear_w4a4_bf16 gives bit for bit what qspec_quant_act_int4 then
     qspec_linear_w4a4 give (and the oracle), on every dispatch path."""
