@@ -8,9 +8,9 @@ Importing the package does not load the library; the first call does, and
 raises if libqspec.so has not been built (``build.build()``).
 """
 from .binding import (QspecError, draft_sample, draft_workspace, kv_overwrite, linear_w4a4,
-                      linear_w4a16, load_library, pack_weights, quant_act_int4, verify_greedy,
-                      verify_sample, verify_workspace)
+                      linear_w4a4_bf16, linear_w4a16, load_library, pack_weights, quant_act_int4,
+                      verify_greedy, verify_sample, verify_workspace)
 
-__all__ = ["QspecError", "draft_sample", "draft_workspace", "kv_overwrite", "linear_w4a4", "linear_w4a16",
-           "load_library", "pack_weights", "quant_act_int4", "verify_greedy", "verify_sample",
+__all__ = ["QspecError", "draft_sample", "draft_workspace", "kv_overwrite", "linear_w4a4", "linear_w4a4_bf16",
+           "linear_w4a16", "load_library", "pack_weights", "quant_act_int4", "verify_greedy", "verify_sample",
            "verify_workspace"]
