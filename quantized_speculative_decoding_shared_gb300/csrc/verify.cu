@@ -1,4 +1,5 @@
-// verify.cu -- a5 greedy and a6 sampled verification of gamma draft tokens.
+// verify.cu -- a5 greedy and a6 sampled verification of gamma draft tokens,
+// and draft-side sampling with the draft statistics.
 //
 // QSPEC summary page, background terms: speculative sampling accepts a draft
 // x with probability min(1, p(x|h) / q(x|h)); greedy decoding accepts it when
@@ -24,6 +25,11 @@
 //            row hitting L2; else memset, then chunk x row kernels for each
 //            with atomics), decisions + residual chunk sums (chunk x
 //            sequence), draw (per sequence)
+//   draft  : the same row statistics over the B draft rows, weight sums and
+//            entropy parts (chunk x row), the draw on the row's own weights
+//            (Philox slot 16 + step), the features (per row).  SpecKV blog,
+//            architecture section: the confidence and entropy of the draft
+//            softmax are the features its gamma controller reads.
 // HBM traffic: one read of every logit (B (2 gamma + 1) V bf16) plus L2
 // re-reads of the rows a later phase needs.
 #include <algorithm>
