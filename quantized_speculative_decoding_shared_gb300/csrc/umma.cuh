@@ -203,34 +203,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t n;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(n));
-    return n;
-}
-// the two halves of cluster_sync(), for work in between
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
-__device__ __forceinline__ uint32_t peer_addr(const void *local_smem, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));
-    return remote;
-}
-__device__ __forceinline__ uint4 ld_peer_v4(const void *local_smem, uint32_t rank) {
-    uint4 v;
-    asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(peer_addr(local_smem, rank))
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ uint32_t ld_peer_u32(const void *local_smem, uint32_t rank) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(peer_addr(local_smem, rank)) : "memory");
-    return v;
-}
 __device__ __forceinline__ float ld_peer_f32(const void *local_smem, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));
