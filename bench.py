@@ -33,6 +33,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -159,12 +160,22 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text):
+    """C/C++ source without comments and with whitespace collapsed: what the
+    compiler sees, so that editing a comment keeps a record valid."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(name):
-    """The kernel's source file with the library headers it compiles in."""
+    """The kernel's source file with the library headers it compiles in
+    (code only: comments and whitespace do not count)."""
     d = os.path.join(ROOT, "quantized_speculative_decoding_shared_gb300", "csrc")
     h = hashlib.sha256()
     for f in (name, "qspec_device.cuh", "qspec_host.h"):
-        h.update(open(os.path.join(d, f), "rb").read())
+        h.update(_code_only(open(os.path.join(d, f)).read()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

@@ -49,9 +49,9 @@ int launch_w4a4_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const 
                    const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st,
                    cudaStream_t stream);
 
-// Decode-sized W4A4 (M <= 8) on the tensor cores with the weights staged in
-// TMEM (w4a4_gemv_tc.cu); QSPEC_ERR_SHAPE before any launch when the shape
-// does not suit it.
+// Decode-sized W4A4 (3 <= M <= 16) on the tensor cores with the weights
+// staged in TMEM (w4a4_gemv_tc.cu); QSPEC_ERR_SHAPE before any launch when
+// the shape does not suit it.
 int launch_w4a4_gemv_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                         const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I,
                         int32_t *dev_status, cudaStream_t stream);

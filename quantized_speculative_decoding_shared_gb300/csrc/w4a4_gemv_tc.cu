@@ -358,9 +358,8 @@ int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t 
 int launch_w4a4_gemv_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                         const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I,
                         int32_t *dev_status, cudaStream_t stream) {
-    if (M > 16) return QSPEC_ERR_SHAPE;
-    if (M == 1) return tg::launch<1>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
-    if (M == 2) return tg::launch<2>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
+    // 3..16 tokens (one and two tokens have their own kernels)
+    if (M < 3 || M > 16) return QSPEC_ERR_SHAPE;
     if (M <= 4) return tg::launch<4>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
     if (M <= 8) return tg::launch<8>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
     return tg::launch<16>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
