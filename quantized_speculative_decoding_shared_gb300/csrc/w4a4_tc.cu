@@ -1,5 +1,6 @@
 // w4a4_tc.cu -- a3, W4A4 linear on the Blackwell tensor cores for larger M
-// (draft passes of large batches, prefill).
+// (draft passes of large batches, prefill; also 13..32 tokens at large K,
+// where the warp-MMA kernel would hold one token per CTA).
 //
 // QSPEC summary page, background terms: 4-bit activations times 4-bit
 // weights, products accumulated exactly (INT32 in the pages' wording), then
