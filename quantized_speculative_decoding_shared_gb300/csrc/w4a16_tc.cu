@@ -77,6 +77,7 @@ struct Smem {
     uint8_t a[kStages][kTileN * kKB];
     uint8_t b[kStages][BN * kKB];
     uint64_t full[kStages], empty[kStages], accf[2], acce[2];
+    uint64_t drain;                    // after a timeout: the MMAs in flight have finished
     uint32_t tmem;
     int timeout;
 };
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&sm.accf[b], 1);
             umma::mbar_init(&sm.acce[b], kEpilogue);
         }
+        umma::mbar_init(&sm.drain, 1);
         sm.timeout = 0;
         umma::mbar_fence_init();
     }
@@ -279,6 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     umma::fence_before_sync();
     __syncthreads();
+    // after a timeout, the MMAs already issued finish (bounded wait) before
+    // the TMEM they write is freed; sm.timeout is settled at this barrier
+    if (sm.timeout) {
+        if (warp == kThreads / 32 - 1 && lane == 0) {
+            umma::mma_commit(&sm.drain);
+            umma::mbar_wait(&sm.drain, 0);
+        }
+        __syncthreads();
+    }
     if (C > 1) {
         // split groups: every CTA's partials -> its shared memory (the operand
         // stages are free now: all MMAs have completed); rank 0 adds them in

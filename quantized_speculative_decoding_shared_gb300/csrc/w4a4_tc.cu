@@ -99,6 +99,7 @@ struct Smem {
     float esx[2][BN];                  // epilogue-owned: sx of the group's tokens
     float enqs[2][BN];                 // -qs as float (exact)
     uint64_t full[kStages], empty[kStages], accf[2], acce[2];
+    uint64_t drain;                    // after a timeout: the MMAs in flight have finished
     uint32_t tmem;
     int timeout;
 };
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&sm.accf[b], 1);
             umma::mbar_init(&sm.acce[b], kEpilogue);
         }
+        umma::mbar_init(&sm.drain, 1);
         sm.timeout = 0;
         umma::mbar_fence_init();
     }
@@ -282,6 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     umma::fence_before_sync();
     __syncthreads();
+    // after a timeout, the MMAs already issued finish (bounded wait) before
+    // the TMEM they write is freed; sm.timeout is settled at this barrier
+    if (sm.timeout) {
+        if (warp == kThreads / 32 - 1 && lane == 0) {
+            umma::mma_commit(&sm.drain);
+            umma::mbar_wait(&sm.drain, 0);
+        }
+        __syncthreads();
+    }
     if (tid == 0 && sm.timeout) flag(st, QSPEC_ERR_TIMEOUT);
     if (warp == 0) umma::tmem_free(tmem, kCols);
 }
