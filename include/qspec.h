@@ -15,7 +15,10 @@
  * Conventions for every call
  *   - Every pointer argument is a DEVICE pointer, owned by the caller, unless
  *     stated otherwise.  The library allocates no device memory and keeps no
- *     state between calls.  Outputs are written in place.
+ *     state between calls, with one exception: the fixed scratch array of
+ *     qspec_verify_sample_noalloc (below), which lives in the library image
+ *     and keeps its contents from one call of that entry point to the next.
+ *     Outputs are written in place.
  *   - bf16 and fp16 values travel as uint16_t bit patterns.
  *   - Calls are enqueued on `stream` and return right after launch; results
  *     and *dev_status are valid once the stream has synchronised.
@@ -224,7 +227,10 @@ int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_logits, cons
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call shares the one array and leaves its
+ * before any stream capture.  The address is remembered per CUDA context:
+ * after a cudaDeviceReset, or in a new context on the same device, the next
+ * call looks it up again, so that call too must come before any capture.
+ * Every call shares the one array and leaves its
  * contents behind (the parts that must start at zero are cleared on the
  * stream by each call): calls that may overlap on the GPU -- on different
  * streams, or from different threads -- race and must not be issued.

@@ -34,6 +34,8 @@
 // re-reads of the rows a later phase needs.
 #include <algorithm>
 
+#include <mutex>
+
 #include "qspec_device.cuh"
 #include "qspec_host.h"
 
@@ -790,10 +792,48 @@ extern "C" int qspec_verify_sample(const uint16_t *p_logits, const uint16_t *q_l
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_noalloc_scratch[QSPEC_VERIFY_NOALLOC_SCRATCH_BYTES];
 
-// Device address of the array, looked up once per device with that device
-// current.  In host code the symbol g_noalloc_scratch is only a host-side
-// stand-in; a kernel handed it would read the wrong memory.
-static void *g_noalloc_addr[64];
+// Device address of the array, looked up with the device current and
+// remembered per CUDA context (keyed on the context's unique id, so a
+// cudaDeviceReset or a new context on the same device triggers a fresh
+// lookup instead of handing the kernels an address from a context that no
+// longer exists).  In host code the symbol g_noalloc_scratch is only a
+// host-side stand-in; a kernel handed it would read the wrong memory.
+namespace {
+
+typedef CUresult (*CtxGetCurrent)(CUcontext *);
+typedef CUresult (*CtxGetId)(CUcontext, unsigned long long *);
+
+struct NoallocSlot {
+    unsigned long long ctx_id;
+    void *addr;
+};
+NoallocSlot g_noalloc_slot[64];
+std::mutex g_noalloc_mu;
+
+// id of the calling thread's current context; false when there is none or
+// the driver entry points are not available
+bool current_ctx_id(unsigned long long *id) {
+    static CtxGetCurrent get_current = nullptr;
+    static CtxGetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetId>(p);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return false;
+    return get_id(c, id) == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 static int noalloc_scratch(void **ptr) {
     int dev = 0;
@@ -803,16 +843,29 @@ static int noalloc_scratch(void **ptr) {
         return QSPEC_ERR_LAUNCH;
     }
     if (dev < 0 || dev >= 64) return QSPEC_ERR_UNSUPPORTED;
-    if (g_noalloc_addr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            set_last_error("cudaGetSymbolAddress(g_noalloc_scratch)", e);
-            return QSPEC_ERR_LAUNCH;
-        }
-        g_noalloc_addr[dev] = p;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    unsigned long long id = 0;
+    const bool have_id = current_ctx_id(&id);
+    NoallocSlot &slot = g_noalloc_slot[dev];
+    if (have_id && slot.addr != nullptr && slot.ctx_id == id) {
+        *ptr = slot.addr;
+        return QSPEC_OK;
     }
-    *ptr = g_noalloc_addr[dev];
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        set_last_error("cudaGetSymbolAddress(g_noalloc_scratch)", e);
+        return QSPEC_ERR_LAUNCH;
+    }
+    // the lookup makes the device's primary context current if none was;
+    // remember the address only when the context can be identified
+    if (current_ctx_id(&id)) {
+        slot.ctx_id = id;
+        slot.addr = p;
+    } else {
+        slot.addr = nullptr;
+    }
+    *ptr = p;
     return QSPEC_OK;
 }
 

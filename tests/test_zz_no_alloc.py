@@ -52,6 +52,24 @@ def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row():
     assert np.array_equal(n1, n3)
 
 
+def test_noalloc_one_block_per_row_path_on_dirty_scratch():
+    dev = need_gpu()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # B (2 gamma + 1) rows at or above two per SM take the one-block-per-row
+    # statistics kernel (no clearing of the scratch); run it right after calls
+    # of the chunked path, which leave their maxima and sums in the array
+    B, gamma, V = 64, 4, 32000
+    assert B * (2 * gamma + 1) >= 2 * sms
+    assert q.qspec_verify_workspace_bytes(B, gamma, V) <= q.NOALLOC_SCRATCH_BYTES
+    Ps, Qs, ds = syn.logits_noisy_draft(16, 4, 128256, 7, device=dev)
+    run_both(Ps, Qs, ds, seed=3, rnd=2, dev=dev)
+    P, Q, d = syn.logits_noisy_draft(B, gamma, V, 8, device=dev)
+    n1 = run_both(P, Q, d, seed=21, rnd=5, dev=dev)
+    run_both(Ps, Qs, ds, seed=4, rnd=3, dev=dev)
+    n2 = run_both(P, Q, d, seed=21, rnd=5, dev=dev)
+    assert np.array_equal(n1, n2)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     dev = need_gpu()
     B, gamma, V = 4096, 16, 600000
