@@ -293,6 +293,35 @@ int qspec_kv_overwrite(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_n
                        int L, int B, int H, int T, int D, int gamma, int32_t *dev_status,
                        qspec_stream_t stream);
 
+/*
+ * Diagnostic for tests of the bounded waits; the pages have no counterpart.
+ * Runs one of the library's tensor-core linear kernels on the same arguments
+ * as qspec_linear_w4a16 / qspec_linear_w4a4 would, with every barrier wait of
+ * that kernel bounded by `wait_limit` polls instead of the library's default
+ * (2^22; each poll suspends for a hardware-chosen time), and, when `stall` is
+ * non-zero, with the kernel's MMA issuer first waiting on a barrier that
+ * nothing ever arrives at, so that this wait runs out.  The kernel then leaves
+ * its loops, lets its copies and MMAs in flight finish (bounded waits of the
+ * default length), frees its tensor memory, stores QSPEC_ERR_TIMEOUT in
+ * *dev_status and returns; its outputs are unspecified.  With stall == 0 and
+ * a long enough wait_limit the outputs are those of the regular call.
+ *
+ *   kernel  QSPEC_KERNEL_W4A16_TC       the W4A16 kernel for M > 16 (any M here); reads x_bf16
+ *           QSPEC_KERNEL_W4A4_GEMV_TC   the decode-sized W4A4 kernel (3 <= M <= 16); reads xq, sx, qs
+ *           QSPEC_KERNEL_W4A4_TC        the W4A4 kernel for larger M (any M here); reads xq, sx, qs
+ *   the other pointers and sizes as in qspec_linear_w4a16 / qspec_linear_w4a4
+ *   (x_bf16 rows are K long, ldx = K).
+ * Returns QSPEC_ERR_SHAPE, before any launch, when the shape does not suit
+ * the kernel; wait_limit must be at least 1.
+ */
+#define QSPEC_KERNEL_W4A16_TC 0
+#define QSPEC_KERNEL_W4A4_GEMV_TC 1
+#define QSPEC_KERNEL_W4A4_TC 2
+int qspec_debug_linear_bounded(int kernel, const uint16_t *x_bf16, const uint8_t *xq, const float *sx,
+                               const int32_t *qs, const uint8_t *packed, const uint32_t *sz, int M, int N,
+                               int K, uint16_t *y_bf16, int ldy, uint32_t wait_limit, int stall,
+                               int32_t *dev_status, qspec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

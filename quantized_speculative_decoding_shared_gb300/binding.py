@@ -33,7 +33,8 @@ EXPORTED = ["qspec_version", "qspec_status_string", "qspec_last_cuda_error", "qs
             "qspec_quant_act_int4", "qspec_linear_w4a4", "qspec_linear_w4a4_bf16", "qspec_linear_w4a16",
             "qspec_verify_workspace_bytes", "qspec_verify_greedy", "qspec_verify_sample",
             "qspec_kv_overwrite", "qspec_verify_sample_noalloc", "qspec_draft_workspace_bytes",
-            "qspec_draft_sample"]
+            "qspec_draft_sample", "qspec_debug_linear_bounded"]
+KERNEL_W4A16_TC, KERNEL_W4A4_GEMV_TC, KERNEL_W4A4_TC = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
@@ -82,6 +83,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                             i32),
             "qspec_draft_workspace_bytes": ([i32, i32], sz_t),
             "qspec_draft_sample": ([vp, i32, i32, u64, u64, i32, vp, vp, vp, vp, sz_t, vp, vp], i32),
+            "qspec_debug_linear_bounded": ([i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, i32,
+                                            ctypes.c_uint32, i32, vp, vp], i32),
         }
         for name, (args, res) in proto.items():
             f = getattr(lib, name)
@@ -198,6 +201,16 @@ def qspec_kv_overwrite(k_cache, v_cache, k_new, v_new, base_pos, n_acc, L, B, H,
     return load_library().qspec_kv_overwrite(_ptr(k_cache), _ptr(v_cache), _ptr(k_new),
                                              _ptr(v_new), _ptr(base_pos), _ptr(n_acc), L, B, H, T,
                                              D, gamma, _ptr(dev_status), _stream(stream))
+
+
+def qspec_debug_linear_bounded(kernel, x, xq, sx, qs, packed, sz, M, N, K, y, ldy, wait_limit,
+                               stall, dev_status=None, stream=None):
+    """Test diagnostic: one tensor-core linear kernel with a chosen bound on
+    its barrier waits (and, with stall, a wait made to run out)."""
+    return load_library().qspec_debug_linear_bounded(kernel, _ptr(x), _ptr(xq), _ptr(sx), _ptr(qs),
+                                                     _ptr(packed), _ptr(sz), M, N, K, _ptr(y), ldy,
+                                                     ctypes.c_uint32(wait_limit), stall,
+                                                     _ptr(dev_status), _stream(stream))
 
 
 # ---------------------------------------------------------------------------

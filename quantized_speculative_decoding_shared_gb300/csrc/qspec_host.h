@@ -40,25 +40,36 @@ int launch_w4a4_dp4a(const uint8_t *xq, const float *sx, const int32_t *qs, cons
                      float *sx_out, int32_t *qs_out, const uint8_t *packed, const uint32_t *sz, int N, int K,
                      uint16_t *y, int32_t *dbg_I, int32_t *dev_status, cudaStream_t stream);
 
+// The tensor-core kernels below bound every barrier wait by wait_limit polls
+// (kWaitLimit in the regular calls); stall != 0 (tests only) makes the MMA
+// issuer first wait on a barrier nothing arrives at, so that the wait runs
+// out and the kernel takes its timeout exit.
+
 // Large-M W4A16 on the tensor cores (w4a16_tc.cu).
 int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
-                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream);
+                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall);
 
 // Larger-M W4A4 on the tensor cores (w4a4_tc.cu).
 int launch_w4a4_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                    const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st,
-                   cudaStream_t stream);
+                   cudaStream_t stream, uint32_t wait_limit, int stall);
 
 // Decode-sized W4A4 (3 <= M <= 16) on the tensor cores with the weights
 // staged in TMEM (w4a4_gemv_tc.cu); QSPEC_ERR_SHAPE before any launch when
 // the shape does not suit it.
 int launch_w4a4_gemv_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                         const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I,
-                        int32_t *dev_status, cudaStream_t stream);
+                        int32_t *dev_status, cudaStream_t stream, uint32_t wait_limit, int stall);
 
 // 2-D TMA map over a packed weight matrix [N][K / 2] bytes: boxes of 128
 // bytes x box_rows rows, 128-byte swizzle, rows past N read as zeros.
 int weight_tmap(CUtensorMap *out, const uint8_t *packed, int N, int K, int box_rows);
+
+// Polls of a bounded barrier wait in the tensor-core kernels (each poll
+// suspends for a hardware-chosen time); a wait that runs out sets
+// QSPEC_ERR_TIMEOUT.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
 
 // Launch `kernel` on `st` with programmatic stream serialisation allowed (the
 // kernel must follow the pdl_wait() rule in qspec_device.cuh).

@@ -362,5 +362,5 @@ extern "C" int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t
             }
         }
     }
-    return launch_w4a16_tc(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, dev_status, st);
+    return launch_w4a16_tc(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, dev_status, st, kWaitLimit, 0);
 }

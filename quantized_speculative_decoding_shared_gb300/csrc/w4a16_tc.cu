@@ -27,7 +27,13 @@
 // CTAs splits a tile's groups; each CTA keeps its fp32 partial sums, and
 // rank 0 reads its peers' partials from distributed shared memory, adds them
 // in rank order and stores bf16.
-// Bounded waits everywhere (QSPEC_ERR_TIMEOUT on expiry, then clean exit).
+// Bounded waits everywhere (the limit is a kernel argument; a test can also
+// make the MMA issuer wait on a barrier nothing arrives at).  After a
+// timeout (QSPEC_ERR_TIMEOUT) every role leaves its loop, the MMAs issued are
+// drained with a bounded wait, and the tensor memory is freed -- even if the
+// drain itself ran out (the next kernel on the SM would otherwise wait for it
+// without bound); in that case the split-K reduction, which reuses the
+// operand stages the MMAs read, is skipped.
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -78,15 +84,17 @@ struct Smem {
     uint8_t b[kStages][BN * kKB];
     uint64_t full[kStages], empty[kStages], accf[2], acce[2];
     uint64_t drain;                    // after a timeout: the MMAs in flight have finished
+    uint64_t never;                    // nothing arrives here (the stall test)
     uint32_t tmem;
     int timeout;
+    int drained;                       // 0 after a drain that ran out
 };
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_umma_kernel(const uint16_t *__restrict__ x, int ldx, const uint8_t *__restrict__ packed,
                       const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
-                      int32_t *st, int C) {
+                      int32_t *st, int C, uint32_t wait_limit, int stall) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem<BN> &sm = *reinterpret_cast<Smem<BN> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -110,7 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&sm.acce[b], kEpilogue);
         }
         umma::mbar_init(&sm.drain, 1);
+        umma::mbar_init(&sm.never, 1);
         sm.timeout = 0;
+        sm.drained = 1;
         umma::mbar_fence_init();
     }
     pdl_launch_dependents();
@@ -118,6 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem;
+    bool issued = false;                          // MMAs issued (MMA lane 0)
+    auto timed_out = [&]() { return *reinterpret_cast<volatile int *>(&sm.timeout) != 0; };
     // epilogue partial sums: per thread (row n, token half) BN / 2 values
     constexpr int kHalf = BN / 2;
     uint64_t acc[kHalf / 2];
@@ -151,7 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int l = lb + p, g = g_lo + l;
                 if (l >= NG) break;
                 const int s = l % kStages;
-                if (l >= kStages && !umma::mbar_wait(&sm.empty[s], ((l / kStages) - 1) & 1)) {
+                if (l >= kStages &&
+                    (timed_out() || !umma::mbar_wait(&sm.empty[s], ((l / kStages) - 1) & 1, wait_limit))) {
                     atomicExch(&sm.timeout, 1);
                     ok = false;
                     break;
@@ -220,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok && l + 1 < NG) szn = __ldg(sz + (size_t)n * G + g_lo + l + 1);
             const float sn = __half2float(__ushort_as_half((uint16_t)(szw & 0xFFFF)));
             const uint64_t s2 = f2(sn, sn);
-            if (!umma::mbar_wait(&sm.accf[buf], (l >> 1) & 1)) {
+            if (timed_out() || !umma::mbar_wait(&sm.accf[buf], (l >> 1) & 1, wait_limit)) {
                 atomicExch(&sm.timeout, 1);
                 ok = false;
                 break;
@@ -257,10 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         if (lane == 0) {
             constexpr uint32_t idesc = umma::instr_desc(1, 1, kTileN, BN);
+            if (stall && !umma::mbar_wait(&sm.never, 0, wait_limit)) atomicExch(&sm.timeout, 1);
             for (int l = 0; l < NG; ++l) {
                 const int s = l % kStages, buf = l & 1;
-                if (!umma::mbar_wait(&sm.full[s], (l / kStages) & 1) ||
-                    (l >= 2 && !umma::mbar_wait(&sm.acce[buf], ((l >> 1) - 1) & 1))) {
+                if (timed_out() || !umma::mbar_wait(&sm.full[s], (l / kStages) & 1, wait_limit) ||
+                    (l >= 2 && !umma::mbar_wait(&sm.acce[buf], ((l >> 1) - 1) & 1, wait_limit))) {
                     atomicExch(&sm.timeout, 1);
                     break;
                 }
@@ -275,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma::mma_commit(&sm.empty[s]);
                 umma::mma_commit(&sm.accf[buf]);
+                issued = true;
             }
         }
         __syncwarp();
@@ -284,9 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // after a timeout, the MMAs already issued finish (bounded wait) before
     // the TMEM they write is freed; sm.timeout is settled at this barrier
     if (sm.timeout) {
-        if (warp == kThreads / 32 - 1 && lane == 0) {
+        if (warp == kThreads / 32 - 1 && lane == 0 && issued) {
             umma::mma_commit(&sm.drain);
-            umma::mbar_wait(&sm.drain, 0);
+            if (!umma::mbar_wait(&sm.drain, 0, kWaitLimit)) sm.drained = 0;
         }
         __syncthreads();
     }
@@ -296,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rank order and stores bf16
         float *red = reinterpret_cast<float *>(smem_raw);          // [BN tokens][128 channels]
         const int eq = warp & 3, eh = (warp - 4) >> 2, row = eq * 32 + lane;
-        if (warp >= 4 && warp < 12) {
+        const bool reuse = sm.drained != 0;                        // the operand stages are free
+        if (warp >= 4 && warp < 12 && reuse) {
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {
                 const int t = eh * kHalf + 2 * i;
@@ -305,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         umma::cluster_sync();
-        if (rank == 0 && warp >= 4 && warp < 12) {
+        if (rank == 0 && warp >= 4 && warp < 12 && reuse && !sm.timeout) {
             const int n = n0 + row;
             if (n < N) {
                 for (int t = eh * kHalf; t < eh * kHalf + kHalf; ++t) {
@@ -325,8 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN>
 int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
-              uint16_t *y, int ldy, int32_t *st, cudaStream_t stream) {
-    static_assert(sizeof(float) * BN * kTileN <= sizeof(Smem<BN>), "partials fit in the operand stages");
+              uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall) {
+    static_assert(sizeof(float) * BN * kTileN <= sizeof(Smem<BN>::a) + sizeof(Smem<BN>::b),
+                  "partials fit in the operand stages");
     const size_t smem = sizeof(Smem<BN>) + 1024;
     int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a16_umma_kernel<BN>), (int)smem);
     if (rc) return rc;
@@ -338,20 +355,20 @@ int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t 
     dim3 grid((unsigned)(n_tiles * C), (unsigned)token_tiles);
     if (C == 1)
         return launch_pdl("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, x, ldx,
-                          packed, sz, M, N, K, y, ldy, st, C);
+                          packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall);
     return launch_pdl_cluster("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, C, x,
-                              ldx, packed, sz, M, N, K, y, ldy, st, C);
+                              ldx, packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall);
 }
 
 }  // namespace
 
 // Large-M W4A16: token tile 32, 64, 96 or 128 (larger M: several token tiles).
 int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
-                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream) {
-    if (M <= 32) return launch_bn<32>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream);
-    if (M <= 64) return launch_bn<64>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream);
-    if (M <= 96) return launch_bn<96>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream);
-    return launch_bn<128>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream);
+                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall) {
+    if (M <= 32) return launch_bn<32>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall);
+    if (M <= 64) return launch_bn<64>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall);
+    if (M <= 96) return launch_bn<96>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall);
+    return launch_bn<128>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall);
 }
 
 }  // namespace qspec

@@ -471,7 +471,7 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
     int rc = check_device();
     if (rc) return rc;
     cudaStream_t st = as_cuda(stream);
-    if (M > 32) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
+    if (M > 32) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st, kWaitLimit, 0);
     if (M == 1) {
         rc = launch_w4a4_dp4a(xq, sx, qs, nullptr, nullptr, nullptr, nullptr, packed, sz, N, K, y_bf16, dbg_I,
                               dev_status, st);
@@ -480,10 +480,10 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
     // 3..16 tokens and at least one 128-row tile per SM: weights through TMA
     // and TMEM, MMAs async (at 1-2 tokens the warp-MMA kernel below is faster)
     if (hm::use_gemv_tc(M, N)) {
-        rc = launch_w4a4_gemv_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
+        rc = launch_w4a4_gemv_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st, kWaitLimit, 0);
         if (rc != QSPEC_ERR_SHAPE) return rc;
     }
-    if (hm::use_tc(M, K)) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
+    if (hm::use_tc(M, K)) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st, kWaitLimit, 0);
     const hm::Act act = {xq, sx, qs, nullptr, 0, nullptr, nullptr, nullptr};
     return hm::launch_small(act, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
 }

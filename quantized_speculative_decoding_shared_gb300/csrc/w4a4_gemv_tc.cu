@@ -29,9 +29,13 @@
 //     accumulators in group order, so no cross-thread reduction exists.
 // Group pairs cycle through kPSlots TMEM slots (A 64 columns + D 32 columns
 // each); one barrier round per pair.
-// Every wait is bounded; after a timeout (QSPEC_ERR_TIMEOUT) later waits are
-// skipped, the copies and MMAs in flight are drained with bounded waits, and
-// the kernel ends.
+// Every wait is bounded (the limit is a kernel argument; a test can also
+// make the MMA issuer wait on a barrier nothing arrives at).  After a timeout
+// (QSPEC_ERR_TIMEOUT) every role leaves its loop -- the producer and the MMA
+// issuer issue nothing more -- the copies in flight and the MMAs issued are
+// drained with bounded waits, and the kernel ends.  Should even the drain run
+// out, the tensor memory is freed all the same: the next kernel on the SM
+// would otherwise wait for it without a bound.
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -89,7 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     w4a4_gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__restrict__ xq,
                         const float *__restrict__ sx, const int32_t *__restrict__ qs,
                         const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
-                        int32_t *__restrict__ dbg_I, int32_t *__restrict__ st, int S) {
+                        int32_t *__restrict__ dbg_I, int32_t *__restrict__ st, int S, uint32_t wait_limit,
+                        int stall) {
     static_assert(MT == 1 || MT == 2 || MT == 4 || MT == 8 || MT == 16, "token columns per CTA");
     constexpr uint32_t kTokBytes = (uint32_t)token_group_bytes(MT);
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -103,6 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = bars + 2 * S, *done = full + kPSlots, *freed = done + kPSlots;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(freed + kPSlots);
     __shared__ int timeout_flag;
+    __shared__ uint64_t never;                 // nothing arrives here (the stall test)
+    __shared__ uint64_t drain_bar;             // the MMAs issued have completed
     volatile int *timeout = &timeout_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -111,8 +118,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_tiles = (N + 127) / 128;
     const int my_tiles = (int)blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int n_pairs = my_tiles * P;          // one box, one TMEM pair slot each
-    auto wait = [&](uint64_t *bar, uint32_t parity) {
-        if (!*timeout && !umma::mbar_wait(bar, parity)) *timeout = 1;
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (*timeout) return false;
+        if (umma::mbar_wait(bar, parity, wait_limit)) return true;
+        *timeout = 1;
+        return false;
     };
 
     if (threadIdx.x == 0) {
@@ -126,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&done[s], 1);
             umma::mbar_init(&freed[s], kEpiWarps);
         }
+        umma::mbar_init(&never, 1);
+        umma::mbar_init(&drain_bar, 1);
         umma::mbar_fence_init();
     }
     if (warp == kMmaWarp) umma::tmem_alloc(tmem_slot, kTmemCols);
@@ -137,9 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // producer cursor over boxes (tile step, group pair)
     int pb = 0, pstep = 0, ppair = 0;
-    auto issue_box = [&]() {
+    auto issue_box = [&]() -> bool {
         const int slot = pb % S;
-        if (pb >= S) wait(&st_empty[slot], (uint32_t)(((pb / S) + 1) & 1));
+        if (pb >= S && !wait(&st_empty[slot], (uint32_t)(((pb / S) + 1) & 1))) return false;
         umma::mbar_arrive_expect_tx(&st_full[slot], kStageBytes);
         umma::tma_load_2d(stages + (size_t)slot * kStageBytes, &tmap, ppair * 128,
                           (blockIdx.x + pstep * gridDim.x) * 128, &st_full[slot]);
@@ -148,10 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ppair = 0;
             ++pstep;
         }
+        return true;
     };
     // the first boxes before the dependency wait: weights are immutable
     if (warp == kProducerWarp && lane == 0)
-        while (pb < n_pairs && pb < S) issue_box();
+        while (pb < n_pairs && pb < S)
+            if (!issue_box()) break;
     pdl_wait();
 
     // token operand: zero rows, then the real tokens' words
@@ -180,20 +194,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tbase = *tmem_slot;
+    int issued = 0;                            // pairs whose MMAs were issued (MMA lane 0)
 
     if (warp == kProducerWarp) {
         // ---- TMA producer ----
         if (lane == 0)
-            while (pb < n_pairs) issue_box();
+            while (pb < n_pairs)
+                if (!issue_box()) break;
     } else if (warp == kMmaWarp) {
         // ---- MMA issuer: per pair, 4 MMAs per group present ----
         if (lane == 0) {
             constexpr uint32_t idesc = umma::instr_desc(0, 0, 128, 16);
             const uint32_t b0 = umma::smem_addr(bsm);
+            if (stall) wait(&never, 0);
             int pp = 0;
             for (int p = 0; p < n_pairs; ++p) {
                 const int s = p % kPSlots;
-                wait(&full[s], (uint32_t)((p / kPSlots) & 1));
+                if (!wait(&full[s], (uint32_t)((p / kPSlots) & 1))) break;
                 umma::fence_after_sync();
                 const int ng = 2 * pp + 1 < G ? 2 : 1;
                 for (int gi = 0; gi < ng; ++gi) {
@@ -207,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           umma::smem_desc(bg + kk * 256, 128, kSbo), idesc, kk > 0 ? 1u : 0u);
                 }
                 umma::mma_commit(&done[s]);
+                ++issued;
                 if (++pp == P) pp = 0;
             }
         }
@@ -218,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pp = 0;
         for (int p = 0; p < n_pairs; ++p) {
             const int slot = p % S, s = p % kPSlots;
-            wait(&st_full[slot], (uint32_t)((p / S) & 1));
-            if (p >= kPSlots) wait(&freed[s], (uint32_t)(((p / kPSlots) + 1) & 1));
+            if (!wait(&st_full[slot], (uint32_t)((p / S) & 1))) break;
+            if (p >= kPSlots && !wait(&freed[s], (uint32_t)(((p / kPSlots) + 1) & 1))) break;
             umma::fence_after_sync();
             const uint8_t *stg = stages + (size_t)slot * kStageBytes;
             const int ng = 2 * pp + 1 < G ? 2 : 1;
@@ -269,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = 0; p < n_pairs; ++p) {
             const int s = p % kPSlots;
             const int ng = 2 * pp + 1 < G ? 2 : 1;
-            wait(&done[s], (uint32_t)((p / kPSlots) & 1));
+            if (!wait(&done[s], (uint32_t)((p / kPSlots) & 1))) break;
             umma::fence_after_sync();
             const uint32_t zw[2] = {za, zb};
             if (p + 1 < n_pairs) zload(za, zb);
@@ -313,14 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // after a timeout: let this CTA's copies and MMAs in flight finish (bounded)
-    // before the shared and tensor memory are released
+    // before the shared and tensor memory are released.  The producer stopped
+    // issuing at the timeout, so at most S boxes are in flight, one per
+    // stage; the MMA issuer's last commit covers all its MMAs.
     __syncthreads();
     if (*timeout) {
         if (warp == kProducerWarp && lane == 0)
-            for (int b = max(0, pb - S); b < pb; ++b) umma::mbar_wait(&st_full[b % S], (uint32_t)((b / S) & 1));
-        if (warp == kMmaWarp && lane == 0)
-            for (int p = max(0, n_pairs - kPSlots); p < n_pairs; ++p)
-                umma::mbar_wait(&done[p % kPSlots], (uint32_t)((p / kPSlots) & 1));
+            for (int b = max(0, pb - S); b < pb; ++b)
+                umma::mbar_wait(&st_full[b % S], (uint32_t)((b / S) & 1), kWaitLimit);
+        if (warp == kMmaWarp && lane == 0 && issued > 0) {
+            umma::mma_commit(&drain_bar);
+            umma::mbar_wait(&drain_bar, 0, kWaitLimit);
+        }
     }
     umma::fence_before_sync();
     __syncthreads();
@@ -330,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MT>
 int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed, const uint32_t *sz, int M,
-           int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *dev_status, cudaStream_t stream) {
+           int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *dev_status, cudaStream_t stream,
+           uint32_t wait_limit, int stall) {
     constexpr size_t kBudget = 220 * 1024;
     const int G = K / kGroup;
     const size_t tail = tail_bytes(MT, G, kMaxStages);
@@ -346,7 +369,7 @@ int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t 
     const int per_col = std::max(1, sm_count() / token_tiles);
     dim3 grid((unsigned)std::min(n_tiles, per_col), (unsigned)token_tiles);
     return launch_pdl("qspec_linear_w4a4", kern, grid, dim3(kThreads), smem_bytes(MT, K, S), stream, tmap, xq, sx,
-                      qs, sz, M, N, K, y, ldy, dbg_I, dev_status, S);
+                      qs, sz, M, N, K, y, ldy, dbg_I, dev_status, S, wait_limit, stall);
 }
 
 }  // namespace tg
@@ -357,12 +380,14 @@ int launch(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t 
 // QSPEC_ERR_SHAPE before any launch when the shape does not suit the kernel.
 int launch_w4a4_gemv_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                         const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I,
-                        int32_t *dev_status, cudaStream_t stream) {
+                        int32_t *dev_status, cudaStream_t stream, uint32_t wait_limit, int stall) {
     // 3..16 tokens (one and two tokens have their own kernels)
     if (M < 3 || M > 16) return QSPEC_ERR_SHAPE;
-    if (M <= 4) return tg::launch<4>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
-    if (M <= 8) return tg::launch<8>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
-    return tg::launch<16>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream);
+    if (M <= 4)
+        return tg::launch<4>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream, wait_limit, stall);
+    if (M <= 8)
+        return tg::launch<8>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream, wait_limit, stall);
+    return tg::launch<16>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, dev_status, stream, wait_limit, stall);
 }
 
 }  // namespace qspec

@@ -25,7 +25,13 @@
 //              of the token columns: per group, TMEM -> registers, I and the
 //              ordered fp32 fold in registers (packed f32x2); finally bf16
 //   warp 12    issues the MMAs into one of two TMEM accumulators per group
-// Bounded waits everywhere (QSPEC_ERR_TIMEOUT on expiry, then clean exit).
+// Bounded waits everywhere (the limit is a kernel argument; a test can also
+// make the MMA issuer wait on a barrier nothing arrives at).  After a
+// timeout (QSPEC_ERR_TIMEOUT) every role leaves its loop -- the epilogue
+// warpgroups together, through a barrier that ORs their failure flags, since
+// they also meet at a named barrier -- the MMAs issued are drained with a
+// bounded wait, and the tensor memory is freed (even if the drain itself ran
+// out: the next kernel on the SM would otherwise wait for it without bound).
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -100,6 +106,7 @@ struct Smem {
     float enqs[2][BN];                 // -qs as float (exact)
     uint64_t full[kStages], empty[kStages], accf[2], acce[2];
     uint64_t drain;                    // after a timeout: the MMAs in flight have finished
+    uint64_t never;                    // nothing arrives here (the stall test)
     uint32_t tmem;
     int timeout;
 };
@@ -108,7 +115,8 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a4_umma_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx, const int32_t *__restrict__ qs,
                      const uint8_t *__restrict__ packed, const uint32_t *__restrict__ sz, int M, int N, int K,
-                     uint16_t *__restrict__ y, int ldy, int32_t *__restrict__ dbg_I, int32_t *st) {
+                     uint16_t *__restrict__ y, int ldy, int32_t *__restrict__ dbg_I, int32_t *st,
+                     uint32_t wait_limit, int stall) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem<BN> &sm = *reinterpret_cast<Smem<BN> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -128,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&sm.acce[b], kEpilogue);
         }
         umma::mbar_init(&sm.drain, 1);
+        umma::mbar_init(&sm.never, 1);
         sm.timeout = 0;
         umma::mbar_fence_init();
     }
@@ -136,6 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem;
+    bool issued = false;                          // MMAs issued (MMA lane 0)
+    auto timed_out = [&]() { return *reinterpret_cast<volatile int *>(&sm.timeout) != 0; };
 
     if (warp < 4) {
         // ------------------------------------------------------------ producers
@@ -148,7 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         for (int g = 0; g < G; ++g) {
             const int s = g % kStages;
-            if (g >= kStages && !umma::mbar_wait(&sm.empty[s], ((g / kStages) - 1) & 1)) {
+            if (g >= kStages &&
+                (timed_out() || !umma::mbar_wait(&sm.empty[s], ((g / kStages) - 1) & 1, wait_limit))) {
                 atomicExch(&sm.timeout, 1);
                 break;
             }
@@ -196,21 +208,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kHalf / 2; ++i) acc[i] = 0;
         bool ok = true;
-        for (int g = 0; g < G && ok; ++g) {
+        for (int g = 0; g < G; ++g) {
             const int buf = g & 1;
             // the group's token scales into the epilogue's own double buffer; the
             // barrier also orders this write after every epilogue thread's reads
-            // of the same buffer two groups ago
+            // of the same buffer two groups ago, and tells every epilogue thread
+            // whether any of them has given up (all leave together)
             for (int t = et; t < BN; t += kEpilogue) {
                 const int m = t0 + t;
                 sm.esx[buf][t] = m < M ? sx[(size_t)m * G + g] : 0.0f;
                 sm.enqs[buf][t] = m < M ? -(float)qs[(size_t)m * G + g] : 0.0f;
             }
-            asm volatile("bar.sync 1, %0;\n" ::"r"(kEpilogue) : "memory");
-            if (!umma::mbar_wait(&sm.accf[buf], (g >> 1) & 1)) {
+            uint32_t any_failed;
+            asm volatile(
+                "{.reg .pred p, q; setp.eq.u32 p, %1, 0; bar.red.or.pred q, 1, %2, p; selp.u32 %0, 1, 0, q;}\n"
+                : "=r"(any_failed)
+                : "r"(ok ? 1u : 0u), "r"(kEpilogue)
+                : "memory");
+            if (any_failed) break;
+            if (timed_out() || !umma::mbar_wait(&sm.accf[buf], (g >> 1) & 1, wait_limit)) {
                 atomicExch(&sm.timeout, 1);
                 ok = false;
-                break;
+                continue;                             // to the barrier, where all leave
             }
             umma::fence_after_sync();
             const uint32_t szw = row_ok ? __ldg(sz + (size_t)n * G + g) : 0u;
@@ -260,10 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         if (lane == 0) {
             constexpr uint32_t idesc = umma::instr_desc(0, 0, kTileN, BN);
+            if (stall && !umma::mbar_wait(&sm.never, 0, wait_limit)) atomicExch(&sm.timeout, 1);
             for (int g = 0; g < G; ++g) {
                 const int s = g % kStages, buf = g & 1;
-                if (!umma::mbar_wait(&sm.full[s], (g / kStages) & 1) ||
-                    (g >= 2 && !umma::mbar_wait(&sm.acce[buf], ((g >> 1) - 1) & 1))) {
+                if (timed_out() || !umma::mbar_wait(&sm.full[s], (g / kStages) & 1, wait_limit) ||
+                    (g >= 2 && !umma::mbar_wait(&sm.acce[buf], ((g >> 1) - 1) & 1, wait_limit))) {
                     atomicExch(&sm.timeout, 1);
                     break;
                 }
@@ -278,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma::mma_commit(&sm.empty[s]);
                 umma::mma_commit(&sm.accf[buf]);
+                issued = true;
             }
         }
         __syncwarp();
@@ -287,9 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // after a timeout, the MMAs already issued finish (bounded wait) before
     // the TMEM they write is freed; sm.timeout is settled at this barrier
     if (sm.timeout) {
-        if (warp == kThreads / 32 - 1 && lane == 0) {
+        if (warp == kThreads / 32 - 1 && lane == 0 && issued) {
             umma::mma_commit(&sm.drain);
-            umma::mbar_wait(&sm.drain, 0);
+            umma::mbar_wait(&sm.drain, 0, kWaitLimit);
         }
         __syncthreads();
     }
@@ -299,13 +320,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN>
 int launch_bn(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed, const uint32_t *sz,
-              int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st, cudaStream_t stream) {
+              int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st, cudaStream_t stream,
+              uint32_t wait_limit, int stall) {
     const size_t smem = sizeof(Smem<BN>) + 1024;
     int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN>), (int)smem);
     if (rc) return rc;
     dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + BN - 1) / BN));
     return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, xq, sx, qs,
-                      packed, sz, M, N, K, y, ldy, dbg_I, st);
+                      packed, sz, M, N, K, y, ldy, dbg_I, st, wait_limit, stall);
 }
 
 }  // namespace
@@ -313,10 +335,10 @@ int launch_bn(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8
 // Larger-M W4A4 on the tensor cores: token tile of 32, 64 or 128.
 int launch_w4a4_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                    const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st,
-                   cudaStream_t stream) {
-    if (M <= 32) return launch_bn<32>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream);
-    if (M <= 64) return launch_bn<64>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream);
-    return launch_bn<128>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream);
+                   cudaStream_t stream, uint32_t wait_limit, int stall) {
+    if (M <= 32) return launch_bn<32>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+    if (M <= 64) return launch_bn<64>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+    return launch_bn<128>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
 }
 
 }  // namespace qspec

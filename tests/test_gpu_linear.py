@@ -301,3 +301,36 @@ def test_w4a16_one_token_tile(M, N, K, seed):
     y16 = q.linear_w4a16(x.to(dev), packed, sz)
     ref = oracle.linear_w4a16(bits(x), po, szo)
     assert_w4a16_close(y16, ref, "w4a16 M=%d N=%d K=%d" % (M, N, K))
+
+
+# ----------------------------------------------------------------- W4A16, decode shapes (M <= 16)
+# The Llama-3-8B decode linears at the verify shape M = 5 (and 8, 13, 16
+# tokens), plus ragged tiles, few groups and many row tiles.
+@pytest.mark.parametrize("M,N,K,seed", [
+    (5, 6144, 4096, 70),     # Llama q/k/v stacked
+    (8, 4096, 4096, 71),     # o
+    (5, 4096, 14336, 72),    # down
+    (13, 4096, 14336, 73),
+    (5, 25600, 2048, 74),
+    (16, 300, 1152, 75),
+    (9, 130, 3072, 76),
+    (1, 777, 384, 77),
+    (7, 129, 128, 78),
+    (2, 19533, 1152, 79),
+    (11, 1000, 4096, 80),
+])
+def test_w4a16_decode_shapes(M, N, K, seed):
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100, outlier_frac=0.01)
+    st = status(dev)
+    y16 = q.linear_w4a16(x.to(dev), packed, sz, dev_status=st)
+    assert read_status(st) == 0
+    ref = oracle.linear_w4a16(bits(x), po, szo)
+    assert_w4a16_close(y16, ref, "w4a16 M=%d N=%d K=%d" % (M, N, K))
+
+
+def test_w4a16_lm_head_m5():
+    """The 128256 x 4096 LM head at M = gamma + 1 = 5."""
+    dev = need_gpu()
+    sampled_compare([5], [("lm_head", 128256, 4096)], 9, dev, outliers=0.01, w4a4=False, points=1024)
