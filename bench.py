@@ -52,6 +52,15 @@ from quantized_speculative_decoding_shared_gb300 import synthetic as syn  # noqa
 
 GROUP = 128
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# dense tcgen05 kind::f8f6f4 (E4M3) rate measured on this GPU with a
+# shared-memory-operand MMA loop (M = 128, N = 256, K = 32, one CTA per SM,
+# CUDA events): 128 cycles per MMA, 4821.8 TFLOP/s
+E4M3_PROBE_TFLOPS = 4821.8
+
+# draft-logit noise of the Qwen2.5-7B workloads: mean acceptance 0.60 per
+# draft position on the oracle (tests/golden/calibrate_q_noise.py)
+QWEN_Q_NOISE = json.load(open(os.path.join(ROOT, "tests", "golden", "qwen_q_noise.json")))["q_noise"]
 
 WORKLOADS = {
     # Llama-3-8B decode at batch 1: W4A4 draft at M = 1, W4A16 verify at M = 5
@@ -63,11 +72,11 @@ WORKLOADS = {
                              T=4096, p_std=3.0, q_noise=0.5, seed=2),
     # Qwen2.5-7B at batch 32, gamma 2 / 4 / 8 (W4A4 at M = 32, W4A16 at M = 96 / 160 / 288)
     "qwen2.5-7b-b32-g2": dict(shape=syn.QWEN25_7B, B=32, gamma=2, outliers=0.0,
-                              T=4096, p_std=3.0, q_noise=0.5, seed=3),
+                              T=4096, p_std=3.0, q_noise=QWEN_Q_NOISE, seed=3),
     "qwen2.5-7b-b32-g4": dict(shape=syn.QWEN25_7B, B=32, gamma=4, outliers=0.0,
-                              T=4096, p_std=3.0, q_noise=0.5, seed=3),
+                              T=4096, p_std=3.0, q_noise=QWEN_Q_NOISE, seed=3),
     "qwen2.5-7b-b32-g8": dict(shape=syn.QWEN25_7B, B=32, gamma=8, outliers=0.0,
-                              T=4096, p_std=3.0, q_noise=0.5, seed=3),
+                              T=4096, p_std=3.0, q_noise=QWEN_Q_NOISE, seed=3),
 }
 PREFILL = "llama3-8b-prefill-m4096"
 
@@ -158,6 +167,14 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def _code_only(text):
@@ -472,6 +489,94 @@ def row_kernels(dev, stream, reps=5, calls=10):
     rec("a7_kv_overwrite", lambda: q.qspec_kv_overwrite(kc, vc, kn, vn, base, na, L, B, H, T, D, g),
         2 * 2 * 2 * L * B * (g + 1) * H * D, "32 layers x 16 seq x 8 heads x 4096 x 128, all 4 drafts accepted")
     del kc, vc, kn, vn
+    torch.cuda.synchronize()
+    return out
+
+
+def targets(rnd_obj, dev, stream, reps=5):
+    """The two explicit performance targets, measured in the same run:
+    W4A16 verify linears at M <= 64 (and 80) against HBM, the W4A4 draft
+    linears at decode M against HBM, and the W4A4 prefill GEMM at M = 4096
+    against the E4M3 tensor peak.  The linears are one Llama-3-8B layer's
+    (q/k/v, o, gate/up, down) plus the LM head, 390 MB of packed weights, so
+    every replay streams from HBM (larger than L2); CUDA-graph replays of one
+    call per linear, CUDA events on the launching stream."""
+    from quantized_speculative_decoding_shared_gb300 import binding as q
+    peak, kind = measured_peaks()
+    linears = [(name, N, K, rnd_obj.w[0][name]) for name, N, K in rnd_obj.linears]
+    linears.append(("lm_head", rnd_obj.V, rnd_obj.hidden, rnd_obj.lm))
+    out = {"peak_hbm_GBs": peak, "peak_source": kind,
+           "shapes": "Llama-3-8B layer (qkv 4096->6144, o 4096->4096, gate/up 4096->28672, down 14336->4096) "
+                     "+ LM head 4096->128256"}
+
+    def run(fn_list, nbytes):
+        for f in fn_list:
+            f()
+        torch.cuda.synchronize()
+
+        def all_calls():
+            for f in fn_list:
+                f()
+        g = capture(all_calls, stream)
+        t = time_graph(g, reps, stream)
+        del g
+        return t, nbytes / (t / 1e3) / 1e9
+
+    w16 = {}
+    for M in (5, 16, 32, 64, 80):
+        fns, nbytes = [], 0
+        for j, (name, N, K, pk) in enumerate(linears):
+            x = syn.activations(M, K, 200 + j, device=dev, outlier_frac=0.01)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fns.append(lambda x=x, y=y, pk=pk, N=N, K=K, M=M: q.qspec_linear_w4a16(x, K, pk[0], pk[1], M, N, K,
+                                                                                   y, N))
+            nbytes += bytes_w4a16(M, N, K)
+        t, gbs = run(fns, nbytes)
+        w16["M%d" % M] = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)}
+    out["w4a16_verify"] = dict(w16, target="frac_hbm >= 0.70 for M <= 64")
+    w4 = {}
+    for M in (1, 16, 32):
+        fns, nbytes = [], 0
+        for j, (name, N, K, pk) in enumerate(linears):
+            x = syn.activations(M, K, 300 + j, device=dev, outlier_frac=0.01)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            xq = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+            sx = torch.empty((M, K // GROUP), dtype=torch.float32, device=dev)
+            qs = torch.empty((M, K // GROUP), dtype=torch.int32, device=dev)
+            fns.append(lambda x=x, y=y, pk=pk, N=N, K=K, M=M, xq=xq, sx=sx, qs=qs:
+                       q.qspec_linear_w4a4_bf16(x, K, pk[0], pk[1], M, N, K, y, N, xq, sx, qs))
+            nbytes += bytes_w4a4_bf16(M, N, K)
+        t, gbs = run(fns, nbytes)
+        w4["M%d" % M] = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)}
+    out["w4a4_draft"] = w4
+    # prefill: M = 4096 through gate/up and down
+    M = 4096
+    bf16, bkind = measured_bf16_tflops()
+    e4m3 = 2.0 * bf16
+    fns4, fns16, flops = [], [], 0
+    for j, (name, N, K, pk) in enumerate(linears):
+        if name not in ("gate_up_proj", "down_proj"):
+            continue
+        x = syn.activations(M, K, 400 + j, device=dev)
+        xq, sx, qs = q.quant_act_int4(x)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fns4.append(lambda xq=xq, sx=sx, qs=qs, pk=pk, y=y, N=N, K=K:
+                    q.qspec_linear_w4a4(xq, sx, qs, pk[0], pk[1], M, N, K, y, N))
+        fns16.append(lambda x=x, pk=pk, y=y, N=N, K=K: q.qspec_linear_w4a16(x, K, pk[0], pk[1], M, N, K, y, N))
+        flops += 2 * M * N * K
+    t4, _ = run(fns4, 0)
+    t16, _ = run(fns16, 0)
+    tops = flops / (t4 / 1e3) / 1e12
+    tf16 = flops / (t16 / 1e3) / 1e12
+    out["w4a4_prefill_m4096"] = {
+        "ms": round(t4, 4), "TOPS": round(tops, 1),
+        "peak_e4m3_TFLOPs": round(e4m3, 1),
+        "peak_source": "%s bf16 dense burst x 2 (the nominal e4m3 / bf16 ratio)" % bkind,
+        "frac": round(tops / e4m3, 4),
+        "frac_of_e4m3_probe": round(tops / E4M3_PROBE_TFLOPS, 4),
+        "target": "frac >= 0.50"}
+    out["w4a16_prefill_m4096"] = {"ms": round(t16, 4), "TFLOPs": round(tf16, 1), "peak_bf16_TFLOPs": bf16,
+                                  "frac": round(tf16 / bf16, 4)}
     torch.cuda.synchronize()
     return out
 
@@ -805,6 +910,7 @@ def main():
                                                  "ms_per_verify_pass": round(t16, 4),
                                                  "M": wl["B"] * (wl["gamma"] + 1)}},
             "rows": row_kernels(dev, stream),
+            "targets": targets(rnd_obj, dev, stream),
             "gpu_launches": rnd_obj.launches_per_round() * args.steps,
             "clocks": clk}
     if world == 1 and not args.no_cpu_baseline:
