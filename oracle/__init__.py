@@ -107,6 +107,18 @@ def _load():
         lib.orc_kv_overwrite.restype = I
         lib.orc_num_threads.argtypes = []
         lib.orc_num_threads.restype = I
+        lib.orc_e4m3_value.argtypes = [u8]
+        lib.orc_e4m3_value.restype = f64
+        lib.orc_e4m3_from_float.argtypes = [f32]
+        lib.orc_e4m3_from_float.restype = u8
+        lib.orc_e4m3_from_float_array.argtypes = [_P(f32), I, _P(u8)]
+        lib.orc_e4m3_from_float_array.restype = None
+        lib.orc_quant_weights_fp8.argtypes = [_P(u16), I, I, _P(u8), _P(f32)]
+        lib.orc_quant_weights_fp8.restype = I
+        lib.orc_quant_act_fp8.argtypes = [_P(u16), I, I, _P(u8), _P(f32)]
+        lib.orc_quant_act_fp8.restype = I
+        lib.orc_linear_fp8.argtypes = [_P(u8), _P(f32), _P(u8), _P(f32), I, I, I, _P(f64)]
+        lib.orc_linear_fp8.restype = None
         _lib = lib
         return lib
 
@@ -328,3 +340,57 @@ def kv_overwrite(k_cache, v_cache, k_new, v_new, base_pos, n_acc, gamma):
                                     _ptr(k_new, ctypes.c_uint16), _ptr(v_new, ctypes.c_uint16),
                                     _ptr(base_pos, ctypes.c_int32), _ptr(n_acc, ctypes.c_int32),
                                     L, B, H, T, D, gamma)
+
+
+# ---------------------------------------------------------------------------
+# next-3 SpecQuant Q8 -- SpecQuant summary page, contributions and approach:
+# Q4 / Q8 (FP8) / Q16 variants derived post-training from one FP16 parent
+# with shared base weights.  E4M3 per output channel for the weights, per
+# token for the activations; the FP8 linear of the Q8 model.
+# ---------------------------------------------------------------------------
+def e4m3_value(b: int) -> float:
+    """Value of one E4M3 byte (NaN for S.1111.111)."""
+    return float(_load().orc_e4m3_value(int(b) & 0xFF))
+
+
+def e4m3_from_float(f) -> np.ndarray:
+    """fp32 values -> E4M3 bytes (round to nearest even, saturate at 448)."""
+    f = _c(np.atleast_1d(np.asarray(f, np.float32)), np.float32)
+    out = np.zeros(f.shape, np.uint8)
+    _load().orc_e4m3_from_float_array(_ptr(f, ctypes.c_float), f.size, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def quant_weights_fp8(w16_bits):
+    """w16_bits: fp16 bit patterns uint16 [N][K] (the parent weights).
+    Returns (status, w8 uint8 [N][K], s8 float32 [N])."""
+    w16_bits = _c(w16_bits, np.uint16)
+    N, K = w16_bits.shape
+    w8 = np.zeros((N, K), np.uint8)
+    s8 = np.zeros(N, np.float32)
+    st = _load().orc_quant_weights_fp8(_ptr(w16_bits, ctypes.c_uint16), N, K, _ptr(w8, ctypes.c_uint8),
+                                       _ptr(s8, ctypes.c_float))
+    return st, w8, s8
+
+
+def quant_act_fp8(x_bits):
+    """x_bits: bf16 bit patterns uint16 [M][K].  Returns (status, xq uint8 [M][K], sa float32 [M])."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    xq = np.zeros((M, K), np.uint8)
+    sa = np.zeros(M, np.float32)
+    st = _load().orc_quant_act_fp8(_ptr(x_bits, ctypes.c_uint16), M, K, _ptr(xq, ctypes.c_uint8),
+                                   _ptr(sa, ctypes.c_float))
+    return st, xq, sa
+
+
+def linear_fp8(xq, sa, w8, s8):
+    """fp64 reference of the FP8 linear: ref [M][N] = sa[m] s8[n] sum_k xq w8."""
+    xq, w8 = _c(xq, np.uint8), _c(w8, np.uint8)
+    sa, s8 = _c(sa, np.float32), _c(s8, np.float32)
+    M, K = xq.shape
+    N = w8.shape[0]
+    ref = np.zeros((M, N), np.float64)
+    _load().orc_linear_fp8(_ptr(xq, ctypes.c_uint8), _ptr(sa, ctypes.c_float), _ptr(w8, ctypes.c_uint8),
+                           _ptr(s8, ctypes.c_float), M, N, K, _ptr(ref, ctypes.c_double))
+    return ref

@@ -621,3 +621,131 @@ int orc_kv_overwrite(uint16_t *kc, uint16_t *vc, const uint16_t *kn, const uint1
     }
     return st;
 }
+
+/* ------------------------------------------------------------------ */
+/* next-3: SpecQuant Q8 -- FP8 (E4M3) weights derived from the FP16     */
+/* parent, and the FP8 linear of the Q8 (parent / verify) model         */
+/* ------------------------------------------------------------------ */
+/*
+ * [SQ] "SpecQuant: Speculative Decoding with Multi-Parent Quantization for
+ * Adaptive LLM Inference" summary (arxiv-wiki), contributions and approach:
+ * Q4 (INT4), Q8 (FP8) and Q16 (FP16) variants derived post-training from one
+ * FP16 parent with shared base weights; a draft proposes, the chosen parent
+ * verifies.  Readings taken (the page names only "FP8"):
+ *   - E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
+ *     infinities, S.1111.111 is NaN, largest finite 448, subnormals m 2^-9;
+ *   - conversion to E4M3: round to nearest, ties to the even code; finite
+ *     values beyond 448 in magnitude saturate to +-448;
+ *   - weights: per output channel n, s8 = amax_k |W[n][k]| / 448 (fp32, IEEE
+ *     division), w8 = E4M3(W / s8) (fp32 quotient, IEEE division); an
+ *     all-zero row has s8 = 0 and codes 0;
+ *   - activations: the same per token m (bf16 input), scale sa[m];
+ *   - linear: y[m][n] = sa[m] s8[n] sum_k E4M3(xq) E4M3(w8), fp64 reference
+ *     (the GPU accumulates in fp32, compared within 1e-2 (1 + |ref|)).
+ */
+
+/* value of an E4M3 byte, from the format definition */
+double orc_e4m3_value(uint8_t b)
+{
+    int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9)             /* subnormal: m / 8 * 2^-6 */
+                        : ldexp(8.0 + (double)m, e - 10);  /* (1 + m / 8) * 2^(e - 7) */
+    return s ? -v : v;
+}
+
+/* float -> E4M3: the nearest representable value (ties to the even code),
+ * magnitudes of 448 and above saturate to 448, NaN -> 0x7F.  The positive
+ * codes 0x00..0x7E are ordered by value, so the neighbours are found by
+ * search and compared exactly in fp64. */
+uint8_t orc_e4m3_from_float(float f)
+{
+    if (isnan(f))
+        return 0x7F;
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int lo = 0;
+    for (int c = 0; c <= 0x7E; ++c)
+        if (orc_e4m3_value((uint8_t)c) <= a)
+            lo = c;
+    double dl = a - orc_e4m3_value((uint8_t)lo), dh = orc_e4m3_value((uint8_t)(lo + 1)) - a;
+    int c = dl < dh ? lo : dh < dl ? lo + 1 : ((lo & 1) ? lo + 1 : lo);
+    return sign | (uint8_t)c;
+}
+
+void orc_e4m3_from_float_array(const float *f, int n, uint8_t *out)
+{
+    for (int i = 0; i < n; ++i)
+        out[i] = orc_e4m3_from_float(f[i]);
+}
+
+/* one row of n values (already as floats): scale amax / 448 and codes */
+static int fp8_row(const float *v, int n, uint8_t *codes, float *scale)
+{
+    float amax = 0.0f;
+    for (int k = 0; k < n; ++k) {
+        if (!isfinite(v[k]))
+            return ORC_ERR_NONFINITE;
+        float a = fabsf(v[k]);
+        if (a > amax)
+            amax = a;
+    }
+    float s = amax / 448.0f;
+    *scale = s;
+    for (int k = 0; k < n; ++k)
+        codes[k] = (s == 0.0f) ? 0 : orc_e4m3_from_float(v[k] / s);
+    return ORC_OK;
+}
+
+/* Q8 weights from the fp16 parent W16 [N][K] -> w8 [N][K], s8 [N] */
+int orc_quant_weights_fp8(const uint16_t *w16, int N, int K, uint8_t *w8, float *s8)
+{
+    int st = ORC_OK;
+#pragma omp parallel for schedule(static) reduction(max : st)
+    for (int n = 0; n < N; ++n) {
+        float *row = (float *)malloc(sizeof(float) * (size_t)K);
+        for (int k = 0; k < K; ++k)
+            row[k] = (float)fp16_value(w16[(size_t)n * K + k]);
+        int r = fp8_row(row, K, w8 + (size_t)n * K, &s8[n]);
+        if (r > st)
+            st = r;
+        free(row);
+    }
+    return st;
+}
+
+/* per-token E4M3 activations from bf16 x [M][K] -> xq [M][K], sa [M] */
+int orc_quant_act_fp8(const uint16_t *x, int M, int K, uint8_t *xq, float *sa)
+{
+    int st = ORC_OK;
+    for (int m = 0; m < M; ++m) {
+        float *row = (float *)malloc(sizeof(float) * (size_t)K);
+        for (int k = 0; k < K; ++k)
+            row[k] = bf16_value(x[(size_t)m * K + k]);
+        int r = fp8_row(row, K, xq + (size_t)m * K, &sa[m]);
+        if (r > st)
+            st = r;
+        free(row);
+    }
+    return st;
+}
+
+/* fp64 reference of the FP8 linear: ref[m][n] = sa s8 sum_k xq w8 */
+void orc_linear_fp8(const uint8_t *xq, const float *sa, const uint8_t *w8, const float *s8, int M, int N, int K,
+                    double *ref)
+{
+    double lut[256];
+    for (int b = 0; b < 256; ++b)
+        lut[b] = orc_e4m3_value((uint8_t)b);
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n)
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k)
+                acc += lut[xq[(size_t)m * K + k]] * lut[w8[(size_t)n * K + k]];
+            ref[(size_t)m * N + n] = acc * (double)sa[m] * (double)s8[n];
+        }
+}

@@ -744,3 +744,99 @@ def test_kv_overwrite_range(base, nacc):
     st = oracle.kv_overwrite(kc, vc, kn, kn.copy(), np.array([base], np.int32),
                              np.array([nacc], np.int32), gamma)
     assert st == oracle.ERR_RANGE and not kc.any()
+
+
+# ----------------------------------------------------------------- SpecQuant Q8 (FP8, next-3)
+# SpecQuant summary page, contributions and approach: FP8 (Q8) variant
+# derived from the FP16 parent.  The E4M3 codec against torch's float8_e4m3fn
+# (an independent implementation of the same format), the derivation against
+# invariants of its definition, the linear against an integer matmul.
+def test_e4m3_decode_every_code_matches_library():
+    import torch
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    got = np.array([oracle.e4m3_value(b) for b in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin].astype(np.float64))
+    # the extremes of the format: 448 and the smallest subnormal 2^-9
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_library_and_saturates():
+    import torch
+    rng = np.random.default_rng(41)
+    x = np.concatenate([rng.standard_normal(40000) * 0.01, rng.standard_normal(40000) * 30,
+                        rng.uniform(-447.9, 447.9, 20000), rng.uniform(-2.0 ** -7, 2.0 ** -7, 20000)])
+    # exact midpoints between neighbouring codes: ties go to the even code
+    pos = np.array([oracle.e4m3_value(b) for b in range(0x7E)])
+    mids = (pos + np.array([oracle.e4m3_value(b + 1) for b in range(0x7E)])) / 2
+    x = np.concatenate([x, mids, -mids]).astype(np.float32)
+    got = oracle.e4m3_from_float(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+    assert all(int(oracle.e4m3_from_float(np.float32(m))[0]) % 2 == 0 for m in mids)
+    # saturation at 448, NaN, signed zero
+    big = np.array([448.0, 464.0, 1e6, 3e38, -500.0], np.float32)
+    assert oracle.e4m3_from_float(big).tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+    assert int(oracle.e4m3_from_float(np.float32("nan"))[0]) == 0x7F
+    assert int(oracle.e4m3_from_float(np.float32(-0.0))[0]) == 0x80
+
+
+def test_fp8_weight_derivation_invariants():
+    rng = np.random.default_rng(42)
+    W = (rng.standard_normal((40, 512)) * 0.02).astype(np.float16)
+    W[3, :] = 0.0                                        # an all-zero row
+    W[5, 7] = np.float16(-3.5)                           # a negative row maximum
+    st, w8, s8 = oracle.quant_weights_fp8(W.view(np.uint16))
+    assert st == 0
+    Wf = W.astype(np.float64)
+    amax = np.abs(Wf).max(axis=1)
+    dec = np.vectorize(oracle.e4m3_value)(w8)
+    for n in range(W.shape[0]):
+        if amax[n] == 0:
+            assert s8[n] == 0 and not w8[n].any()
+            continue
+        j = int(np.argmax(np.abs(Wf[n])))
+        assert w8[n, j] == (0xFE if Wf[n, j] < 0 else 0x7E)            # the row maximum maps to 448
+        rec = dec[n] * float(s8[n])
+        # E4M3 keeps 3 mantissa bits: a half-ulp error of at most 2^-4 of the
+        # value (normal range), at most 2^-10 s8 in the subnormal range
+        bound = np.maximum(np.abs(Wf[n]) * 2.0 ** -4, 2.0 ** -10 * float(s8[n])) * (1 + 1e-6)
+        assert np.all(np.abs(rec - Wf[n]) <= bound)
+        assert abs(float(s8[n]) * 448 - amax[n]) <= amax[n] * 2.0 ** -23
+    bad = W.copy()
+    bad[0, 0] = np.float16("inf")
+    assert oracle.quant_weights_fp8(bad.view(np.uint16))[0] == 8
+
+
+def test_fp8_activation_quant_invariants():
+    import torch
+    rng = np.random.default_rng(43)
+    x = torch.from_numpy(rng.standard_normal((6, 384)).astype(np.float32)).to(torch.bfloat16)
+    x[2] = 0.0
+    st, xq, sa = oracle.quant_act_fp8(x.view(torch.int16).numpy().view(np.uint16))
+    assert st == 0
+    xf = x.float().numpy().astype(np.float64)
+    for m in range(6):
+        if sa[m] == 0:
+            assert not xq[m].any()
+            continue
+        j = int(np.argmax(np.abs(xf[m])))
+        assert xq[m, j] == (0xFE if xf[m, j] < 0 else 0x7E)
+
+
+def test_fp8_linear_reduces_to_integer_matmul():
+    # codes holding the integers -8..8 exactly, unit scales: an integer matmul
+    rng = np.random.default_rng(44)
+    ints = np.arange(-8, 9)
+    code_of = {int(v): int(oracle.e4m3_from_float(np.float32(v))[0]) for v in ints}
+    assert all(oracle.e4m3_value(c) == v for v, c in code_of.items())
+    A = rng.integers(-8, 9, (5, 256))
+    B = rng.integers(-8, 9, (7, 256))
+    xq = np.vectorize(code_of.get)(A).astype(np.uint8)
+    w8 = np.vectorize(code_of.get)(B).astype(np.uint8)
+    ref = oracle.linear_fp8(xq, np.ones(5, np.float32), w8, np.ones(7, np.float32))
+    assert np.array_equal(ref, (A @ B.T).astype(np.float64))
+    # power-of-two scales scale the result exactly; the operands are not swapped
+    ref2 = oracle.linear_fp8(xq, np.full(5, 0.25, np.float32), w8, np.arange(1, 8, dtype=np.float32))
+    assert np.array_equal(ref2, (A @ B.T) * 0.25 * np.arange(1, 8)[None, :])
