@@ -11,6 +11,8 @@
  *   [QS-bg]     "QSPEC: Speculative Decoding with Complementary Quantization
  *               Schemes" summary page (molayo1419.me), background terms.
  *   [QS-design] same page, "QSPEC structure".
+ *   [SQ]        "SpecQuant: Speculative Decoding with Multi-Parent
+ *               Quantization for Adaptive LLM Inference" summary page.
  *
  * Conventions for every call
  *   - Every pointer argument is a DEVICE pointer, owned by the caller, unless
@@ -292,6 +294,38 @@ int qspec_kv_overwrite(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_n
                        const uint16_t *v_new, const int32_t *base_pos, const int32_t *n_acc,
                        int L, int B, int H, int T, int D, int gamma, int32_t *dev_status,
                        qspec_stream_t stream);
+
+/*
+ * SpecQuant Q8 variant.  [SQ] "SpecQuant: Speculative Decoding with
+ * Multi-Parent Quantization for Adaptive LLM Inference" summary page,
+ * contributions and approach: INT4 (Q4), FP8 (Q8) and FP16 (Q16) variants are
+ * derived post-training from one FP16 parent with shared base weights, and
+ * the chosen parent verifies the draft.  FP8 is E4M3 (1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits, largest finite 448); a conversion rounds
+ * to nearest even and saturates at +-448.
+ *
+ * qspec_quant_weights_fp8: per output channel n of the parent weights,
+ *   s8[n] = amax_k |W[n][k]| / 448 (fp32, IEEE division),
+ *   w8[n][k] = E4M3(W[n][k] / s8[n]) (fp32 IEEE quotient); a zero row gives
+ *   s8 = 0 and codes 0.
+ *   w_fp16 uint16 [N][K] fp16 bits (16-byte aligned), w8 uint8 [N][K] out
+ *   (8-byte aligned), s8 float [N] out.
+ * qspec_quant_act_fp8: the same per token m of bf16 activations.
+ *   x_bf16 uint16 [M][ldx] (ldx >= K, ldx % 8 == 0, 16-byte aligned),
+ *   xq uint8 [M][K] out, sa float [M] out.
+ * qspec_linear_fp8: the Q8 linear on the tensor cores (E4M3 x E4M3, fp32
+ *   accumulation): y[m][n] = bf16(sum_k E4M3(xq) E4M3(w8) * sa[m] * s8[n]),
+ *   within 1e-2 (1 + |ref|) of the fp64 value of the same sum.
+ *   xq, w8 16-byte aligned; y_bf16 uint16 [M][ldy] out (ldy >= N).
+ * K is a multiple of 128.  Device errors: QSPEC_ERR_NONFINITE (a NaN or inf
+ * input to a quantiser), QSPEC_ERR_TIMEOUT (a bounded wait expired).
+ */
+int qspec_quant_weights_fp8(const uint16_t *w_fp16, int N, int K, uint8_t *w8, float *s8,
+                            int32_t *dev_status, qspec_stream_t stream);
+int qspec_quant_act_fp8(const uint16_t *x_bf16, int M, int K, int ldx, uint8_t *xq, float *sa,
+                        int32_t *dev_status, qspec_stream_t stream);
+int qspec_linear_fp8(const uint8_t *xq, const float *sa, const uint8_t *w8, const float *s8, int M, int N,
+                     int K, uint16_t *y_bf16, int ldy, int32_t *dev_status, qspec_stream_t stream);
 
 /*
  * Diagnostic for tests of the bounded waits; the pages have no counterpart.

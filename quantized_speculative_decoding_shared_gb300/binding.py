@@ -33,7 +33,8 @@ EXPORTED = ["qspec_version", "qspec_status_string", "qspec_last_cuda_error", "qs
             "qspec_quant_act_int4", "qspec_linear_w4a4", "qspec_linear_w4a4_bf16", "qspec_linear_w4a16",
             "qspec_verify_workspace_bytes", "qspec_verify_greedy", "qspec_verify_sample",
             "qspec_kv_overwrite", "qspec_verify_sample_noalloc", "qspec_draft_workspace_bytes",
-            "qspec_draft_sample", "qspec_debug_linear_bounded"]
+            "qspec_draft_sample", "qspec_debug_linear_bounded", "qspec_quant_weights_fp8",
+            "qspec_quant_act_fp8", "qspec_linear_fp8"]
 KERNEL_W4A16_TC, KERNEL_W4A4_GEMV_TC, KERNEL_W4A4_TC = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -85,6 +86,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "qspec_draft_sample": ([vp, i32, i32, u64, u64, i32, vp, vp, vp, vp, sz_t, vp, vp], i32),
             "qspec_debug_linear_bounded": ([i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, i32,
                                             ctypes.c_uint32, i32, vp, vp], i32),
+            "qspec_quant_weights_fp8": ([vp, i32, i32, vp, vp, vp, vp], i32),
+            "qspec_quant_act_fp8": ([vp, i32, i32, i32, vp, vp, vp, vp], i32),
+            "qspec_linear_fp8": ([vp, vp, vp, vp, i32, i32, i32, vp, i32, vp, vp], i32),
         }
         for name, (args, res) in proto.items():
             f = getattr(lib, name)
@@ -213,6 +217,21 @@ def qspec_debug_linear_bounded(kernel, x, xq, sx, qs, packed, sz, M, N, K, y, ld
                                                      _ptr(dev_status), _stream(stream))
 
 
+def qspec_quant_weights_fp8(w16, N, K, w8, s8, dev_status=None, stream=None):
+    return load_library().qspec_quant_weights_fp8(_ptr(w16), N, K, _ptr(w8), _ptr(s8), _ptr(dev_status),
+                                                  _stream(stream))
+
+
+def qspec_quant_act_fp8(x, M, K, ldx, xq, sa, dev_status=None, stream=None):
+    return load_library().qspec_quant_act_fp8(_ptr(x), M, K, ldx, _ptr(xq), _ptr(sa), _ptr(dev_status),
+                                              _stream(stream))
+
+
+def qspec_linear_fp8(xq, sa, w8, s8, M, N, K, y, ldy, dev_status=None, stream=None):
+    return load_library().qspec_linear_fp8(_ptr(xq), _ptr(sa), _ptr(w8), _ptr(s8), M, N, K, _ptr(y), ldy,
+                                           _ptr(dev_status), _stream(stream))
+
+
 # ---------------------------------------------------------------------------
 # allocating conveniences (torch tensors in, torch tensors out)
 # ---------------------------------------------------------------------------
@@ -332,3 +351,31 @@ def kv_overwrite(k_cache, v_cache, k_new, v_new, base_pos, n_acc, dev_status=Non
     gamma = k_new.shape[2] - 1
     _check(qspec_kv_overwrite(k_cache, v_cache, k_new, v_new, base_pos, n_acc, L, B, H, T, D,
                               gamma, dev_status, stream), "qspec_kv_overwrite")
+
+
+def quant_weights_fp8(w16, dev_status=None, stream=None):
+    """Parent weights fp16 [N][K] -> (w8 uint8 [N][K] E4M3, s8 fp32 [N])."""
+    _need(w16, torch.float16, "w16")
+    N, K = w16.shape
+    w8 = torch.empty((N, K), dtype=torch.uint8, device=w16.device)
+    s8 = torch.empty(N, dtype=torch.float32, device=w16.device)
+    _check(qspec_quant_weights_fp8(w16, N, K, w8, s8, dev_status, stream), "qspec_quant_weights_fp8")
+    return w8, s8
+
+
+def quant_act_fp8(x, dev_status=None, stream=None):
+    """bf16 [M][K] -> (xq uint8 [M][K] E4M3, sa fp32 [M])."""
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sa = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(qspec_quant_act_fp8(x, M, K, x.stride(0), xq, sa, dev_status, stream), "qspec_quant_act_fp8")
+    return xq, sa
+
+
+def linear_fp8(xq, sa, w8, s8, out=None, dev_status=None, stream=None):
+    M, K = xq.shape
+    N = w8.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    _check(qspec_linear_fp8(xq, sa, w8, s8, M, N, K, y, y.stride(0), dev_status, stream), "qspec_linear_fp8")
+    return y

@@ -65,6 +65,11 @@ int launch_w4a4_gemv_tc(const uint8_t *xq, const float *sx, const int32_t *qs, c
 // bytes x box_rows rows, 128-byte swizzle, rows past N read as zeros.
 int weight_tmap(CUtensorMap *out, const uint8_t *packed, int N, int K, int box_rows);
 
+// 2-D TMA map over a row-major byte matrix [rows][cols], rows `pitch` bytes
+// apart: boxes of 128 bytes x box_rows rows, 128-byte swizzle, reads past
+// the matrix give zeros (not cached).
+int byte_tmap_sw128(CUtensorMap *out, const void *base, int rows, int cols, size_t pitch, int box_rows);
+
 // Polls of a bounded barrier wait in the tensor-core kernels (each poll
 // suspends for a hardware-chosen time); a wait that runs out sets
 // QSPEC_ERR_TIMEOUT.

@@ -74,4 +74,22 @@ int weight_tmap(CUtensorMap *out, const uint8_t *packed, int N, int K, int box_r
     return QSPEC_OK;
 }
 
+// 2-D TMA map over a row-major byte matrix [rows][cols] with rows `pitch`
+// bytes apart: boxes of 128 bytes x box_rows rows, 128-byte swizzle, rows
+// and columns past the matrix read as zeros.  Not cached (for per-call
+// operands); QSPEC_ERR_UNSUPPORTED if the driver refuses the map.
+int byte_tmap_sw128(CUtensorMap *out, const void *base, int rows, int cols, size_t pitch, int box_rows) {
+    EncodeTiled fn = encoder();
+    if (!fn) return QSPEC_ERR_UNSUPPORTED;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)pitch};
+    const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    std::memset(out, 0, sizeof(*out));
+    CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QSPEC_OK : QSPEC_ERR_UNSUPPORTED;
+}
+
 }  // namespace qspec
