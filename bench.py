@@ -549,6 +549,30 @@ def targets(rnd_obj, dev, stream, reps=5):
         t, gbs = run(fns, nbytes)
         w4["M%d" % M] = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)}
     out["w4a4_draft"] = w4
+    # SpecQuant Q8 verify: FP8 weights derived from an FP16 parent of the same
+    # shapes, per-token E4M3 activations, the FP8 linear (two calls per linear)
+    q8 = {}
+    fp8w = []
+    for j, (name, N, K, _) in enumerate(linears):
+        g = torch.Generator(device=dev).manual_seed(500 + j)
+        w16 = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.float16)
+        fp8w.append((name, N, K) + q.quant_weights_fp8(w16))
+        del w16
+    for M in (5, 80):
+        fns, nbytes = [], 0
+        for j, (name, N, K, w8, s8) in enumerate(fp8w):
+            x = syn.activations(M, K, 600 + j, device=dev, outlier_frac=0.01)
+            xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+            sa = torch.empty(M, dtype=torch.float32, device=dev)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fns.append(lambda x=x, xq=xq, sa=sa, K=K, M=M: q.qspec_quant_act_fp8(x, M, K, K, xq, sa))
+            fns.append(lambda xq=xq, sa=sa, w8=w8, s8=s8, y=y, N=N, K=K, M=M:
+                       q.qspec_linear_fp8(xq, sa, w8, s8, M, N, K, y, N))
+            nbytes += N * K + 4 * N + 2 * M * K + M * K + 4 * M + M * K + 2 * M * N
+        t, gbs = run(fns, nbytes)
+        q8["M%d" % M] = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)}
+    del fp8w
+    out["q8_fp8_verify"] = dict(q8, bytes="E4M3 weights 1 byte each + scales; activations quantised per call")
     # prefill: M = 4096 through gate/up and down
     M = 4096
     bf16, bkind = measured_bf16_tflops()

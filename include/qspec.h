@@ -164,6 +164,39 @@ int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t *packed, c
                        int M, int N, int K, uint16_t *y_bf16, int ldy, int32_t *dev_status,
                        qspec_stream_t stream);
 
+/*
+ * a4 + a7 in one call: the verify pass's k / v projection, writing its
+ * outputs into the KV caches from the epilogue.  [QS-design] for accepted
+ * tokens the W4A4 cache entries are replaced by the W4A16 ones; doing it in
+ * the projection that produces those entries removes the separate copy
+ * (qspec_kv_overwrite) and its second read.
+ *
+ * Computes y exactly as qspec_linear_w4a16 (M = B (gamma + 1) verify rows,
+ * row m = b (gamma + 1) + r) and also stores every output of columns
+ *   [kv_col0, kv_col0 + H D)          into k_cache[b][h][base_pos[b] + r][d]
+ *   [kv_col0 + H D, kv_col0 + 2 H D)  into v_cache[b][h][base_pos[b] + r][d]
+ * (column kv_col0 + h D + d), for r = 0 .. n_acc[b] -- or, with n_acc NULL,
+ * for every r = 0 .. gamma: the verify pass runs before acceptance is known,
+ * and the rows past the accepted ones lie beyond the cache length the caller
+ * keeps (base_pos[b] + n_acc[b] + 1), so the cache read afterwards is the
+ * same as with qspec_kv_overwrite.
+ *
+ *   x_bf16 .. ldy                     as in qspec_linear_w4a16
+ *   kv_col0, H, D                     the K columns' offset in y, heads, head dim
+ *   T                                 cache capacity (positions)
+ *   k_cache, v_cache uint16 [B][H][T][D]  one layer's caches, bf16 (either may be
+ *                                     NULL; with v_cache NULL only H D columns
+ *                                     are needed)
+ *   base_pos int32 [B], n_acc int32 [B] (nullable)
+ * Device errors: QSPEC_ERR_RANGE when base_pos < 0, n_acc outside [0, gamma]
+ * or base_pos + (the last row written) >= T (that sequence's cache is left
+ * untouched; y is still written).
+ */
+int qspec_linear_w4a16_kv(const uint16_t *x_bf16, int ldx, const uint8_t *packed, const uint32_t *sz, int M,
+                          int N, int K, uint16_t *y_bf16, int ldy, int kv_col0, int H, int D, int T, int gamma,
+                          uint16_t *k_cache, uint16_t *v_cache, const int32_t *base_pos, const int32_t *n_acc,
+                          int32_t *dev_status, qspec_stream_t stream);
+
 /* Bytes of workspace the verification calls need for (B, gamma, V). */
 size_t qspec_verify_workspace_bytes(int B, int gamma, int V);
 

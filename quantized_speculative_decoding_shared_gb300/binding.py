@@ -34,7 +34,7 @@ EXPORTED = ["qspec_version", "qspec_status_string", "qspec_last_cuda_error", "qs
             "qspec_verify_workspace_bytes", "qspec_verify_greedy", "qspec_verify_sample",
             "qspec_kv_overwrite", "qspec_verify_sample_noalloc", "qspec_draft_workspace_bytes",
             "qspec_draft_sample", "qspec_debug_linear_bounded", "qspec_quant_weights_fp8",
-            "qspec_quant_act_fp8", "qspec_linear_fp8"]
+            "qspec_quant_act_fp8", "qspec_linear_fp8", "qspec_linear_w4a16_kv"]
 KERNEL_W4A16_TC, KERNEL_W4A4_GEMV_TC, KERNEL_W4A4_TC = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -89,6 +89,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "qspec_quant_weights_fp8": ([vp, i32, i32, vp, vp, vp, vp], i32),
             "qspec_quant_act_fp8": ([vp, i32, i32, i32, vp, vp, vp, vp], i32),
             "qspec_linear_fp8": ([vp, vp, vp, vp, i32, i32, i32, vp, i32, vp, vp], i32),
+            "qspec_linear_w4a16_kv": ([vp, i32, vp, vp, i32, i32, i32, vp, i32, i32, i32, i32, i32, i32,
+                                       vp, vp, vp, vp, vp, vp], i32),
         }
         for name, (args, res) in proto.items():
             f = getattr(lib, name)
@@ -158,6 +160,13 @@ def qspec_linear_w4a4_bf16(x, ldx, packed, sz, M, N, K, y, ldy, xq, sx, qs, dbg_
 def qspec_linear_w4a16(x, ldx, packed, sz, M, N, K, y, ldy, dev_status=None, stream=None):
     return load_library().qspec_linear_w4a16(_ptr(x), ldx, _ptr(packed), _ptr(sz), M, N, K,
                                              _ptr(y), ldy, _ptr(dev_status), _stream(stream))
+
+
+def qspec_linear_w4a16_kv(x, ldx, packed, sz, M, N, K, y, ldy, kv_col0, H, D, T, gamma, k_cache, v_cache,
+                          base_pos, n_acc, dev_status=None, stream=None):
+    return load_library().qspec_linear_w4a16_kv(_ptr(x), ldx, _ptr(packed), _ptr(sz), M, N, K, _ptr(y), ldy,
+                                                kv_col0, H, D, T, gamma, _ptr(k_cache), _ptr(v_cache),
+                                                _ptr(base_pos), _ptr(n_acc), _ptr(dev_status), _stream(stream))
 
 
 def qspec_verify_workspace_bytes(B, gamma, V):

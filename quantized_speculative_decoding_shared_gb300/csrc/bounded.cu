@@ -2,6 +2,7 @@
 // with a chosen bound on its barrier waits and, optionally, a wait that is
 // made to run out, so that the timeout exit (status, drain, tensor memory
 // freed, context still usable) can be tested without any fault.
+#include "qspec_device.cuh"
 #include "qspec_host.h"
 
 using namespace qspec;
@@ -26,7 +27,8 @@ extern "C" int qspec_debug_linear_bounded(int kernel, const uint16_t *x_bf16, co
     cudaStream_t st = as_cuda(stream);
     switch (kernel) {
         case QSPEC_KERNEL_W4A16_TC:
-            return launch_w4a16_tc(x_bf16, K, packed, sz, M, N, K, y_bf16, ldy, dev_status, st, wait_limit, stall);
+            return launch_w4a16_tc(x_bf16, K, packed, sz, M, N, K, y_bf16, ldy, dev_status, st, wait_limit, stall,
+                                   KvOut{nullptr, nullptr, nullptr, nullptr, 0, 1, 1, 1, 0, nullptr});
         case QSPEC_KERNEL_W4A4_GEMV_TC:
             return launch_w4a4_gemv_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, nullptr, dev_status, st,
                                        wait_limit, stall);

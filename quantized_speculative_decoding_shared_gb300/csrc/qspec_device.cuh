@@ -254,6 +254,40 @@ __device__ __forceinline__ uint32_t quant_group_halfwarp(uint4 v, float &scale, 
     return n[0];
 }
 
+// A W4A16 linear whose epilogue also writes its outputs into a KV cache
+// (the verify pass's k / v projection, QSPEC summary page, "QSPEC
+// structure": the accepted tokens' cache entries become the W4A16 ones).
+// Output columns [c0, c0 + H D) are K and the next H D columns V (either
+// cache may be null); output row m = b (gamma + 1) + r is position
+// base[b] + r of sequence b in the caches [B][H][T][D], written for
+// r <= nacc[b], or for every r when nacc is null.  A sequence with
+// base[b] < 0, nacc[b] outside [0, gamma] or base[b] + (its last r) >= T is
+// left untouched and QSPEC_ERR_RANGE is flagged.  k == v == null: no cache
+// output.
+struct KvOut {
+    uint16_t *k, *v;
+    const int32_t *base, *nacc;
+    int c0, H, D, T, gamma;
+    int32_t *st;
+};
+
+__device__ __forceinline__ void kv_store(const KvOut &kv, int m, int n, uint16_t val) {
+    if (kv.k == nullptr && kv.v == nullptr) return;
+    const int HD = kv.H * kv.D, j = n - kv.c0;
+    if (j < 0 || j >= 2 * HD) return;
+    uint16_t *cache = j < HD ? kv.k : kv.v;
+    if (cache == nullptr) return;
+    const int jj = j < HD ? j : j - HD, h = jj / kv.D, d = jj - h * kv.D;
+    const int b = m / (kv.gamma + 1), r = m - b * (kv.gamma + 1);
+    const int last = kv.nacc ? kv.nacc[b] : kv.gamma, p0 = kv.base[b];
+    if (p0 < 0 || last < 0 || last > kv.gamma || p0 + last >= kv.T) {
+        flag(kv.st, QSPEC_ERR_RANGE);
+        return;
+    }
+    if (r > last) return;
+    cache[(((size_t)b * kv.H + h) * kv.T + p0 + r) * kv.D + d] = val;
+}
+
 typedef unsigned __int128 u128;
 
 }  // namespace qspec

@@ -45,9 +45,12 @@ int launch_w4a4_dp4a(const uint8_t *xq, const float *sx, const int32_t *qs, cons
 // issuer first wait on a barrier nothing arrives at, so that the wait runs
 // out and the kernel takes its timeout exit.
 
-// Large-M W4A16 on the tensor cores (w4a16_tc.cu).
+// Large-M W4A16 on the tensor cores (w4a16_tc.cu); kv: the optional cache
+// output of the epilogue (KvOut in qspec_device.cuh).
+struct KvOut;
 int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
-                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall);
+                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall,
+                    const KvOut &kv);
 
 // Larger-M W4A4 on the tensor cores (w4a4_tc.cu).
 int launch_w4a4_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,

@@ -87,7 +87,7 @@ template <int MT, int kPrefetch, int kWarps>
 __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
     w4a16_hmma_gemv_kernel(const uint16_t *__restrict__ x, int ldx, const uint8_t *__restrict__ packed,
                            const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y,
-                           int ldy) {
+                           int ldy, KvOut kv) {
     static_assert(MT >= 1 && MT <= 8 && (MT == 1 || MT % 2 == 0), "one n8 block of tokens");
     constexpr int kThreads = kWarps * 32;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -228,7 +228,9 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
             float sum = 0.0f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) sum += rb[(size_t)w * 16 * MT + p];
-            y[(size_t)m * ldy + n] = float_to_bf16_bits(sum);
+            const uint16_t v16 = float_to_bf16_bits(sum);
+            y[(size_t)m * ldy + n] = v16;
+            kv_store(kv, m, n, v16);
         }
     };
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
 
 template <int MT, int kWarps>
 int launch_w4a16_w(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
-                   uint16_t *y, int ldy, cudaStream_t st) {
+                   uint16_t *y, int ldy, const KvOut &kv, cudaStream_t st) {
     const size_t smem = smem_bytes(MT, M, K, kWarps);
     auto kern = w4a16_hmma_gemv_kernel<MT, 1, kWarps>;
     int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 200 * 1024);
@@ -320,15 +322,16 @@ int launch_w4a16_w(const uint16_t *x, int ldx, const uint8_t *packed, const uint
     const int per_col = std::max(1, (16 / kWarps) * sm_count() / token_tiles);
     dim3 grid((unsigned)std::min(n_tiles, per_col), (unsigned)token_tiles);
     return launch_pdl("qspec_linear_w4a16", kern, grid, dim3(kWarps * 32), smem, st, x, ldx, packed, sz, M, N, K, y,
-                      ldy);
+                      ldy, kv);
 }
 
 // two 8-warp CTAs per SM when their shared memory fits, else one of 16 warps
 template <int MT>
 int launch_w4a16(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
-                 uint16_t *y, int ldy, cudaStream_t st) {
-    if (smem_bytes(MT, M, K, 8) <= 112 * 1024) return launch_w4a16_w<MT, 8>(x, ldx, packed, sz, M, N, K, y, ldy, st);
-    return launch_w4a16_w<MT, 16>(x, ldx, packed, sz, M, N, K, y, ldy, st);
+                 uint16_t *y, int ldy, const KvOut &kv, cudaStream_t st) {
+    if (smem_bytes(MT, M, K, 8) <= 112 * 1024)
+        return launch_w4a16_w<MT, 8>(x, ldx, packed, sz, M, N, K, y, ldy, kv, st);
+    return launch_w4a16_w<MT, 16>(x, ldx, packed, sz, M, N, K, y, ldy, kv, st);
 }
 
 }  // namespace
@@ -337,17 +340,9 @@ int launch_w4a16(const uint16_t *x, int ldx, const uint8_t *packed, const uint32
 
 using namespace qspec;
 
-extern "C" int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t *packed,
-                                  const uint32_t *sz, int M, int N, int K, uint16_t *y_bf16,
-                                  int ldy, int32_t *dev_status, qspec_stream_t stream) {
-    if (!x_bf16 || !packed || !sz || !y_bf16) return QSPEC_ERR_NULL;
-    if (M < 1 || N < 1 || K < kGroup || K % kGroup || ldx < K || ldy < N) return QSPEC_ERR_SHAPE;
-    if (!aligned(x_bf16, 16) || ldx % 8 || !aligned(packed, 16) || !aligned(sz, 4) ||
-        !aligned(y_bf16, 2))
-        return QSPEC_ERR_ALIGN;
-    int rc = check_device();
-    if (rc) return rc;
-    cudaStream_t st = as_cuda(stream);
+// the W4A16 linear, with the cache output of `kv` when it names a cache
+static int linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N,
+                        int K, uint16_t *y_bf16, int ldy, const KvOut &kv, int32_t *dev_status, cudaStream_t st) {
     if (M <= 16) {
         // tokens per CTA: up to 8 (one MMA column block), halved while the
         // token fragments do not fit
@@ -355,12 +350,47 @@ extern "C" int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t
         while (mt > 1 && smem_bytes(mt, M, K, 16) > 200 * 1024) mt /= 2;
         if (smem_bytes(mt, M, K, 16) <= 200 * 1024) {
             switch (mt) {
-                case 1: return launch_w4a16<1>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
-                case 2: return launch_w4a16<2>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
-                case 4: return launch_w4a16<4>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
-                default: return launch_w4a16<8>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, st);
+                case 1: return launch_w4a16<1>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, kv, st);
+                case 2: return launch_w4a16<2>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, kv, st);
+                case 4: return launch_w4a16<4>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, kv, st);
+                default: return launch_w4a16<8>(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, kv, st);
             }
         }
     }
-    return launch_w4a16_tc(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, dev_status, st, kWaitLimit, 0);
+    return launch_w4a16_tc(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, dev_status, st, kWaitLimit, 0, kv);
+}
+
+static int w4a16_args(const uint16_t *x_bf16, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N,
+                      int K, const uint16_t *y_bf16, int ldy) {
+    if (!x_bf16 || !packed || !sz || !y_bf16) return QSPEC_ERR_NULL;
+    if (M < 1 || N < 1 || K < kGroup || K % kGroup || ldx < K || ldy < N) return QSPEC_ERR_SHAPE;
+    if (!aligned(x_bf16, 16) || ldx % 8 || !aligned(packed, 16) || !aligned(sz, 4) || !aligned(y_bf16, 2))
+        return QSPEC_ERR_ALIGN;
+    return check_device();
+}
+
+extern "C" int qspec_linear_w4a16(const uint16_t *x_bf16, int ldx, const uint8_t *packed,
+                                  const uint32_t *sz, int M, int N, int K, uint16_t *y_bf16,
+                                  int ldy, int32_t *dev_status, qspec_stream_t stream) {
+    int rc = w4a16_args(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy);
+    if (rc) return rc;
+    const KvOut none = {nullptr, nullptr, nullptr, nullptr, 0, 1, 1, 1, 0, nullptr};
+    return linear_w4a16(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, none, dev_status, as_cuda(stream));
+}
+
+extern "C" int qspec_linear_w4a16_kv(const uint16_t *x_bf16, int ldx, const uint8_t *packed, const uint32_t *sz,
+                                     int M, int N, int K, uint16_t *y_bf16, int ldy, int kv_col0, int H, int D, int T,
+                                     int gamma, uint16_t *k_cache, uint16_t *v_cache, const int32_t *base_pos,
+                                     const int32_t *n_acc, int32_t *dev_status, qspec_stream_t stream) {
+    int rc = w4a16_args(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy);
+    if (rc) return rc;
+    if ((!k_cache && !v_cache) || !base_pos) return QSPEC_ERR_NULL;
+    if (gamma < 1 || gamma > QSPEC_MAX_GAMMA || M % (gamma + 1) || H < 1 || D < 1 || T < 1 || kv_col0 < 0 ||
+        kv_col0 + (v_cache ? 2 : 1) * H * D > N)
+        return QSPEC_ERR_SHAPE;
+    if ((k_cache && !aligned(k_cache, 2)) || (v_cache && !aligned(v_cache, 2)) || !aligned(base_pos, 4) ||
+        (n_acc && !aligned(n_acc, 4)))
+        return QSPEC_ERR_ALIGN;
+    const KvOut kv = {k_cache, v_cache, base_pos, n_acc, kv_col0, H, D, T, gamma, dev_status};
+    return linear_w4a16(x_bf16, ldx, packed, sz, M, N, K, y_bf16, ldy, kv, dev_status, as_cuda(stream));
 }

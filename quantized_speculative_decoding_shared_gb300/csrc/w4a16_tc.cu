@@ -94,7 +94,7 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_umma_kernel(const uint16_t *__restrict__ x, int ldx, const uint8_t *__restrict__ packed,
                       const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
-                      int32_t *st, int C, uint32_t wait_limit, int stall) {
+                      int32_t *st, int C, uint32_t wait_limit, int stall, KvOut kv) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem<BN> &sm = *reinterpret_cast<Smem<BN> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -260,9 +260,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {
                 const int m = t0 + eh * kHalf + 2 * i;
-                if (m < M) y[(size_t)m * ldy + n] = float_to_bf16_bits(__uint_as_float((uint32_t)acc[i]));
-                if (m + 1 < M)
-                    y[(size_t)(m + 1) * ldy + n] = float_to_bf16_bits(__uint_as_float((uint32_t)(acc[i] >> 32)));
+                if (m < M) {
+                    const uint16_t v16 = float_to_bf16_bits(__uint_as_float((uint32_t)acc[i]));
+                    y[(size_t)m * ldy + n] = v16;
+                    kv_store(kv, m, n, v16);
+                }
+                if (m + 1 < M) {
+                    const uint16_t v16 = float_to_bf16_bits(__uint_as_float((uint32_t)(acc[i] >> 32)));
+                    y[(size_t)(m + 1) * ldy + n] = v16;
+                    kv_store(kv, m + 1, n, v16);
+                }
             }
         }
     } else {
@@ -329,7 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (m >= M) break;
                     float sum = red[(size_t)t * kTileN + row];
                     for (int q = 1; q < C; ++q) sum += umma::ld_peer_f32(&red[(size_t)t * kTileN + row], (uint32_t)q);
-                    y[(size_t)m * ldy + n] = float_to_bf16_bits(sum);
+                    const uint16_t v16 = float_to_bf16_bits(sum);
+                    y[(size_t)m * ldy + n] = v16;
+                    kv_store(kv, m, n, v16);
                 }
             }
         }
@@ -341,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN>
 int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
-              uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall) {
+              uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall,
+              const KvOut &kv) {
     static_assert(sizeof(float) * BN * kTileN <= sizeof(Smem<BN>::a) + sizeof(Smem<BN>::b),
                   "partials fit in the operand stages");
     const size_t smem = sizeof(Smem<BN>) + 1024;
@@ -355,20 +365,21 @@ int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t 
     dim3 grid((unsigned)(n_tiles * C), (unsigned)token_tiles);
     if (C == 1)
         return launch_pdl("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, x, ldx,
-                          packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall);
+                          packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
     return launch_pdl_cluster("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, C, x,
-                              ldx, packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall);
+                              ldx, packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
 }
 
 }  // namespace
 
 // Large-M W4A16: token tile 32, 64, 96 or 128 (larger M: several token tiles).
 int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
-                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall) {
-    if (M <= 32) return launch_bn<32>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall);
-    if (M <= 64) return launch_bn<64>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall);
-    if (M <= 96) return launch_bn<96>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall);
-    return launch_bn<128>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall);
+                    uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall,
+                    const KvOut &kv) {
+    if (M <= 32) return launch_bn<32>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+    if (M <= 64) return launch_bn<64>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+    if (M <= 96) return launch_bn<96>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+    return launch_bn<128>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
 }
 
 }  // namespace qspec

@@ -72,3 +72,94 @@ def test_kv_overwrite_llama_cache_full_size():
     mask = ~touched[None, :, None, :, None].expand_as(kc)
     assert torch.equal(kc.view(torch.int16)[mask], k0.view(torch.int16)[mask])
     assert torch.equal(vc.view(torch.int16)[mask], v0.view(torch.int16)[mask])
+
+
+# ----------------------------------------------------------------- a4 + a7: the k/v projection
+# writing the cache from its epilogue (qspec_linear_w4a16_kv)
+def _expected_caches(kc, vc, ref, B, gamma, H, D, c0, base, nacc):
+    """The oracle's caches: the oracle's W4A16 values (fp64, rounded to bf16)
+    of the K and V columns, placed by the oracle's KV overwrite."""
+    M = B * (gamma + 1)
+    rows = torch.from_numpy(ref).to(torch.bfloat16)                      # [M][N]
+    kn = rows[:, c0:c0 + H * D].reshape(1, B, gamma + 1, H, D)
+    vn = rows[:, c0 + H * D:c0 + 2 * H * D].reshape(1, B, gamma + 1, H, D)
+    ko, vo = bits(kc).copy()[None], bits(vc).copy()[None]               # one layer
+    assert oracle.kv_overwrite(ko, vo, bits(kn), bits(vn), base, nacc, gamma) == 0
+    return ko[0], vo[0]
+
+
+# (B, gamma, K): 15 verify rows (the small-M kernel) and 80 rows (the tensor-core kernel);
+# n_acc given, or unknown (all gamma + 1 rows written)
+@pytest.mark.parametrize("B,gamma,K,given", [(3, 4, 1024, True), (3, 4, 1024, False), (16, 4, 2048, True),
+                                             (16, 4, 2048, False), (2, 7, 512, True)])
+def test_w4a16_kv_epilogue_matches_oracle(B, gamma, K, given):
+    from gpuhelp import W4A16_RTOL
+    dev = need_gpu()
+    H, D, T, c0 = 2, 128, 96, 384
+    N = c0 + 2 * H * D
+    M = B * (gamma + 1)
+    codes, s, z = syn.weights(N, K, 21 + B)
+    packed, sz = q.pack_weights(codes.to(dev), s.to(dev), z.to(dev))
+    rc, po, szo = oracle.pack_weights(codes.numpy(), bits(s), bits(z))
+    x = syn.activations(M, K, 22 + B, outlier_frac=0.01)
+    kc, vc = syn.kv_cache(1, B, H, T, D, 23)
+    kc, vc = kc[0].contiguous(), vc[0].contiguous()                    # [B][H][T][D]
+    base = syn.base_positions(B, T, gamma, 24)
+    nacc = torch.from_numpy(np.random.default_rng(B).integers(0, gamma + 1, B).astype(np.int32))
+    kcd, vcd = kc.to(dev), vc.to(dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    st = status(dev)
+    rc = q.qspec_linear_w4a16_kv(x.to(dev), K, packed, sz, M, N, K, y, N, c0, H, D, T, gamma, kcd, vcd,
+                                 base.to(dev), nacc.to(dev) if given else None, st)
+    assert rc == q.OK and read_status(st) == 0
+    ref = oracle.linear_w4a16(bits(x), po, szo)
+    # y as the plain W4A16 linear
+    got = y.float().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= W4A16_RTOL * (1 + np.abs(ref)))
+    written = nacc.numpy() if given else np.full(B, gamma, np.int32)
+    ko, vo = _expected_caches(kc, vc, ref, B, gamma, H, D, c0, base.numpy(), written)
+    for cache_gpu, cache_orc, col in ((kcd, ko, c0), (vcd, vo, c0 + H * D)):
+        g = bits(cache_gpu)
+        touched = np.zeros(g.shape, bool)
+        for b in range(B):
+            touched[b, :, base[b]:base[b] + written[b] + 1, :] = True
+        # untouched positions: bit for bit the old cache (the oracle's copy of it)
+        assert np.array_equal(g[~touched], cache_orc[~touched])
+        # written positions: the W4A16 tolerance against the oracle's values,
+        # and exactly the call's own outputs (placement)
+        gv = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).float().numpy()
+        for b in range(B):
+            for r in range(written[b] + 1):
+                m = b * (gamma + 1) + r
+                refr = ref[m, col:col + H * D].reshape(H, D)
+                sl = gv[b, :, base[b] + r, :]
+                assert np.all(np.abs(sl - refr) <= W4A16_RTOL * (1 + np.abs(refr)))
+                assert np.array_equal(g[b, :, base[b] + r, :],
+                                      bits(y[m, col:col + H * D].reshape(H, D)))
+
+
+def test_w4a16_kv_epilogue_range():
+    dev = need_gpu()
+    B, gamma, K, H, D, T, c0 = 2, 3, 256, 1, 64, 16, 0
+    N = 2 * H * D
+    M = B * (gamma + 1)
+    codes, s, z = syn.weights(N, K, 31)
+    packed, sz = q.pack_weights(codes.to(dev), s.to(dev), z.to(dev))
+    x = syn.activations(M, K, 32).to(dev)
+    kc, vc = syn.kv_cache(1, B, H, T, D, 33)
+    kcd, vcd = kc[0].contiguous().to(dev), vc[0].contiguous().to(dev)
+    before = bits(kcd).copy()
+    base = torch.tensor([13, 2], dtype=torch.int32, device=dev)        # 13 + 3 >= 16: sequence 0 out of range
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    st = status(dev)
+    rc = q.qspec_linear_w4a16_kv(x, K, packed, sz, M, N, K, y, N, c0, H, D, T, gamma, kcd, vcd, base, None, st)
+    assert rc == q.OK and read_status(st) == q.ERR_RANGE
+    after = bits(kcd)
+    assert np.array_equal(after[0], before[0])                        # untouched
+    assert not np.array_equal(after[1, :, 2:6], before[1, :, 2:6])    # written
+    # host checks: M not a multiple of gamma + 1, columns past N
+    one = torch.zeros(1, dtype=torch.int32, device=dev)
+    assert q.qspec_linear_w4a16_kv(x, K, packed, sz, M - 1, N, K, y, N, c0, H, D, T, gamma, kcd, vcd, base, None,
+                                   None) == q.ERR_SHAPE
+    assert q.qspec_linear_w4a16_kv(x, K, packed, sz, M, N, K, y, N, 1, H, D, T, gamma, kcd, vcd, base, None,
+                                   None) == q.ERR_SHAPE
