@@ -92,7 +92,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rounds", type=int, default=16, help="distinct captured rounds (RNG round ids)")
     ap.add_argument("--profile-case", choices=["w4a4_m1", "w4a16_m5", "w4a16_m80", "quant", "verify_sample",
-                                               "verify_greedy", "kv"],
+                                               "verify_greedy", "kv", "fp8_m5", "w4a4_m4096"],
                     help="run one kernel a few times on a single LM-head-sized case (for ncu)")
     ap.add_argument("--profile-reps", type=int, default=3)
     return ap.parse_args()
@@ -119,6 +119,23 @@ def profile_case(name, reps):
                 q.linear_w4a16(x, packed, sz)
             else:
                 q.quant_act_int4(syn.activations(4096, 14336, 7, device=dev))
+    elif name == "fp8_m5":
+        # the Q8 (FP8) verify linear on the 128256 x 4096 LM head at M = 5
+        g = torch.Generator(device=dev).manual_seed(5)
+        w16 = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.float16)
+        w8, s8 = q.quant_weights_fp8(w16)
+        del w16
+        xq, sa = q.quant_act_fp8(syn.activations(5, K, 6, device=dev, outlier_frac=0.01))
+        for _ in range(reps):
+            q.linear_fp8(xq, sa, w8, s8)
+    elif name == "w4a4_m4096":
+        # W4A4 at M = 4096 through the stacked gate/up projection (4096 -> 28672)
+        codes, s, z = syn.weights(28672, 4096, 40, device=dev)
+        packed, sz = q.pack_weights(codes, s, z)
+        del codes
+        xq, sx, qs = q.quant_act_int4(syn.activations(4096, 4096, 50, device=dev))
+        for _ in range(reps):
+            q.linear_w4a4(xq, sx, qs, packed, sz)
     elif name in ("verify_sample", "verify_greedy"):
         P, Q, d = syn.logits_noisy_draft(256, 4, 128256, 4, device=dev)
         ws = q.verify_workspace(256, 4, 128256, dev)
@@ -694,7 +711,25 @@ class OracleRound:
         return int((n_acc + 1).sum()), t_round, sampled
 
 
+def cpu_model():
+    """The host CPU's model string, from /proc/cpuinfo (or lscpu)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(wl, steps=3):
+    """The oracle on the host cores (all of them, then one thread) on a
+    bounded sample of the round, extrapolated to the whole round."""
     import oracle
     orc = OracleRound(wl)
     orc.step(0)
@@ -702,11 +737,19 @@ def cpu_baseline(wl, steps=3):
     for r in range(steps):
         k, t, s = orc.step(r)
         tok, tsum, sampled = tok + k, tsum + t, sampled + s
-    return {"value": tok / tsum, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+    cores = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        k1, t1, s1 = orc.step(steps)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": tok / tsum, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(), "single_thread_value": k1 / t1,
             "sample": ("%d rounds; per round 1 of %d layers (draft and verify linears), LM head "
                        "%d of %d rows, full verification and 1-layer KV overwrite, extrapolated "
-                       "to the full round; %.1f s of oracle time measured"
-                       % (steps, orc.L, orc.lm_rows, orc.V, sampled))}
+                       "to the full round; %.1f s of oracle time measured on %d threads, then one "
+                       "round on 1 thread (%.1f s)"
+                       % (steps, orc.L, orc.lm_rows, orc.V, sampled, cores, s1))}
 
 
 # ---------------------------------------------------------------------------
@@ -805,7 +848,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights; u64/u128 sums",
                 "data": "synthetic", "config": cfg,
                 "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(),
-                                 "kind": "oracle",
+                                 "kind": "oracle", "cpu_model": cpu_model(),
                                  "sample": "per step 1 of %d layers, LM head %d of %d rows, full "
                                            "verification; %.1f s of oracle time in total"
                                            % (orc.L, orc.lm_rows, orc.V, sampled)},

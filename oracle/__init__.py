@@ -107,6 +107,8 @@ def _load():
         lib.orc_kv_overwrite.restype = I
         lib.orc_num_threads.argtypes = []
         lib.orc_num_threads.restype = I
+        lib.orc_set_num_threads.argtypes = [I]
+        lib.orc_set_num_threads.restype = None
         lib.orc_e4m3_value.argtypes = [u8]
         lib.orc_e4m3_value.restype = f64
         lib.orc_e4m3_from_float.argtypes = [f32]
@@ -121,6 +123,11 @@ def _load():
         lib.orc_linear_fp8.restype = None
         _lib = lib
         return lib
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's later OpenMP loops."""
+    _load().orc_set_num_threads(int(n))
 
 
 def num_threads() -> int:

@@ -749,3 +749,10 @@ void orc_linear_fp8(const uint8_t *xq, const float *sa, const uint8_t *w8, const
             ref[(size_t)m * N + n] = acc * (double)sa[m] * (double)s8[n];
         }
 }
+
+/* threads for the oracle's later OpenMP regions (the CPU baseline measures
+ * all host cores and one) */
+void orc_set_num_threads(int n)
+{
+    omp_set_num_threads(n > 0 ? n : 1);
+}

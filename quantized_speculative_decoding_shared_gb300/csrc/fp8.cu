@@ -20,7 +20,9 @@
 // first stages before the dependency wait, the weights being immutable --
 // warp 5 (one lane) issues 4 MMAs kind::f8f6f4 (M = 128, N = BN, K = 32) per
 // stage into one fp32 accumulator in tensor memory, and warps 0-3 (thread =
-// TMEM lane = output channel) scale and store it at the end.  Every wait is
+// TMEM lane = output channel) scale and store it at the end.  A CTA uses at
+// most ~110 KB of shared memory and BN (>= 32) tensor-memory columns, so two
+// share an SM and one's start and end overlap the other's streaming.  Every wait is
 // bounded (QSPEC_ERR_TIMEOUT on expiry, then a drain and a clean exit).
 #include <algorithm>
 #include <cuda_fp8.h>
@@ -106,7 +108,7 @@ constexpr int kTileN = 128;                 // output channels per CTA (MMA M)
 constexpr int kKB = 128;                    // K per stage: 128 E4M3 bytes
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kSmemBudget = 110 * 1024;   // two CTAs per SM: one's start and end overlap the other's stream
 
 // shared-memory descriptor of a K-major operand in the 128-byte swizzled
 // layout: start address, leading offset unused (16 bytes), stride 1024 bytes
@@ -124,7 +126,7 @@ template <int BN>
 constexpr int stage_bytes() { return kTileN * kKB + BN * kKB; }
 
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     fp8_umma_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
                     const float *__restrict__ sa, const float *__restrict__ s8, int M, int N, int K,
                     uint16_t *__restrict__ y, int ldy, int32_t *__restrict__ st, int S, uint32_t wait_limit) {
