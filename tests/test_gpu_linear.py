@@ -334,3 +334,32 @@ def test_w4a16_lm_head_m5():
     """The 128256 x 4096 LM head at M = gamma + 1 = 5."""
     dev = need_gpu()
     sampled_compare([5], [("lm_head", 128256, 4096)], 9, dev, outliers=0.01, w4a4=False, points=1024)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [1, 5, 8, 16])
+def test_w4a16_small_m_token_scales(M):
+    """Tokens whose magnitudes span the bf16 range -- beyond the f16 range
+    (2^40), far below it (2^-40), an all-zero token and ordinary ones -- in
+    one call: each token's result, relative to its own scale, within the
+    W4A16 tolerance of the oracle, and the zero token exactly zero."""
+    dev = need_gpu()
+    N, K = 272, 1024
+    packed, sz, po, szo = make_layer(N, K, 31, dev)
+    x = syn.activations(M, K, 77, outlier_frac=0.01).float()
+    exps = [40, -40, 0, 12, -12, 0, 20, -20][:M] + [0] * max(0, M - 8)
+    for t in range(M):
+        x[t] *= 2.0 ** exps[t]
+    if M > 2:
+        x[2] = 0.0
+    x = x.to(torch.bfloat16)
+    st = status(dev)
+    y16 = q.linear_w4a16(x.to(dev), packed, sz, dev_status=st)
+    assert read_status(st) == 0
+    got = y16.float().cpu().numpy()
+    ref = oracle.linear_w4a16(bits(x), po, szo)
+    for t in range(M):
+        sc = 2.0 ** -exps[t]
+        assert_w4a16_close(got[t] * sc, ref[t] * sc, "w4a16 M=%d token %d (scale 2^%d)" % (M, t, exps[t]))
+    if M > 2:
+        assert not got[2].any()
