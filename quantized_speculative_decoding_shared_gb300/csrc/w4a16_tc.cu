@@ -11,29 +11,35 @@
 // 128-wide group into a TMEM accumulator in fp32; the epilogue applies the
 // group's scale, y += s * D_g, in fp32 registers.
 //
+// Both operands sit in shared memory in the K-major layout with 128-byte
+// swizzle (rows of 64 bf16; 8-row groups 1024 bytes apart; the 16-byte chunk
+// j of row r stored at position j ^ (r % 8)), which the MMA reads directly:
+//   - the activations arrive by TMA, two boxes of BN tokens x 64 k per group,
+//     in their natural k order;
+//   - the weights are converted by 8 warps, two threads per output channel,
+//     each 64 k of a group: a code byte (c_2j in the low nibble, c_2j+1 in
+//     the high one) times 0x1001 puts the two codes 16 bits apart, OR-ed into
+//     the mantissa of 128.0 they give the bf16 pair (128 + c_2j, 128 + c_2j+1)
+//     exactly, and one exact bf16 subtraction of 128 + z leaves (c - z).
 // One CTA computes a 128 (output channels) x BN (tokens) tile of Y^T:
-//   warps 0-3  producers: per group, the packed codes of one channel each ->
-//              bf16 (c - z) (the code OR-ed into the mantissa of 128.0 gives
-//              128 + c exactly, then an exact subtraction of 128 + z), and
-//              the activation rows; both in shared memory in the no-swizzle
-//              K-major core-matrix layout, with k permuted within each 8-wide
-//              chunk identically on both operands (a dot product does not
-//              depend on the order of k)
-//   warps 4-11 epilogue, two warpgroups on the same TMEM lanes, each with half
-//              of the token columns: per group, TMEM -> registers,
-//              y = fma(D, s, y) in packed f32x2; finally bf16
-//   warp 12    issues 8 MMAs (K = 16) per group into one of two TMEM buffers
+//   warps 0-7   weight converters (the first groups' codes are loaded before
+//               the dependency wait: the weights are immutable)
+//   warps 8-15  epilogue, two warpgroups on the same TMEM lanes, each with
+//               half of the token columns: per group, TMEM -> registers,
+//               y = fma(D, s, y) in packed f32x2; finally bf16
+//   warp 16     issues 8 MMAs (K = 16) per group into one of two TMEM buffers
+//   warp 17     issues the activation boxes
 // When the 128-channel tiles alone would leave SMs idle, a cluster of up to 8
 // CTAs splits a tile's groups; each CTA keeps its fp32 partial sums, and
 // rank 0 reads its peers' partials from distributed shared memory, adds them
 // in rank order and stores bf16.
 // Bounded waits everywhere (the limit is a kernel argument; a test can also
 // make the MMA issuer wait on a barrier nothing arrives at).  After a
-// timeout (QSPEC_ERR_TIMEOUT) every role leaves its loop, the MMAs issued are
-// drained with a bounded wait, and the tensor memory is freed -- even if the
-// drain itself ran out (the next kernel on the SM would otherwise wait for it
-// without bound); in that case the split-K reduction, which reuses the
-// operand stages the MMAs read, is skipped.
+// timeout (QSPEC_ERR_TIMEOUT) every role leaves its loop, the activation
+// copies and the MMAs issued are drained with bounded waits, and the tensor
+// memory is freed -- even if a drain ran out (the next kernel on the SM would
+// otherwise wait for it without bound); in that case the split-K reduction,
+// which reuses the operand stages, is skipped.
 #include <algorithm>
 
 #include "qspec_device.cuh"
@@ -44,29 +50,48 @@ namespace qspec {
 
 namespace {
 
-constexpr int kStages = 3;
 constexpr int kTileN = 128;              // output channels per CTA (MMA M)
-constexpr int kKB = kGroup * 2;          // bytes of K per row per stage (bf16)
-constexpr int kProducers = 128;
+constexpr int kAtom = 128;               // bytes of K per swizzle atom row (64 bf16)
+constexpr int kConv = 256;               // converter threads: two per channel
 constexpr int kEpilogue = 256;
-constexpr int kThreads = kProducers + kEpilogue + 32;
+constexpr int kMmaWarp = (kConv + kEpilogue) / 32, kTmaWarp = kMmaWarp + 1;
+constexpr int kThreads = kConv + kEpilogue + 64;
+constexpr int kA = kTileN * 2 * kAtom;   // A bytes per stage (one group: two atoms)
+
+template <int BN>
+constexpr int stage_bytes() { return kA + BN * 2 * kAtom; }
+template <int BN>
+constexpr int n_stages() { return std::min(4, (200 * 1024) / stage_bytes<BN>()); }
 
 __device__ __forceinline__ uint32_t bf2_sub(uint32_t a, uint32_t b) {
     __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// eight codes of a word -> bf16 (c - z) in the order k0,k4,k1,k5,k2,k6,k3,k7
-__device__ __forceinline__ uint4 codes_minus_z(uint32_t w, uint32_t zz) {
-    const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;   // bf16 128 + c
-    return make_uint4(bf2_sub((w & mask) | magic, zz), bf2_sub(((w >> 4) & mask) | magic, zz),
-                      bf2_sub(((w >> 8) & mask) | magic, zz), bf2_sub(((w >> 12) & mask) | magic, zz));
+// one code byte (c_2j low nibble, c_2j+1 high) -> bf16 pair (c_2j - z, c_2j+1 - z)
+__device__ __forceinline__ uint32_t pair_minus_z(uint32_t b, uint32_t zz) {
+    const uint32_t t = b * 0x1001u;                        // low nibble at bits 0-3, high at 16-19
+    return bf2_sub((t & 0x000F000Fu) | 0x43004300u, zz);   // (128 + c) - (128 + z), exact
+}
+// eight codes of a word (k = 0..7) -> 16 bytes of bf16 (c - z), natural k order
+__device__ __forceinline__ uint4 word_minus_z(uint32_t w, uint32_t zz) {
+    return make_uint4(pair_minus_z(w & 0xFFu, zz), pair_minus_z((w >> 8) & 0xFFu, zz),
+                      pair_minus_z((w >> 16) & 0xFFu, zz), pair_minus_z(w >> 24, zz));
 }
 
-// eight bf16 activations x0..x7 -> the same order
-__device__ __forceinline__ uint4 acts_permuted(uint4 v) {
-    return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632), __byte_perm(v.y, v.w, 0x5410),
-                      __byte_perm(v.y, v.w, 0x7632));
+// K-major 128-byte-swizzle descriptor: start address, leading offset unused
+// (16 bytes), 1024 bytes between 8-row groups, version 1, swizzle mode 2
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// byte offset of (row, 16-byte chunk) in a 128-byte-swizzled atom
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
+    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -79,10 +104,8 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 }
 
 template <int BN>
-struct Smem {
-    uint8_t a[kStages][kTileN * kKB];
-    uint8_t b[kStages][BN * kKB];
-    uint64_t full[kStages], empty[kStages], accf[2], acce[2];
+struct Ctl {
+    uint64_t full[4], bfull[4], empty[4], accf[2], acce[2];   // full: weights converted; bfull: activations landed
     uint64_t drain;                    // after a timeout: the MMAs in flight have finished
     uint64_t never;                    // nothing arrives here (the stall test)
     uint32_t tmem;
@@ -91,12 +114,20 @@ struct Smem {
 };
 
 template <int BN>
+constexpr size_t smem_total() { return (size_t)n_stages<BN>() * stage_bytes<BN>() + sizeof(Ctl<BN>) + 1024; }
+
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    w4a16_umma_kernel(const uint16_t *__restrict__ x, int ldx, const uint8_t *__restrict__ packed,
+    w4a16_umma_kernel(const __grid_constant__ CUtensorMap tx, const uint8_t *__restrict__ packed,
                       const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
                       int32_t *st, int C, uint32_t wait_limit, int stall, KvOut kv) {
+    constexpr int S = n_stages<BN>();
+    constexpr int kStage = stage_bytes<BN>();
+    static_assert(BN % 16 == 0 && BN >= 32 && BN <= 128, "token tile");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    Smem<BN> &sm = *reinterpret_cast<Smem<BN> *>(smem_raw);
+    // stages 1024-aligned (the swizzle pattern is a function of the address)
+    uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctl<BN> &sm = *reinterpret_cast<Ctl<BN> *>(stages + (size_t)S * kStage);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // cluster of C CTAs splits the groups of one 128-channel tile
     const int rank = C > 1 ? (int)umma::cluster_rank() : 0;
@@ -109,8 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem, kCols);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            umma::mbar_init(&sm.full[s], kProducers);
+        for (int s = 0; s < S; ++s) {
+            umma::mbar_init(&sm.full[s], kConv);
+            umma::mbar_init(&sm.bfull[s], 1);
             umma::mbar_init(&sm.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -123,104 +155,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.drained = 1;
         umma::mbar_fence_init();
     }
+    if (warp == kTmaWarp && lane == 0) umma::prefetch_tmap(&tx);
     pdl_launch_dependents();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem;
     bool issued = false;                          // MMAs issued (MMA lane 0)
+    int copies = 0;                               // groups whose activation boxes were issued (copy lane 0)
     auto timed_out = [&]() { return *reinterpret_cast<volatile int *>(&sm.timeout) != 0; };
     // epilogue partial sums: per thread (row n, token half) BN / 2 values
     constexpr int kHalf = BN / 2;
     uint64_t acc[kHalf / 2];
     bool epi_ok = false;
 
-    if (warp < 4) {
-        // ------------------------------------------------------------ producers
-        // weights: kD groups in flight per thread (one row each); activations
-        // of a group: all of a thread's chunks loaded before any is stored
-        constexpr int kD = 2;
-        constexpr int kChunks = BN * 16 / kProducers;  // 16-byte activation chunks per thread per group
-        const int r = tid, n = n0 + r;
+    if (warp < kConv / 32) {
+        // ------------------------------------------------------ weight converters
+        // thread: channel r = tid / 2, k half h = tid % 2 (atom h of each
+        // group); kD groups of codes in flight per thread
+        constexpr int kD = 3;
+        const int r = tid >> 1, h = tid & 1, n = n0 + r;
         const bool row_ok = n < N;
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(packed + (size_t)(row_ok ? n : 0) * (K / 2));
-        uint4 ring[kD][4];
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(packed + (size_t)(row_ok ? n : 0) * (K / 2)) + 2 * h;
+        uint4 ring[kD][2];
         uint32_t zring[kD];
 #pragma unroll
         for (int p = 0; p < kD; ++p) {
             const int g = g_lo + p;
             if (g < g_hi) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) ring[p][u] = __ldg(wrow + (size_t)g * 4 + u);
+                ring[p][0] = __ldg(wrow + (size_t)g * 4);
+                ring[p][1] = __ldg(wrow + (size_t)g * 4 + 1);
                 zring[p] = row_ok ? __ldg(sz + (size_t)n * G + g) : 0u;
             }
         }
-        pdl_wait();
         bool ok = true;
         for (int lb = 0; lb < NG && ok; lb += kD) {
 #pragma unroll
             for (int p = 0; p < kD; ++p) {
                 const int l = lb + p, g = g_lo + l;
                 if (l >= NG) break;
-                const int s = l % kStages;
-                if (l >= kStages &&
-                    (timed_out() || !umma::mbar_wait(&sm.empty[s], ((l / kStages) - 1) & 1, wait_limit))) {
+                const int s = l % S;
+                if (l >= S &&
+                    (timed_out() || !umma::mbar_wait(&sm.empty[s], ((l / S) - 1) & 1, wait_limit))) {
                     atomicExch(&sm.timeout, 1);
                     ok = false;
                     break;
                 }
-                uint4 cw[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) cw[u] = ring[p][u];
+                const uint4 c0 = ring[p][0], c1 = ring[p][1];
                 const uint32_t szc = zring[p];
                 if (l + kD < NG) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) ring[p][u] = __ldg(wrow + (size_t)(g + kD) * 4 + u);
+                    ring[p][0] = __ldg(wrow + (size_t)(g + kD) * 4);
+                    ring[p][1] = __ldg(wrow + (size_t)(g + kD) * 4 + 1);
                     zring[p] = row_ok ? __ldg(sz + (size_t)n * G + g + kD) : 0u;
                 }
                 const uint32_t zb =
                     float_to_bf16_bits(128.0f + __half2float(__ushort_as_half((uint16_t)(szc >> 16))));
                 const uint32_t zz = zb | (zb << 16);
-                // weights: 128 codes of row r -> 16 chunks of 8 bf16
-                uint8_t *a = sm.a[s];
+                // 64 codes of row r (k = 64 h ..) -> 8 chunks of 8 bf16 in atom h
+                uint8_t *a = stages + (size_t)s * kStage + (size_t)h * (kTileN * kAtom);
+                const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t words[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 v = row_ok ? codes_minus_z(words[q], zz) : make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(a + umma::core_offset(r, 4 * u + q, kKB)) = v;
-                    }
-                }
-                // this group's activation chunks, in batches: loads first
-                uint8_t *b = sm.b[s];
-                constexpr int kBatch = kChunks % 8 == 0 ? 8 : kChunks % 6 == 0 ? 6 : 4;
-                static_assert(kChunks % kBatch == 0, "batches cover the chunks exactly");
-#pragma unroll
-                for (int j0 = 0; j0 < kChunks; j0 += kBatch) {
-                    uint4 av[kBatch];
-#pragma unroll
-                    for (int j = 0; j < kBatch; ++j) {
-                        const int c = tid + (j0 + j) * kProducers, t = c >> 4, jj = c & 15, m = t0 + t;
-                        av[j] = m < M ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)m * ldx +
-                                                                              (size_t)g * kGroup + jj * 8))
-                                      : make_uint4(0, 0, 0, 0);
-                    }
-#pragma unroll
-                    for (int j = 0; j < kBatch; ++j) {
-                        const int c = tid + (j0 + j) * kProducers, t = c >> 4, jj = c & 15;
-                        *reinterpret_cast<uint4 *>(b + umma::core_offset(t, jj, kKB)) = acts_permuted(av[j]);
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 v = row_ok ? word_minus_z(words[j], zz) : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(a + sw128_offset(r, j)) = v;
                 }
                 umma::fence_proxy_async();
                 umma::mbar_arrive(&sm.full[s]);
             }
         }
-    } else if (warp < 12) {
+    } else if (warp < kMmaWarp) {
         // ------------------------------------------------------------ epilogue
         pdl_wait();
-        constexpr int kW = kHalf % 32 == 0 ? 32 : 16;
-        const int eq = warp & 3, eh = (warp - 4) >> 2;
+        constexpr int kW = kHalf % 16 == 0 ? 16 : 8;
+        const int eq = warp & 3, eh = (warp - kConv / 32) >> 2;
         const int n = n0 + eq * 32 + lane;
         const bool row_ok = n < N;
 #pragma unroll
@@ -241,12 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::fence_after_sync();
 #pragma unroll
             for (int c0 = 0; c0 < kHalf; c0 += kW) {
-                uint32_t v[32];
+                uint32_t v[kW];
                 const uint32_t ta = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(buf * kBuf + eh * kHalf + c0);
-                if (kW == 32)
-                    umma::tmem_ld32(ta, *reinterpret_cast<uint32_t(*)[32]>(v));
-                else
-                    umma::tmem_ld16(ta, v);
+                umma::tmem_ld_cols<kW>(ta, *reinterpret_cast<uint32_t(*)[kW]>(v));
                 umma::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < kW; j += 2)
@@ -272,27 +276,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        pdl_wait();
         if (lane == 0) {
             constexpr uint32_t idesc = umma::instr_desc(1, 1, kTileN, BN);
             if (stall && !umma::mbar_wait(&sm.never, 0, wait_limit)) atomicExch(&sm.timeout, 1);
             for (int l = 0; l < NG; ++l) {
-                const int s = l % kStages, buf = l & 1;
-                if (timed_out() || !umma::mbar_wait(&sm.full[s], (l / kStages) & 1, wait_limit) ||
+                const int s = l % S, buf = l & 1;
+                if (timed_out() || !umma::mbar_wait(&sm.full[s], (l / S) & 1, wait_limit) ||
+                    !umma::mbar_wait(&sm.bfull[s], (l / S) & 1, wait_limit) ||
                     (l >= 2 && !umma::mbar_wait(&sm.acce[buf], ((l >> 1) - 1) & 1, wait_limit))) {
                     atomicExch(&sm.timeout, 1);
                     break;
                 }
                 umma::fence_after_sync();
-                const uint32_t a0 = umma::smem_addr(sm.a[s]), b0 = umma::smem_addr(sm.b[s]);
+                const uint32_t a0 = umma::smem_addr(stages + (size_t)s * kStage), b0 = a0 + kA;
                 const uint32_t d = tmem + (uint32_t)(buf * kBuf);
 #pragma unroll
-                for (int j = 0; j < kKB / 32; ++j) {       // K = 16 bf16 = 2 core matrices per MMA
-                    const uint64_t da = umma::smem_desc(a0 + j * 256, 128, (kKB / 16) * 128);
-                    const uint64_t db = umma::smem_desc(b0 + j * 256, 128, (kKB / 16) * 128);
-                    umma::mma_bf16(d, da, db, idesc, j != 0);
+                for (int h = 0; h < 2; ++h) {
+                    const uint64_t da = desc_sw128(a0 + h * kTileN * kAtom), db = desc_sw128(b0 + h * BN * kAtom);
+#pragma unroll
+                    for (int kk = 0; kk < kAtom / 32; ++kk)   // K = 16 bf16 = 32 bytes: +2 in the address field
+                        umma::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (h | kk) != 0 ? 1u : 0u);
                 }
                 umma::mma_commit(&sm.empty[s]);
                 umma::mma_commit(&sm.accf[buf]);
@@ -300,13 +305,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else {
+        // ------------------------------------------------------------ activation copies
+        pdl_wait();
+        if (lane == 0) {
+            for (int l = 0; l < NG; ++l) {
+                const int s = l % S, g = g_lo + l;
+                if (l >= S && (timed_out() || !umma::mbar_wait(&sm.empty[s], ((l / S) - 1) & 1, wait_limit))) {
+                    atomicExch(&sm.timeout, 1);
+                    break;
+                }
+                uint8_t *b = stages + (size_t)s * kStage + kA;
+                umma::mbar_arrive_expect_tx(&sm.bfull[s], (uint32_t)(BN * 2 * kAtom));
+                umma::tma_load_2d(b, &tx, g * 2 * kAtom, t0, &sm.bfull[s]);
+                umma::tma_load_2d(b + BN * kAtom, &tx, g * 2 * kAtom + kAtom, t0, &sm.bfull[s]);
+                copies = l + 1;
+            }
+        }
+        __syncwarp();
     }
     umma::fence_before_sync();
     __syncthreads();
-    // after a timeout, the MMAs already issued finish (bounded wait) before
-    // the TMEM they write is freed; sm.timeout is settled at this barrier
+    // after a timeout, the copies and MMAs already issued finish (bounded
+    // waits) before the shared and tensor memory are released; sm.timeout is
+    // settled at this barrier
     if (sm.timeout) {
-        if (warp == kThreads / 32 - 1 && lane == 0 && issued) {
+        if (warp == kTmaWarp && lane == 0)
+            for (int l = std::max(0, copies - S); l < copies; ++l)
+                if (!umma::mbar_wait(&sm.bfull[l % S], (l / S) & 1, kWaitLimit)) sm.drained = 0;
+        if (warp == kMmaWarp && lane == 0 && issued) {
             umma::mma_commit(&sm.drain);
             if (!umma::mbar_wait(&sm.drain, 0, kWaitLimit)) sm.drained = 0;
         }
@@ -314,12 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (C > 1) {
         // split groups: every CTA's partials -> its shared memory (the operand
-        // stages are free now: all MMAs have completed); rank 0 adds them in
-        // rank order and stores bf16
-        float *red = reinterpret_cast<float *>(smem_raw);          // [BN tokens][128 channels]
-        const int eq = warp & 3, eh = (warp - 4) >> 2, row = eq * 32 + lane;
+        // stages are free now: all copies and MMAs have completed); rank 0
+        // adds them in rank order and stores bf16
+        float *red = reinterpret_cast<float *>(stages);            // [BN tokens][128 channels]
+        const int eq = warp & 3, eh = (warp - kConv / 32) >> 2, row = eq * 32 + lane;
+        const bool epi_warp = warp >= kConv / 32 && warp < kMmaWarp;
         const bool reuse = sm.drained != 0;                        // the operand stages are free
-        if (warp >= 4 && warp < 12 && reuse) {
+        if (epi_warp && reuse) {
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {
                 const int t = eh * kHalf + 2 * i;
@@ -328,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         umma::cluster_sync();
-        if (rank == 0 && warp >= 4 && warp < 12 && reuse && !sm.timeout) {
+        if (rank == 0 && epi_warp && reuse && !sm.timeout) {
             const int n = n0 + row;
             if (n < N) {
                 for (int t = eh * kHalf; t < eh * kHalf + kHalf; ++t) {
@@ -352,9 +380,12 @@ template <int BN>
 int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
               uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall,
               const KvOut &kv) {
-    static_assert(sizeof(float) * BN * kTileN <= sizeof(Smem<BN>::a) + sizeof(Smem<BN>::b),
+    static_assert(sizeof(float) * BN * kTileN <= (size_t)n_stages<BN>() * stage_bytes<BN>(),
                   "partials fit in the operand stages");
-    const size_t smem = sizeof(Smem<BN>) + 1024;
+    CUtensorMap tx;
+    // the activations as bytes: rows of K bf16, boxes of 128 bytes x BN tokens
+    if (byte_tmap_sw128(&tx, x, M, 2 * K, (size_t)ldx * 2, BN)) return QSPEC_ERR_UNSUPPORTED;
+    const size_t smem = smem_total<BN>();
     int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a16_umma_kernel<BN>), (int)smem);
     if (rc) return rc;
     const int n_tiles = (N + kTileN - 1) / kTileN, token_tiles = (M + BN - 1) / BN, G = K / kGroup;
@@ -364,22 +395,29 @@ int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t 
     while (C < 8 && n_tiles * token_tiles * C * 2 <= sm_count() && 2 * C * 2 <= G) C *= 2;
     dim3 grid((unsigned)(n_tiles * C), (unsigned)token_tiles);
     if (C == 1)
-        return launch_pdl("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, x, ldx,
+        return launch_pdl("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, tx,
                           packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
-    return launch_pdl_cluster("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, C, x,
-                              ldx, packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
+    return launch_pdl_cluster("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, C, tx,
+                              packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
 }
 
 }  // namespace
 
-// Large-M W4A16: token tile 32, 64, 96 or 128 (larger M: several token tiles).
+// Large-M W4A16: ceil(M / 128) token tiles of BN tokens (a multiple of 16,
+// 32 ... 128).
 int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t *sz, int M, int N, int K,
                     uint16_t *y, int ldy, int32_t *st, cudaStream_t stream, uint32_t wait_limit, int stall,
                     const KvOut &kv) {
-    if (M <= 32) return launch_bn<32>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
-    if (M <= 64) return launch_bn<64>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
-    if (M <= 96) return launch_bn<96>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
-    return launch_bn<128>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+    const int tiles = (M + 127) / 128, per = (M + tiles - 1) / tiles, bn = std::max(32, (per + 15) / 16 * 16);
+    switch (bn) {
+        case 32: return launch_bn<32>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+        case 48: return launch_bn<48>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+        case 64: return launch_bn<64>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+        case 80: return launch_bn<80>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+        case 96: return launch_bn<96>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+        case 112: return launch_bn<112>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+        default: return launch_bn<128>(x, ldx, packed, sz, M, N, K, y, ldy, st, stream, wait_limit, stall, kv);
+    }
 }
 
 }  // namespace qspec

@@ -363,3 +363,18 @@ def test_w4a16_small_m_token_scales(M):
         assert_w4a16_close(got[t] * sc, ref[t] * sc, "w4a16 M=%d token %d (scale 2^%d)" % (M, t, exps[t]))
     if M > 2:
         assert not got[2].any()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K,seed", [(17, 384, 1024, 80), (40, 256, 2048, 81), (100, 640, 1152, 82),
+                                        (129, 384, 1024, 83), (200, 272, 4096, 84), (64, 130, 14336, 85)])
+def test_w4a16_tensor_core_token_tiles(M, N, K, seed):
+    """W4A16 above 16 tokens: token tiles of 32, 48, 80, 112 and 64 tokens
+    (one or two per call, a ragged channel tail, long K), against the oracle."""
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100, outlier_frac=0.01)
+    st = status(dev)
+    y16 = q.linear_w4a16(x.to(dev), packed, sz, dev_status=st)
+    assert read_status(st) == 0
+    assert_w4a16_close(y16, oracle.linear_w4a16(bits(x), po, szo), "w4a16 M=%d N=%d K=%d" % (M, N, K))
