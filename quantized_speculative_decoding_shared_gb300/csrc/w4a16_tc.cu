@@ -16,19 +16,21 @@
 // j of row r stored at position j ^ (r % 8)), which the MMA reads directly:
 //   - the activations arrive by TMA, two boxes of BN tokens x 64 k per group,
 //     in their natural k order;
-//   - the weights are converted by 8 warps, two threads per output channel,
-//     each 64 k of a group: a code byte (c_2j in the low nibble, c_2j+1 in
+//   - the packed codes arrive by TMA too, 128 channels x 128 bytes (two
+//     groups) per box, into a ring of four boxes whose first entries go out
+//     before the dependency wait (the weights are immutable); 8 warps convert
+//     them, two threads per output channel, each 64 k of a group: a code byte
+//     (c_2j in the low nibble, c_2j+1 in
 //     the high one) times 0x1001 puts the two codes 16 bits apart, OR-ed into
 //     the mantissa of 128.0 they give the bf16 pair (128 + c_2j, 128 + c_2j+1)
 //     exactly, and one exact bf16 subtraction of 128 + z leaves (c - z).
 // One CTA computes a 128 (output channels) x BN (tokens) tile of Y^T:
-//   warps 0-7   weight converters (the first groups' codes are loaded before
-//               the dependency wait: the weights are immutable)
+//   warps 0-7   weight converters
 //   warps 8-15  epilogue, two warpgroups on the same TMEM lanes, each with
 //               half of the token columns: per group, TMEM -> registers,
 //               y = fma(D, s, y) in packed f32x2; finally bf16
 //   warp 16     issues 8 MMAs (K = 16) per group into one of two TMEM buffers
-//   warp 17     issues the activation boxes
+//   warp 17     lane 0 issues the code boxes, lane 1 the activation boxes
 // When the 128-channel tiles alone would leave SMs idle, a cluster of up to 8
 // CTAs splits a tile's groups; each CTA keeps its fp32 partial sums, and
 // rank 0 reads its peers' partials from distributed shared memory, adds them
@@ -57,11 +59,13 @@ constexpr int kEpilogue = 256;
 constexpr int kMmaWarp = (kConv + kEpilogue) / 32, kTmaWarp = kMmaWarp + 1;
 constexpr int kThreads = kConv + kEpilogue + 64;
 constexpr int kA = kTileN * 2 * kAtom;   // A bytes per stage (one group: two atoms)
+constexpr int kCodeBox = kTileN * kAtom; // packed codes of two groups for 128 channels
+constexpr int kSC = 4;                   // code boxes in the ring
 
 template <int BN>
 constexpr int stage_bytes() { return kA + BN * 2 * kAtom; }
 template <int BN>
-constexpr int n_stages() { return std::min(4, (200 * 1024) / stage_bytes<BN>()); }
+constexpr int n_stages() { return std::min(3, (212 * 1024 - kSC * kCodeBox) / stage_bytes<BN>()); }
 
 __device__ __forceinline__ uint32_t bf2_sub(uint32_t a, uint32_t b) {
     __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
@@ -94,6 +98,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// every thread of the role waits on (and arrives at) the barrier itself:
+// measured faster here than one elected lane per warp
+__device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, uint32_t limit, const int *timeout) {
+    return *reinterpret_cast<const volatile int *>(timeout) == 0 && umma::mbar_wait(bar, parity, limit);
+}
+__device__ __forceinline__ void role_arrive(uint64_t *bar) { umma::mbar_arrive(bar); }
+
 __device__ __forceinline__ uint64_t f2(float a, float b) {
     return (uint64_t)__float_as_uint(a) | ((uint64_t)__float_as_uint(b) << 32);
 }
@@ -105,7 +116,8 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 
 template <int BN>
 struct Ctl {
-    uint64_t full[4], bfull[4], empty[4], accf[2], acce[2];   // full: weights converted; bfull: activations landed
+    uint64_t full[3], bfull[3], empty[3], accf[2], acce[2];   // full: weights converted; bfull: activations landed
+    uint64_t cfull[kSC], cempty[kSC];                         // code boxes landed / read by every converter
     uint64_t drain;                    // after a timeout: the MMAs in flight have finished
     uint64_t never;                    // nothing arrives here (the stall test)
     uint32_t tmem;
@@ -114,11 +126,13 @@ struct Ctl {
 };
 
 template <int BN>
-constexpr size_t smem_total() { return (size_t)n_stages<BN>() * stage_bytes<BN>() + sizeof(Ctl<BN>) + 1024; }
+constexpr size_t smem_total() {
+    return (size_t)n_stages<BN>() * stage_bytes<BN>() + (size_t)kSC * kCodeBox + sizeof(Ctl<BN>) + 1024;
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    w4a16_umma_kernel(const __grid_constant__ CUtensorMap tx, const uint8_t *__restrict__ packed,
+    w4a16_umma_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw,
                       const uint32_t *__restrict__ sz, int M, int N, int K, uint16_t *__restrict__ y, int ldy,
                       int32_t *st, int C, uint32_t wait_limit, int stall, KvOut kv) {
     constexpr int S = n_stages<BN>();
@@ -127,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // stages 1024-aligned (the swizzle pattern is a function of the address)
     uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctl<BN> &sm = *reinterpret_cast<Ctl<BN> *>(stages + (size_t)S * kStage);
+    uint8_t *codes = stages + (size_t)S * kStage;                 // kSC boxes of kCodeBox bytes
+    Ctl<BN> &sm = *reinterpret_cast<Ctl<BN> *>(codes + (size_t)kSC * kCodeBox);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // cluster of C CTAs splits the groups of one 128-channel tile
     const int rank = C > 1 ? (int)umma::cluster_rank() : 0;
@@ -145,6 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&sm.bfull[s], 1);
             umma::mbar_init(&sm.empty[s], 1);
         }
+        for (int c = 0; c < kSC; ++c) {
+            umma::mbar_init(&sm.cfull[c], 1);
+            umma::mbar_init(&sm.cempty[c], kConv);
+        }
         for (int b = 0; b < 2; ++b) {
             umma::mbar_init(&sm.accf[b], 1);
             umma::mbar_init(&sm.acce[b], kEpilogue);
@@ -155,14 +174,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.drained = 1;
         umma::mbar_fence_init();
     }
-    if (warp == kTmaWarp && lane == 0) umma::prefetch_tmap(&tx);
+    if (warp == kTmaWarp && lane == 0) {
+        umma::prefetch_tmap(&tx);
+        umma::prefetch_tmap(&tw);
+    }
     pdl_launch_dependents();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem;
     bool issued = false;                          // MMAs issued (MMA lane 0)
-    int copies = 0;                               // groups whose activation boxes were issued (copy lane 0)
+    int copies = 0;                               // activation stages issued (copy lane 1) / code boxes (lane 0)
     auto timed_out = [&]() { return *reinterpret_cast<volatile int *>(&sm.timeout) != 0; };
     // epilogue partial sums: per thread (row n, token half) BN / 2 values
     constexpr int kHalf = BN / 2;
@@ -172,41 +194,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kConv / 32) {
         // ------------------------------------------------------ weight converters
         // thread: channel r = tid / 2, k half h = tid % 2 (atom h of each
-        // group); kD groups of codes in flight per thread
-        constexpr int kD = 3;
+        // group); its 32 code bytes of a group come from the code box (row r,
+        // 16-byte chunks 4 (l % 2) + 2 h + {0, 1}, 128-byte swizzle); the
+        // zero points kD groups ahead in registers
+        constexpr int kD = 8;
         const int r = tid >> 1, h = tid & 1, n = n0 + r;
         const bool row_ok = n < N;
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(packed + (size_t)(row_ok ? n : 0) * (K / 2)) + 2 * h;
-        uint4 ring[kD][2];
+        const uint32_t *zrow = sz + (size_t)(row_ok ? n : 0) * G;
         uint32_t zring[kD];
 #pragma unroll
-        for (int p = 0; p < kD; ++p) {
-            const int g = g_lo + p;
-            if (g < g_hi) {
-                ring[p][0] = __ldg(wrow + (size_t)g * 4);
-                ring[p][1] = __ldg(wrow + (size_t)g * 4 + 1);
-                zring[p] = row_ok ? __ldg(sz + (size_t)n * G + g) : 0u;
-            }
-        }
+        for (int p = 0; p < kD; ++p) zring[p] = (row_ok && p < NG) ? __ldg(zrow + g_lo + p) : 0u;
         bool ok = true;
         for (int lb = 0; lb < NG && ok; lb += kD) {
 #pragma unroll
             for (int p = 0; p < kD; ++p) {
-                const int l = lb + p, g = g_lo + l;
+                const int l = lb + p;
                 if (l >= NG) break;
-                const int s = l % S;
-                if (l >= S &&
-                    (timed_out() || !umma::mbar_wait(&sm.empty[s], ((l / S) - 1) & 1, wait_limit))) {
+                const int s = l % S, c = (l >> 1) % kSC;
+                // this group's codes (the box holds groups 2 (l / 2), + 1)
+                if ((l & 1) == 0 && !role_wait(&sm.cfull[c], ((l >> 1) / kSC) & 1, wait_limit, &sm.timeout)) {
                     atomicExch(&sm.timeout, 1);
                     ok = false;
                     break;
                 }
-                const uint4 c0 = ring[p][0], c1 = ring[p][1];
+                const uint8_t *crow = codes + (size_t)c * kCodeBox + (size_t)r * kAtom;
+                const int j0 = 4 * (l & 1) + 2 * h;
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(crow + ((j0 ^ (r & 7)) << 4));
+                const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + (((j0 + 1) ^ (r & 7)) << 4));
+                if ((l & 1) == 1 || l + 1 == NG) role_arrive(&sm.cempty[c]);
                 const uint32_t szc = zring[p];
-                if (l + kD < NG) {
-                    ring[p][0] = __ldg(wrow + (size_t)(g + kD) * 4);
-                    ring[p][1] = __ldg(wrow + (size_t)(g + kD) * 4 + 1);
-                    zring[p] = row_ok ? __ldg(sz + (size_t)n * G + g + kD) : 0u;
+                if (row_ok && l + kD < NG) zring[p] = __ldg(zrow + g_lo + l + kD);
+                if (l >= S && !role_wait(&sm.empty[s], ((l / S) - 1) & 1, wait_limit, &sm.timeout)) {
+                    atomicExch(&sm.timeout, 1);
+                    ok = false;
+                    break;
                 }
                 const uint32_t zb =
                     float_to_bf16_bits(128.0f + __half2float(__ushort_as_half((uint16_t)(szc >> 16))));
@@ -220,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(a + sw128_offset(r, j)) = v;
                 }
                 umma::fence_proxy_async();
-                umma::mbar_arrive(&sm.full[s]);
+                role_arrive(&sm.full[s]);
             }
         }
     } else if (warp < kMmaWarp) {
@@ -240,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok && l + 1 < NG) szn = __ldg(sz + (size_t)n * G + g_lo + l + 1);
             const float sn = __half2float(__ushort_as_half((uint16_t)(szw & 0xFFFF)));
             const uint64_t s2 = f2(sn, sn);
-            if (timed_out() || !umma::mbar_wait(&sm.accf[buf], (l >> 1) & 1, wait_limit)) {
+            if (!role_wait(&sm.accf[buf], (l >> 1) & 1, wait_limit, &sm.timeout)) {
                 atomicExch(&sm.timeout, 1);
                 ok = false;
                 break;
@@ -257,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc[(c0 + j) / 2] = fma2(f2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c0 + j) / 2]);
             }
             umma::fence_before_sync();
-            umma::mbar_arrive(&sm.acce[buf]);
+            role_arrive(&sm.acce[buf]);
         }
         epi_ok = ok;
         if (C == 1 && ok && row_ok) {
@@ -306,9 +327,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ activation copies
-        pdl_wait();
+        // ------------------------------------------------------------ copies
+        const int NP = (NG + 1) / 2;                      // code boxes: two groups each
         if (lane == 0) {
+            // code boxes: the first kSC before the dependency wait
+            for (int p = 0; p < NP; ++p) {
+                const int c = p % kSC;
+                if (p >= kSC && (timed_out() || !umma::mbar_wait(&sm.cempty[c], ((p / kSC) - 1) & 1, wait_limit))) {
+                    atomicExch(&sm.timeout, 1);
+                    break;
+                }
+                umma::mbar_arrive_expect_tx(&sm.cfull[c], (uint32_t)kCodeBox);
+                umma::tma_load_2d(codes + (size_t)c * kCodeBox, &tw, (g_lo + 2 * p) * (kGroup / 2), n0, &sm.cfull[c]);
+                copies = p + 1;
+            }
+        } else if (lane == 1) {
+            pdl_wait();
             for (int l = 0; l < NG; ++l) {
                 const int s = l % S, g = g_lo + l;
                 if (l >= S && (timed_out() || !umma::mbar_wait(&sm.empty[s], ((l / S) - 1) & 1, wait_limit))) {
@@ -331,6 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // settled at this barrier
     if (sm.timeout) {
         if (warp == kTmaWarp && lane == 0)
+            for (int p = std::max(0, copies - kSC); p < copies; ++p)
+                if (!umma::mbar_wait(&sm.cfull[p % kSC], (p / kSC) & 1, kWaitLimit)) sm.drained = 0;
+        if (warp == kTmaWarp && lane == 1)
             for (int l = std::max(0, copies - S); l < copies; ++l)
                 if (!umma::mbar_wait(&sm.bfull[l % S], (l / S) & 1, kWaitLimit)) sm.drained = 0;
         if (warp == kMmaWarp && lane == 0 && issued) {
@@ -382,9 +419,12 @@ int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t 
               const KvOut &kv) {
     static_assert(sizeof(float) * BN * kTileN <= (size_t)n_stages<BN>() * stage_bytes<BN>(),
                   "partials fit in the operand stages");
-    CUtensorMap tx;
-    // the activations as bytes: rows of K bf16, boxes of 128 bytes x BN tokens
-    if (byte_tmap_sw128(&tx, x, M, 2 * K, (size_t)ldx * 2, BN)) return QSPEC_ERR_UNSUPPORTED;
+    CUtensorMap tx, tw;
+    // the activations as bytes: rows of K bf16, boxes of 128 bytes x BN tokens;
+    // the packed codes: rows of K / 2 bytes, boxes of 128 bytes x 128 channels
+    if (byte_tmap_sw128(&tx, x, M, 2 * K, (size_t)ldx * 2, BN) ||
+        byte_tmap_sw128(&tw, packed, N, K / 2, (size_t)K / 2, kTileN))
+        return QSPEC_ERR_UNSUPPORTED;
     const size_t smem = smem_total<BN>();
     int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a16_umma_kernel<BN>), (int)smem);
     if (rc) return rc;
@@ -395,10 +435,10 @@ int launch_bn(const uint16_t *x, int ldx, const uint8_t *packed, const uint32_t 
     while (C < 8 && n_tiles * token_tiles * C * 2 <= sm_count() && 2 * C * 2 <= G) C *= 2;
     dim3 grid((unsigned)(n_tiles * C), (unsigned)token_tiles);
     if (C == 1)
-        return launch_pdl("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, tx,
-                          packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
+        return launch_pdl("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, tx, tw,
+                          sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
     return launch_pdl_cluster("qspec_linear_w4a16", w4a16_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, C, tx,
-                              packed, sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
+                              tw, sz, M, N, K, y, ldy, st, C, wait_limit, stall, kv);
 }
 
 }  // namespace
