@@ -11,26 +11,34 @@
 // 128-wide group into a TMEM accumulator in fp32; the epilogue applies the
 // group's scale, y += s * D_g, in fp32 registers.
 //
-// Both operands sit in shared memory in the K-major layout with 128-byte
-// swizzle (rows of 64 bf16; 8-row groups 1024 bytes apart; the 16-byte chunk
-// j of row r stored at position j ^ (r % 8)), which the MMA reads directly:
-//   - the activations arrive by TMA, two boxes of BN tokens x 64 k per group,
-//     in their natural k order;
+// Operands:
+//   - the activations (B) arrive by TMA in shared memory, two boxes of BN
+//     tokens x 64 k per group, in the K-major layout with 128-byte swizzle
+//     (rows of 64 bf16; 8-row groups 1024 bytes apart; the 16-byte chunk j of
+//     row r at position j ^ (r % 8)), which the MMA reads directly;
 //   - the packed codes arrive by TMA too, 128 channels x 128 bytes (two
 //     groups) per box, into a ring of four boxes whose first entries go out
 //     before the dependency wait (the weights are immutable); 8 warps convert
-//     them, two threads per output channel, each 64 k of a group: a code byte
-//     (c_2j in the low nibble, c_2j+1 in
-//     the high one) times 0x1001 puts the two codes 16 bits apart, OR-ed into
-//     the mantissa of 128.0 they give the bf16 pair (128 + c_2j, 128 + c_2j+1)
-//     exactly, and one exact bf16 subtraction of 128 + z leaves (c - z).
+//     them, two threads per output channel, each 64 k of a group: the codes
+//     of a word are split one per byte (even k, odd k), interleaved back into
+//     k order and spread into the low bytes of bf16 lanes of 128.0 by byte
+//     permutes, which gives the bf16 pairs (128 + c_2j, 128 + c_2j+1)
+//     exactly; one exact bf16 subtraction of 128 + z leaves (c - z);
+//   - the converted weights (A) go to tensor memory, not shared memory (lane
+//     = output channel, column = a pair of consecutive k), and the MMA reads
+//     them there: written and read in shared memory they would share its
+//     bandwidth with the activations and the codes, and bound the kernel.
 // One CTA computes a 128 (output channels) x BN (tokens) tile of Y^T:
-//   warps 0-7   weight converters
+//   warps 0-7   weight converters (warp w: TMEM lanes 32 (w % 4) .., k half w / 4)
 //   warps 8-15  epilogue, two warpgroups on the same TMEM lanes, each with
 //               half of the token columns: per group, TMEM -> registers,
 //               y = fma(D, s, y) in packed f32x2; finally bf16
-//   warp 16     issues 8 MMAs (K = 16) per group into one of two TMEM buffers
-//   warp 17     lane 0 issues the code boxes, lane 1 the activation boxes
+//   warps 16-17 lane 0 of each issues the 8 MMAs (K = 16) of every other
+//               group, into its own TMEM accumulator, A from one of four TMEM
+//               operand buffers (a thread that issued MMAs waits for them on
+//               its own next shared-memory access, so one issuer alone would
+//               leave the tensor core idle between groups)
+//   warp 18     lane 0 issues the code boxes, lane 1 the activation boxes
 // When the 128-channel tiles alone would leave SMs idle, a cluster of up to 8
 // CTAs splits a tile's groups; each CTA keeps its fp32 partial sums, and
 // rank 0 reads its peers' partials from distributed shared memory, adds them
@@ -56,31 +64,32 @@ constexpr int kTileN = 128;              // output channels per CTA (MMA M)
 constexpr int kAtom = 128;               // bytes of K per swizzle atom row (64 bf16)
 constexpr int kConv = 256;               // converter threads: two per channel
 constexpr int kEpilogue = 256;
-constexpr int kMmaWarp = (kConv + kEpilogue) / 32, kTmaWarp = kMmaWarp + 1;
-constexpr int kThreads = kConv + kEpilogue + 64;
-constexpr int kA = kTileN * 2 * kAtom;   // A bytes per stage (one group: two atoms)
+constexpr int kMmaWarp = (kConv + kEpilogue) / 32, kTmaWarp = kMmaWarp + 2;   // two issuer warps
+constexpr int kThreads = kConv + kEpilogue + 96;
 constexpr int kCodeBox = kTileN * kAtom; // packed codes of two groups for 128 channels
 constexpr int kSC = 4;                   // code boxes in the ring
+constexpr int kSA = 4;                   // A operand buffers in TMEM (64 columns: one group)
 
 template <int BN>
-constexpr int stage_bytes() { return kA + BN * 2 * kAtom; }
+constexpr int stage_bytes() { return BN * 2 * kAtom; }       // activations of one group
 template <int BN>
-constexpr int n_stages() { return std::min(3, (212 * 1024 - kSC * kCodeBox) / stage_bytes<BN>()); }
+constexpr int n_stages() {   // even: each issuer then uses its own stages
+    return std::min(4, (212 * 1024 - kSC * kCodeBox) / stage_bytes<BN>()) & ~1;
+}
 
 __device__ __forceinline__ uint32_t bf2_sub(uint32_t a, uint32_t b) {
     __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// one code byte (c_2j low nibble, c_2j+1 high) -> bf16 pair (c_2j - z, c_2j+1 - z)
-__device__ __forceinline__ uint32_t pair_minus_z(uint32_t b, uint32_t zz) {
-    const uint32_t t = b * 0x1001u;                        // low nibble at bits 0-3, high at 16-19
-    return bf2_sub((t & 0x000F000Fu) | 0x43004300u, zz);   // (128 + c) - (128 + z), exact
-}
-// eight codes of a word (k = 0..7) -> 16 bytes of bf16 (c - z), natural k order
+// eight codes of a word (k = 0..7) -> 16 bytes of bf16 (c - z), natural k order:
+// the codes one per byte (even k / odd k), interleaved in k order, then each
+// pair of bytes spread into the low bytes of two bf16 lanes of 128.0
 __device__ __forceinline__ uint4 word_minus_z(uint32_t w, uint32_t zz) {
-    return make_uint4(pair_minus_z(w & 0xFFu, zz), pair_minus_z((w >> 8) & 0xFFu, zz),
-                      pair_minus_z((w >> 16) & 0xFFu, zz), pair_minus_z(w >> 24, zz));
+    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu, m = 0x43434343u;
+    const uint32_t u0 = __byte_perm(lo, hi, 0x5140), u1 = __byte_perm(lo, hi, 0x7362);   // c0..c3, c4..c7
+    return make_uint4(bf2_sub(__byte_perm(u0, m, 0x4140), zz), bf2_sub(__byte_perm(u0, m, 0x4342), zz),
+                      bf2_sub(__byte_perm(u1, m, 0x4140), zz), bf2_sub(__byte_perm(u1, m, 0x4342), zz));
 }
 
 // K-major 128-byte-swizzle descriptor: start address, leading offset unused
@@ -93,11 +102,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     d |= (uint64_t)2 << 61;
     return d;
 }
-// byte offset of (row, 16-byte chunk) in a 128-byte-swizzled atom
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
-    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
 // every thread of the role waits on (and arrives at) the barrier itself:
 // measured faster here than one elected lane per warp
 __device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, uint32_t limit, const int *timeout) {
@@ -116,9 +120,11 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 
 template <int BN>
 struct Ctl {
-    uint64_t full[3], bfull[3], empty[3], accf[2], acce[2];   // full: weights converted; bfull: activations landed
+    uint64_t afull[kSA], aempty[kSA];                         // A buffers: converted / read by the MMAs
+    uint64_t bfull[4], bempty[4];                             // activation stages: landed / read
+    uint64_t accf[2], acce[2];
     uint64_t cfull[kSC], cempty[kSC];                         // code boxes landed / read by every converter
-    uint64_t drain;                    // after a timeout: the MMAs in flight have finished
+    uint64_t drain[2];                 // after a timeout: each issuer's MMAs in flight have finished
     uint64_t never;                    // nothing arrives here (the stall test)
     uint32_t tmem;
     int timeout;
@@ -150,15 +156,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = K / kGroup;
     const int g_lo = (int)(((long long)rank * G) / C), g_hi = (int)(((long long)(rank + 1) * G) / C);
     const int NG = g_hi - g_lo;                          // this CTA's groups
+    // TMEM: two accumulators of kBuf columns, then kSA A buffers of 64
     constexpr uint32_t kBuf = BN <= 32 ? 32 : BN <= 64 ? 64 : 128;
-    constexpr uint32_t kCols = 2 * kBuf;
+    constexpr uint32_t kAcol = 2 * kBuf;
+    constexpr uint32_t kCols = kAcol + 64 * kSA <= 256 ? 256 : 512;
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem, kCols);
     if (tid == 0) {
+        for (int s = 0; s < kSA; ++s) {
+            umma::mbar_init(&sm.afull[s], kConv);
+            umma::mbar_init(&sm.aempty[s], 1);
+        }
         for (int s = 0; s < S; ++s) {
-            umma::mbar_init(&sm.full[s], kConv);
             umma::mbar_init(&sm.bfull[s], 1);
-            umma::mbar_init(&sm.empty[s], 1);
+            umma::mbar_init(&sm.bempty[s], 1);
         }
         for (int c = 0; c < kSC; ++c) {
             umma::mbar_init(&sm.cfull[c], 1);
@@ -168,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&sm.accf[b], 1);
             umma::mbar_init(&sm.acce[b], kEpilogue);
         }
-        umma::mbar_init(&sm.drain, 1);
+        umma::mbar_init(&sm.drain[0], 1);
+        umma::mbar_init(&sm.drain[1], 1);
         umma::mbar_init(&sm.never, 1);
         sm.timeout = 0;
         sm.drained = 1;
@@ -193,14 +205,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kConv / 32) {
         // ------------------------------------------------------ weight converters
-        // thread: channel r = tid / 2, k half h = tid % 2 (atom h of each
-        // group); its 32 code bytes of a group come from the code box (row r,
-        // 16-byte chunks 4 (l % 2) + 2 h + {0, 1}, 128-byte swizzle); the
-        // zero points kD groups ahead in registers
+        // warp w: channels r = 32 (w % 4) + lane (its TMEM lanes), k half
+        // h = w / 4 of each group; the thread's 32 code bytes of a group come
+        // from the code box (row r, 16-byte chunks 4 (l % 2) + 2 h + {0, 1},
+        // 128-byte swizzle); the zero points kD groups ahead in registers
         constexpr int kD = 8;
-        const int r = tid >> 1, h = tid & 1, n = n0 + r;
+        const int r = 32 * (warp & 3) + lane, h = warp >> 2, n = n0 + r;
         const bool row_ok = n < N;
         const uint32_t *zrow = sz + (size_t)(row_ok ? n : 0) * G;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t zring[kD];
 #pragma unroll
         for (int p = 0; p < kD; ++p) zring[p] = (row_ok && p < NG) ? __ldg(zrow + g_lo + p) : 0u;
@@ -210,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int p = 0; p < kD; ++p) {
                 const int l = lb + p;
                 if (l >= NG) break;
-                const int s = l % S, c = (l >> 1) % kSC;
+                const int sa = l % kSA, c = (l >> 1) % kSC;
                 // this group's codes (the box holds groups 2 (l / 2), + 1)
                 if ((l & 1) == 0 && !role_wait(&sm.cfull[c], ((l >> 1) / kSC) & 1, wait_limit, &sm.timeout)) {
                     atomicExch(&sm.timeout, 1);
@@ -224,24 +237,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if ((l & 1) == 1 || l + 1 == NG) role_arrive(&sm.cempty[c]);
                 const uint32_t szc = zring[p];
                 if (row_ok && l + kD < NG) zring[p] = __ldg(zrow + g_lo + l + kD);
-                if (l >= S && !role_wait(&sm.empty[s], ((l / S) - 1) & 1, wait_limit, &sm.timeout)) {
+                const uint32_t zb =
+                    float_to_bf16_bits(128.0f + __half2float(__ushort_as_half((uint16_t)(szc >> 16))));
+                const uint32_t zz = zb | (zb << 16);
+                // 64 codes of row r (k = 64 h ..) -> 32 bf16 pairs
+                const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 q = word_minus_z(words[j], zz);   // rows past N: zero codes, z = 0 -> 0
+                    v[4 * j] = q.x;
+                    v[4 * j + 1] = q.y;
+                    v[4 * j + 2] = q.z;
+                    v[4 * j + 3] = q.w;
+                }
+                // A buffer sa is free once the MMAs of group l - kSA have read it
+                if (l >= kSA && !role_wait(&sm.aempty[sa], ((l / kSA) - 1) & 1, wait_limit, &sm.timeout)) {
                     atomicExch(&sm.timeout, 1);
                     ok = false;
                     break;
                 }
-                const uint32_t zb =
-                    float_to_bf16_bits(128.0f + __half2float(__ushort_as_half((uint16_t)(szc >> 16))));
-                const uint32_t zz = zb | (zb << 16);
-                // 64 codes of row r (k = 64 h ..) -> 8 chunks of 8 bf16 in atom h
-                uint8_t *a = stages + (size_t)s * kStage + (size_t)h * (kTileN * kAtom);
-                const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 v = row_ok ? word_minus_z(words[j], zz) : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(a + sw128_offset(r, j)) = v;
-                }
-                umma::fence_proxy_async();
-                role_arrive(&sm.full[s]);
+                umma::fence_after_sync();
+                umma::tmem_st32(tmem + lane_off + kAcol + (uint32_t)(sa * 64 + h * 32), v);
+                umma::tmem_st_wait();
+                umma::fence_before_sync();
+                role_arrive(&sm.afull[sa]);
             }
         }
     } else if (warp < kMmaWarp) {
@@ -297,30 +317,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp < kTmaWarp) {
+        // ------------------------------------------------------------ MMA issuers
+        // issuer i takes groups l = i, i + 2, ...: accumulator i, A buffers
+        // and activation stages of parity i (kSA and S are even), so each
+        // barrier it polls is at most one phase ahead of the last it saw
+        const int iss = warp - kMmaWarp;
         if (lane == 0) {
             constexpr uint32_t idesc = umma::instr_desc(1, 1, kTileN, BN);
-            if (stall && !umma::mbar_wait(&sm.never, 0, wait_limit)) atomicExch(&sm.timeout, 1);
-            for (int l = 0; l < NG; ++l) {
-                const int s = l % S, buf = l & 1;
-                if (timed_out() || !umma::mbar_wait(&sm.full[s], (l / S) & 1, wait_limit) ||
-                    !umma::mbar_wait(&sm.bfull[s], (l / S) & 1, wait_limit) ||
+            if (stall && iss == 0 && !umma::mbar_wait(&sm.never, 0, wait_limit)) atomicExch(&sm.timeout, 1);
+            for (int l = iss; l < NG; l += 2) {
+                const int sa = l % kSA, sb = l % S, buf = l & 1;
+                if (timed_out() || !umma::mbar_wait(&sm.afull[sa], (l / kSA) & 1, wait_limit) ||
+                    !umma::mbar_wait(&sm.bfull[sb], (l / S) & 1, wait_limit) ||
                     (l >= 2 && !umma::mbar_wait(&sm.acce[buf], ((l >> 1) - 1) & 1, wait_limit))) {
                     atomicExch(&sm.timeout, 1);
                     break;
                 }
                 umma::fence_after_sync();
-                const uint32_t a0 = umma::smem_addr(stages + (size_t)s * kStage), b0 = a0 + kA;
+                const uint32_t b0 = umma::smem_addr(stages + (size_t)sb * kStage);
+                const uint32_t a0 = tmem + kAcol + (uint32_t)(sa * 64);
                 const uint32_t d = tmem + (uint32_t)(buf * kBuf);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint64_t da = desc_sw128(a0 + h * kTileN * kAtom), db = desc_sw128(b0 + h * BN * kAtom);
-#pragma unroll
-                    for (int kk = 0; kk < kAtom / 32; ++kk)   // K = 16 bf16 = 32 bytes: +2 in the address field
-                        umma::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (h | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {               // K = 16 bf16: 8 TMEM columns of A, 32 bytes of B
+                    const uint64_t db = desc_sw128(b0 + (kk >> 2) * BN * kAtom);
+                    umma::mma_bf16_ta(d, a0 + 8 * kk, db + 2 * (kk & 3), idesc, kk != 0 ? 1u : 0u);
                 }
-                umma::mma_commit(&sm.empty[s]);
+                umma::mma_commit(&sm.aempty[sa]);
+                umma::mma_commit(&sm.bempty[sb]);
                 umma::mma_commit(&sm.accf[buf]);
                 issued = true;
             }
@@ -345,11 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             pdl_wait();
             for (int l = 0; l < NG; ++l) {
                 const int s = l % S, g = g_lo + l;
-                if (l >= S && (timed_out() || !umma::mbar_wait(&sm.empty[s], ((l / S) - 1) & 1, wait_limit))) {
+                if (l >= S && (timed_out() || !umma::mbar_wait(&sm.bempty[s], ((l / S) - 1) & 1, wait_limit))) {
                     atomicExch(&sm.timeout, 1);
                     break;
                 }
-                uint8_t *b = stages + (size_t)s * kStage + kA;
+                uint8_t *b = stages + (size_t)s * kStage;
                 umma::mbar_arrive_expect_tx(&sm.bfull[s], (uint32_t)(BN * 2 * kAtom));
                 umma::tma_load_2d(b, &tx, g * 2 * kAtom, t0, &sm.bfull[s]);
                 umma::tma_load_2d(b + BN * kAtom, &tx, g * 2 * kAtom + kAtom, t0, &sm.bfull[s]);
@@ -370,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == kTmaWarp && lane == 1)
             for (int l = std::max(0, copies - S); l < copies; ++l)
                 if (!umma::mbar_wait(&sm.bfull[l % S], (l / S) & 1, kWaitLimit)) sm.drained = 0;
-        if (warp == kMmaWarp && lane == 0 && issued) {
-            umma::mma_commit(&sm.drain);
-            if (!umma::mbar_wait(&sm.drain, 0, kWaitLimit)) sm.drained = 0;
+        if (warp >= kMmaWarp && warp < kTmaWarp && lane == 0 && issued) {
+            umma::mma_commit(&sm.drain[warp - kMmaWarp]);
+            if (!umma::mbar_wait(&sm.drain[warp - kMmaWarp], 0, kWaitLimit)) sm.drained = 0;
         }
         __syncthreads();
     }
