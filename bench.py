@@ -343,21 +343,6 @@ class GpuRound:
         self.out = torch.zeros((B, g + 1), dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
 
-    # kernel launches of the library per step (for gpu_launches)
-    def launches_per_round(self):
-        n_lin = len(self.linears)
-        sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
-
-        def w4a4_launches(N):
-            # the fused call is one launch on the warp-MMA path (M <= 32, not
-            # the tensor-memory GEMV), else quantiser + linear
-            two = self.B > 32 or (3 <= self.B <= 8 and (N + 127) // 128 >= sms)
-            return 2 if two else 1
-        draft = self.gamma * (self.L * sum(w4a4_launches(N) for _, N, _ in self.linears) +
-                              w4a4_launches(self.V))
-        verify = self.L * n_lin + 1
-        return draft + verify + 4 + 1
-
     def _check(self, rc, what):
         if rc != 0:
             raise RuntimeError("%s returned %s" % (what, self.q.STATUS.get(rc, rc)))
@@ -877,7 +862,13 @@ def main():
     torch.cuda.synchronize()
     if int(rnd_obj.status.item()) != 0:
         raise RuntimeError("device status %d after the eager round" % int(rnd_obj.status.item()))
-    graphs = [capture(lambda r=r: rnd_obj.run(r, acc_log[r]), stream) for r in range(R)]
+    # the library's own count of the kernels one round launches (read around
+    # the capture of the first round's graph)
+    from quantized_speculative_decoding_shared_gb300 import binding as qb
+    n_before = qb.qspec_kernel_launches()
+    graphs = [capture(lambda: rnd_obj.run(0, acc_log[0]), stream)]
+    launches_per_round = qb.qspec_kernel_launches() - n_before
+    graphs += [capture(lambda r=r: rnd_obj.run(r, acc_log[r]), stream) for r in range(1, R)]
 
     def barrier():
         if world > 1:
@@ -978,7 +969,7 @@ def main():
                                                  "M": wl["B"] * (wl["gamma"] + 1)}},
             "rows": row_kernels(dev, stream),
             "targets": targets(rnd_obj, dev, stream),
-            "gpu_launches": rnd_obj.launches_per_round() * args.steps,
+            "gpu_launches": launches_per_round * args.steps,
             "clocks": clk}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)

@@ -75,6 +75,11 @@ const char *qspec_status_string(int status);
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */
 const char *qspec_last_cuda_error(void);
 
+/* Number of kernel launches this library has issued since it was loaded,
+ * all threads together, counting a launch recorded into a CUDA graph once
+ * (at capture).  Host only; never fails. */
+unsigned long long qspec_kernel_launches(void);
+
 /*
  * a1. Pack INT4 weights.  [QS-bg] dequantisation W^ = s (W_INT4 - z);
  * [QS-design] one 4-bit weight set serves both the W4A4 draft and the W4A16

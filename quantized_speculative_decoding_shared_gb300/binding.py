@@ -29,7 +29,8 @@ STATUS = {0: "QSPEC_OK", 1: "QSPEC_ERR_NULL", 2: "QSPEC_ERR_SHAPE", 3: "QSPEC_ER
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_LAUNCH, ERR_WORKSPACE = 0, 1, 2, 3, 4, 5
 ERR_RANGE, ERR_ZERO_POINT, ERR_NONFINITE, ERR_TIMEOUT, ERR_UNSUPPORTED = 6, 7, 8, 9, 10
 
-EXPORTED = ["qspec_version", "qspec_status_string", "qspec_last_cuda_error", "qspec_pack_weights",
+EXPORTED = ["qspec_version", "qspec_status_string", "qspec_last_cuda_error", "qspec_kernel_launches",
+            "qspec_pack_weights",
             "qspec_quant_act_int4", "qspec_linear_w4a4", "qspec_linear_w4a4_bf16", "qspec_linear_w4a16",
             "qspec_verify_workspace_bytes", "qspec_verify_greedy", "qspec_verify_sample",
             "qspec_kv_overwrite", "qspec_verify_sample_noalloc", "qspec_draft_workspace_bytes",
@@ -66,6 +67,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i32, sz_t, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64
         proto = {
             "qspec_version": ([], i32),
+            "qspec_kernel_launches": ([], ctypes.c_ulonglong),
             "qspec_status_string": ([i32], ctypes.c_char_p),
             "qspec_last_cuda_error": ([], ctypes.c_char_p),
             "qspec_pack_weights": ([vp, vp, vp, i32, i32, vp, vp, vp, vp], i32),
@@ -214,6 +216,11 @@ def qspec_kv_overwrite(k_cache, v_cache, k_new, v_new, base_pos, n_acc, L, B, H,
     return load_library().qspec_kv_overwrite(_ptr(k_cache), _ptr(v_cache), _ptr(k_new),
                                              _ptr(v_new), _ptr(base_pos), _ptr(n_acc), L, B, H, T,
                                              D, gamma, _ptr(dev_status), _stream(stream))
+
+
+def qspec_kernel_launches():
+    """Kernel launches this library has issued (graph captures count once)."""
+    return int(load_library().qspec_kernel_launches())
 
 
 def qspec_debug_linear_bounded(kernel, x, xq, sx, qs, packed, sz, M, N, K, y, ldy, wait_limit,

@@ -1,6 +1,7 @@
 // abi.cu -- version, status strings, error text, device checks.
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "qspec_host.h"
@@ -8,6 +9,12 @@
 namespace qspec {
 
 static thread_local char g_last_error[256] = "";
+
+std::atomic<unsigned long long> &launch_count() {
+    static std::atomic<unsigned long long> n{0};
+    return n;
+}
+void count_launch() { launch_count().fetch_add(1, std::memory_order_relaxed); }
 
 void set_last_error(const char *where, cudaError_t e) {
     snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
@@ -99,6 +106,8 @@ int check_launch(const char *where) {
 extern "C" {
 
 int qspec_version(void) { return 100; }   // 0.1.0
+
+unsigned long long qspec_kernel_launches(void) { return (unsigned long long)qspec::launch_count().load(); }
 
 const char *qspec_status_string(int status) {
     switch (status) {

@@ -71,5 +71,10 @@ extern "C" int qspec_pack_weights(const uint8_t *codes, const uint16_t *s_fp16,
     pack_codes_kernel<<<g1, 256, 0, st>>>(reinterpret_cast<const uint4 *>(codes), n_chunks,
                                           reinterpret_cast<uint4 *>(packed), dev_status);
     pack_scales_kernel<<<g2, 256, 0, st>>>(s_fp16, z_fp16, n_groups, sz, dev_status);
-    return check_launch("qspec_pack_weights");
+    const int lrc = check_launch("qspec_pack_weights");
+    if (lrc == QSPEC_OK) {
+        count_launch();
+        count_launch();
+    }
+    return lrc;
 }

@@ -56,6 +56,9 @@ int launch_w4a16_tc(const uint16_t *x, int ldx, const uint8_t *packed, const uin
 int launch_w4a4_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                    const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st,
                    cudaStream_t stream, uint32_t wait_limit, int stall);
+int launch_w4a4_tc_wide(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
+                   const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st,
+                   cudaStream_t stream, uint32_t wait_limit, int stall);
 
 // Decode-sized W4A4 (3 <= M <= 16) on the tensor cores with the weights
 // staged in TMEM (w4a4_gemv_tc.cu); QSPEC_ERR_SHAPE before any launch when
@@ -79,6 +82,9 @@ int byte_tmap_sw128(CUtensorMap *out, const void *base, int rows, int cols, size
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 
+// One more kernel launch issued (the count qspec_kernel_launches reports).
+void count_launch();
+
 // Launch `kernel` on `st` with programmatic stream serialisation allowed (the
 // kernel must follow the pdl_wait() rule in qspec_device.cuh).
 template <typename... KArgs, typename... Args>
@@ -99,6 +105,7 @@ int launch_pdl(const char *where, void (*kernel)(KArgs...), dim3 grid, dim3 bloc
         set_last_error(where, e);
         return QSPEC_ERR_LAUNCH;
     }
+    count_launch();
     return QSPEC_OK;
 }
 
@@ -126,6 +133,7 @@ int launch_pdl_cluster(const char *where, void (*kernel)(KArgs...), dim3 grid, d
         set_last_error(where, e);
         return QSPEC_ERR_LAUNCH;
     }
+    count_launch();
     return QSPEC_OK;
 }
 

@@ -234,7 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j0 = 4 * (l & 1) + 2 * h;
                 const uint4 c0 = *reinterpret_cast<const uint4 *>(crow + ((j0 ^ (r & 7)) << 4));
                 const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + (((j0 + 1) ^ (r & 7)) << 4));
-                if ((l & 1) == 1 || l + 1 == NG) role_arrive(&sm.cempty[c]);
+                // the box's next contents come by TMA (the async proxy): these
+                // reads are fenced against it before the box is released
+                if ((l & 1) == 1 || l + 1 == NG) {
+                    umma::fence_proxy_async();
+                    role_arrive(&sm.cempty[c]);
+                }
                 const uint32_t szc = zring[p];
                 if (row_ok && l + kD < NG) zring[p] = __ldg(zrow + g_lo + l + kD);
                 const uint32_t zb =

@@ -425,13 +425,13 @@ int tokens_per_cta(int M, int K) {
 
 // up to 32 tokens go to the tensor-core kernel (all tokens of a 128-row tile
 // in one CTA) when the warp-MMA path would read the weights more than 12
-// times: large K leaves room for one token per warp-MMA CTA, whose time grows
-// by ~7 us per token tile on a 4096 x 14336 layer, while the tensor-core
-// kernel takes 100-150 us at any token count up to 32 (measured crossover
-// near 13 tiles)
-bool use_tc(int M, int K) {
+// times (large K leaves room for few tokens per warp-MMA CTA), and 17..32
+// tokens on the larger layers (N >= 6144), where it measured 1.2-2.5x faster
+// than the warp-MMA kernel's several token tiles (LM head at 32 tokens: 216
+// vs 547 us) even with its separate quantiser launch
+bool use_tc(int M, int N, int K) {
     const int mt = tokens_per_cta(M, K);
-    return (M + mt - 1) / mt > 12;
+    return (M + mt - 1) / mt > 12 || (M > 16 && N >= 6144);
 }
 
 // warp-MMA path for M <= 32: QSPEC_ERR_SHAPE when the shape does not fit
@@ -483,7 +483,7 @@ extern "C" int qspec_linear_w4a4(const uint8_t *xq, const float *sx, const int32
         rc = launch_w4a4_gemv_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st, kWaitLimit, 0);
         if (rc != QSPEC_ERR_SHAPE) return rc;
     }
-    if (hm::use_tc(M, K)) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st, kWaitLimit, 0);
+    if (hm::use_tc(M, N, K)) return launch_w4a4_tc(xq, sx, qs, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st, kWaitLimit, 0);
     const hm::Act act = {xq, sx, qs, nullptr, 0, nullptr, nullptr, nullptr};
     return hm::launch_small(act, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
 }
@@ -504,7 +504,7 @@ extern "C" int qspec_linear_w4a4_bf16(const uint16_t *x_bf16, int ldx, const uin
                               dev_status, st);
         if (rc != QSPEC_ERR_SHAPE) return rc;
     }
-    if (M <= 32 && !hm::use_gemv_tc(M, N) && !hm::use_tc(M, K)) {
+    if (M <= 32 && !hm::use_gemv_tc(M, N) && !hm::use_tc(M, N, K)) {
         const hm::Act act = {xq, sx, qs, x_bf16, ldx, xq, sx, qs};
         rc = hm::launch_small(act, packed, sz, M, N, K, y_bf16, ldy, dbg_I, dev_status, st);
         if (rc != QSPEC_ERR_SHAPE) return rc;

@@ -254,6 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma::tmem_st_wait();
             umma::fence_before_sync();
+            // the stage's next contents come by TMA (the async proxy): this
+            // thread's reads of it are fenced against that before its release
+            umma::fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
                 umma::mbar_arrive(&full[s]);

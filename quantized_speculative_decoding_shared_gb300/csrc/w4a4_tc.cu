@@ -4,33 +4,46 @@
 //
 // QSPEC summary page, background terms: 4-bit activations times 4-bit
 // weights, products accumulated exactly (INT32 in the pages' wording), then
-// scaled to 16 bits.  Bit-exact definition (the same as the small-M kernel
+// scaled to 16 bits.  Bit-exact definition (the same as the small-M kernels
 // and the CPU oracle):
 //   I[m][n][g] = sum_{k in g} q (W - z) ; acc = fmaf((float) I, sx * s, acc)
 //   for g ascending from acc = 0 ; y = bf16_rn(acc).
 //
 // sm_103a has no integer tcgen05 MMA, so the products run as
-// tcgen05.mma kind::f8f6f4 with E4M3 operands that hold the integers exactly:
-// codes 0..15 (weights, A operand, 128 output channels per CTA) and
-// q in [-8, 7] (activations, B operand, BN tokens per CTA).  One K step is
-// one 128-wide group (4 MMAs of K = 32).  Every product is an integer of
-// magnitude <= 120 and every partial sum of a group stays below 2^14, so the
-// fp32 accumulator in TMEM holds sum q W exactly; the epilogue forms
-// I = sum q W - z qs exactly in fp32 (|I| <= 13440) and folds it.
+// tcgen05.mma kind::f8f6f4 on E4M3 bytes that hold the integers exactly up
+// to a power of two: a byte b in 0..15 read as E4M3 is b * 2^-9 (subnormal
+// below 8, exponent 1 above), so a weight code needs no table -- its nibble
+// is the byte -- and a token's q in [-8, 7] is the byte |q| with the sign
+// bit set for q < 0.  Every product is c q 2^-18 with |c q| <= 120 and every
+// partial sum of a group stays below 2^14 * 2^-18, so the fp32 accumulator
+// holds D = 2^-18 sum q W exactly; the epilogue forms I = D 2^18 - z qs
+// exactly in fp32 and folds it.  Inside each 8-wide k block both operands
+// keep the even k first (w & 0x0F0F0F0F) and the odd k after
+// ((w >> 4) & 0x0F0F0F0F): the MMA sums over k in any order common to both.
 //
-//   warps 0-3  producers: nibbles -> E4M3 bytes (byte permutes), written to
-//              shared memory in the no-swizzle K-major core-matrix layout,
-//              with the tokens' sx / qs of the group
-//   warps 4-11 epilogue, two warpgroups on the same TMEM lanes, each with half
-//              of the token columns: per group, TMEM -> registers, I and the
-//              ordered fp32 fold in registers (packed f32x2); finally bf16
-//   warp 12    issues the MMAs into one of two TMEM accumulators per group
+// Operands and roles (one CTA: 128 output channels x BN tokens of Y^T):
+//   - the packed weight codes arrive by TMA, 128 channels x 128 bytes (two
+//     groups) per box, 128-byte swizzle, into a ring of four boxes whose
+//     first entries go out before the dependency wait (the weights are
+//     immutable); warps 0-3 (thread = TMEM lane = channel) split each word
+//     into its even- and odd-k bytes and store the group's 128 bytes into
+//     one of four A buffers in tensor memory (32 columns);
+//   - warps 12-15 build the tokens' E4M3 bytes for a group from the packed
+//     activation codes into a B stage in shared memory (K-major, 128-byte
+//     swizzle: 16-byte chunk j of token row t at position j ^ (t % 8));
+//   - warps 16-17, lane 0 of each, issue the 4 MMAs (M = 128, N = BN,
+//     K = 32) of every other group into their own TMEM accumulator (a thread
+//     that issued MMAs waits for them on its own next shared-memory access);
+//   - warps 4-11, two warpgroups on the same TMEM lanes with half of the
+//     token columns each: per group, TMEM -> registers, I and the ordered
+//     fold in packed f32x2; finally bf16;
+//   - warp 18, lane 0, issues the code boxes.
 // Bounded waits everywhere (the limit is a kernel argument; a test can also
-// make the MMA issuer wait on a barrier nothing arrives at).  After a
-// timeout (QSPEC_ERR_TIMEOUT) every role leaves its loop -- the epilogue
-// warpgroups together, through a barrier that ORs their failure flags, since
-// they also meet at a named barrier -- the MMAs issued are drained with a
-// bounded wait, and the tensor memory is freed (even if the drain itself ran
+// make an MMA issuer wait on a barrier nothing arrives at).  After a timeout
+// (QSPEC_ERR_TIMEOUT) every role leaves its loop -- the epilogue warpgroups
+// together, through a barrier that ORs their failure flags, since they also
+// meet at a named barrier -- the code copies and MMAs in flight are drained
+// with bounded waits, and the tensor memory is freed (even if a drain ran
 // out: the next kernel on the SM would otherwise wait for it without bound).
 #include <algorithm>
 
@@ -42,46 +55,39 @@ namespace qspec {
 
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kTileN = 128;        // output channels per CTA (MMA M)
-constexpr int kKB = kGroup;        // bytes of K per row per stage (E4M3)
-constexpr int kProducers = 128;
-constexpr int kEpilogue = 256;        // two warpgroups, each folds half of the token columns
-constexpr int kThreads = kProducers + kEpilogue + 32;
+constexpr int kTileN = 128;                // output channels per CTA (MMA M)
+constexpr int kAtom = 128;                 // bytes of K per row per group (E4M3)
+constexpr int kConv = 128, kEpilogue = 256, kBld = 128;
+constexpr int kEpiWarp0 = kConv / 32, kBldWarp0 = kEpiWarp0 + kEpilogue / 32;
+constexpr int kMmaWarp = kBldWarp0 + kBld / 32, kTmaWarp = kMmaWarp + 2;   // two issuer warps
+constexpr int kThreads = (kTmaWarp + 1) * 32;
+constexpr int kCodeBox = kTileN * kAtom;   // packed codes of two groups for 128 channels
+constexpr int kSC = 4;                     // code boxes in the ring
+constexpr int kSA = 4;                     // A buffers in TMEM (32 columns: one group)
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+template <int BN>
+constexpr int stage_bytes() { return BN * kAtom; }            // the tokens' bytes of one group
+template <int BN>
+constexpr int n_stages() {                 // even: each issuer then uses its own stages
+    return std::min(4, (200 * 1024 - kSC * kCodeBox) / stage_bytes<BN>()) & ~1;
+}
+
+// K-major 128-byte-swizzle descriptor: start address, leading offset unused
+// (16 bytes), 1024 bytes between 8-row groups, version 1, swizzle mode 2
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
     return d;
 }
 
-// E4M3 bytes of the unsigned codes 0..15 in the low 16 bits' nibbles of `w`.
-// prmt's selector nibble bit 3 replicates the sign bit of the chosen byte; all
-// table bytes are positive, so codes >= 8 give 0 from the first lookup and
-// codes < 8 give 0 from the second (which looks up ~w).
-__device__ __forceinline__ uint32_t e4m3_codes4(uint32_t w, uint32_t nw) {
-    const uint32_t t0 = 0x44403800u, t1 = 0x4E4C4A48u;   // E4M3 of 0..7
-    const uint32_t u0 = 0x54555657u, u1 = 0x50515253u;   // E4M3 of 15..8 (index 7 - (c - 8))
-    return prmt(t0, t1, w) | prmt(u0, u1, nw);
-}
-
-// eight codes (one word) -> two words of E4M3 bytes in k order
-__device__ __forceinline__ uint2 e4m3_codes8(uint32_t w) {
-    const uint32_t nw = ~w;
-    return make_uint2(e4m3_codes4(w, nw), e4m3_codes4(w >> 16, nw >> 16));
-}
-
-// eight two's-complement nibbles q in [-8, 7] -> two words of E4M3 bytes:
-// magnitude through the code tables, sign bit set from the nibble's bit 3
-__device__ __forceinline__ uint2 e4m3_acts8(uint32_t w) {
-    const uint32_t s4 = (w >> 3) & 0x11111111u;            // sign of each nibble
-    const uint32_t mag = (w ^ (s4 * 15u)) + s4;            // |q| per nibble, 0..8, no carries
-    const uint32_t nmag = ~mag;
-    const uint32_t k80 = 0x80808080u;
-    // byte i of prmt(k80, k80, w) is 0xFF when nibble i is negative, else 0x80
-    const uint32_t sg_lo = (prmt(k80, k80, w) << 7) & 0x80808080u;
-    const uint32_t sg_hi = (prmt(k80, k80, w >> 16) << 7) & 0x80808080u;
-    return make_uint2(e4m3_codes4(mag, nmag) | sg_lo, e4m3_codes4(mag >> 16, nmag >> 16) | sg_hi);
+// four two's-complement q (one per byte, low nibble) -> E4M3 bytes of q 2^-9
+__device__ __forceinline__ uint32_t e4m3_q4(uint32_t b) {
+    const uint32_t s = (b >> 3) & 0x01010101u;                 // 1 where q < 0
+    const uint32_t mag = (b ^ (s * 0x0Fu)) + s;                // |q| in 0..8, no carry out of a byte
+    return mag | (s << 7);
 }
 
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -99,125 +105,159 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 }
 
 template <int BN>
-struct Smem {
-    uint8_t a[kStages][kTileN * kKB];
-    uint8_t b[kStages][BN * kKB];
+struct Ctl {
     float esx[2][BN];                  // epilogue-owned: sx of the group's tokens
     float enqs[2][BN];                 // -qs as float (exact)
-    uint64_t full[kStages], empty[kStages], accf[2], acce[2];
-    uint64_t drain;                    // after a timeout: the MMAs in flight have finished
+    uint64_t afull[kSA], aempty[kSA];  // A buffers: stored / read by the MMAs
+    uint64_t bfull[4], bempty[4];      // token stages: built / read
+    uint64_t cfull[kSC], cempty[kSC];  // code boxes: landed / read by every converter
+    uint64_t accf[2], acce[2];
+    uint64_t drain[2];                 // after a timeout: each issuer's MMAs in flight have finished
     uint64_t never;                    // nothing arrives here (the stall test)
     uint32_t tmem;
     int timeout;
 };
 
 template <int BN>
+constexpr size_t smem_total() {
+    return (size_t)n_stages<BN>() * stage_bytes<BN>() + (size_t)kSC * kCodeBox + sizeof(Ctl<BN>) + 1024;
+}
+
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    w4a4_umma_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ sx, const int32_t *__restrict__ qs,
-                     const uint8_t *__restrict__ packed, const uint32_t *__restrict__ sz, int M, int N, int K,
-                     uint16_t *__restrict__ y, int ldy, int32_t *__restrict__ dbg_I, int32_t *st,
-                     uint32_t wait_limit, int stall) {
+    w4a4_umma_kernel(const __grid_constant__ CUtensorMap tw, const uint8_t *__restrict__ xq,
+                     const float *__restrict__ sx, const int32_t *__restrict__ qs, const uint32_t *__restrict__ sz,
+                     int M, int N, int K, uint16_t *__restrict__ y, int ldy, int32_t *__restrict__ dbg_I,
+                     int32_t *st, uint32_t wait_limit, int stall) {
+    constexpr int S = n_stages<BN>();
+    constexpr int kStage = stage_bytes<BN>();
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128 && S >= 2, "token tile");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    Smem<BN> &sm = *reinterpret_cast<Smem<BN> *>(smem_raw);
+    // stages 1024-aligned (the swizzle pattern is a function of the address)
+    uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *codes = stages + (size_t)S * kStage;                 // kSC boxes of kCodeBox bytes
+    Ctl<BN> &sm = *reinterpret_cast<Ctl<BN> *>(codes + (size_t)kSC * kCodeBox);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * kTileN, t0 = blockIdx.y * BN;
     const int G = K / kGroup;
-    constexpr uint32_t kCols = 2 * (BN <= 32 ? 32 : BN <= 64 ? 64 : 128);
-    constexpr uint32_t kBuf = kCols / 2;
+    // TMEM: two accumulators of kBuf columns, then kSA A buffers of 32
+    constexpr uint32_t kBuf = BN <= 32 ? 32 : BN <= 64 ? 64 : 128;
+    constexpr uint32_t kAcol = 2 * kBuf;
+    constexpr uint32_t kCols = kAcol + 32 * kSA <= 256 ? 256 : 512;
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem, kCols);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            umma::mbar_init(&sm.full[s], kProducers);
-            umma::mbar_init(&sm.empty[s], 1);
+        for (int s = 0; s < kSA; ++s) {
+            umma::mbar_init(&sm.afull[s], kConv);
+            umma::mbar_init(&sm.aempty[s], 1);
+        }
+        for (int s = 0; s < S; ++s) {
+            umma::mbar_init(&sm.bfull[s], kBld);
+            umma::mbar_init(&sm.bempty[s], 1);
+        }
+        for (int c = 0; c < kSC; ++c) {
+            umma::mbar_init(&sm.cfull[c], 1);
+            umma::mbar_init(&sm.cempty[c], kConv);
         }
         for (int b = 0; b < 2; ++b) {
             umma::mbar_init(&sm.accf[b], 1);
             umma::mbar_init(&sm.acce[b], kEpilogue);
+            umma::mbar_init(&sm.drain[b], 1);
         }
-        umma::mbar_init(&sm.drain, 1);
         umma::mbar_init(&sm.never, 1);
         sm.timeout = 0;
         umma::mbar_fence_init();
     }
+    if (warp == kTmaWarp && lane == 0) umma::prefetch_tmap(&tw);
     pdl_launch_dependents();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem;
-    bool issued = false;                          // MMAs issued (MMA lane 0)
+    bool issued = false;                          // MMAs issued (issuer lane 0)
+    int copies = 0;                               // code boxes issued (copy lane 0)
     auto timed_out = [&]() { return *reinterpret_cast<volatile int *>(&sm.timeout) != 0; };
+    auto give_up = [&]() { atomicExch(&sm.timeout, 1); };
 
-    if (warp < 4) {
-        // ------------------------------------------------------------ producers
-        const int r = tid, n = n0 + r;
-        const bool row_ok = n < N;
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(packed + (size_t)(row_ok ? n : 0) * (K / 2));
-        uint4 w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = row_ok ? __ldg(wrow + u) : make_uint4(0, 0, 0, 0);
-        pdl_wait();
-        for (int g = 0; g < G; ++g) {
-            const int s = g % kStages;
-            if (g >= kStages &&
-                (timed_out() || !umma::mbar_wait(&sm.empty[s], ((g / kStages) - 1) & 1, wait_limit))) {
-                atomicExch(&sm.timeout, 1);
+    if (warp < kEpiWarp0) {
+        // ------------------------------------------------------ weight converters
+        // thread = channel r = TMEM lane; its 64 code bytes of a group come
+        // from the code box (row r, 16-byte chunks 4 (l % 2) .. + 3, 128-byte
+        // swizzle); rows past N arrive as zeros
+        const int r = tid;
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        for (int l = 0; l < G; ++l) {
+            const int sa = l % kSA, c = (l >> 1) % kSC;
+            if ((l & 1) == 0 && (timed_out() || !umma::mbar_wait(&sm.cfull[c], ((l >> 1) / kSC) & 1, wait_limit))) {
+                give_up();
                 break;
             }
+            const uint8_t *crow = codes + (size_t)c * kCodeBox + (size_t)r * kAtom;
             uint4 cw[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) cw[u] = w[u];
-            if (row_ok && g + 1 < G) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) w[u] = __ldg(wrow + (g + 1) * 4 + u);
+            for (int u = 0; u < 4; ++u)
+                cw[u] = *reinterpret_cast<const uint4 *>(crow + (((4 * (l & 1) + u) ^ (r & 7)) << 4));
+            // the box's next contents come by TMA (the async proxy): these
+            // reads are fenced against it before the box is released
+            if ((l & 1) == 1 || l + 1 == G) {
+                umma::fence_proxy_async();
+                umma::mbar_arrive(&sm.cempty[c]);
             }
-            // weights: 128 codes of row r -> 8 chunks of 16 E4M3 bytes
-            uint8_t *a = sm.a[s];
+            // 128 codes -> 32 words of bytes: per code word, even k then odd k
+            uint32_t v[32];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const uint2 e0 = e4m3_codes8(cw[u].x), e1 = e4m3_codes8(cw[u].y);
-                const uint2 e2 = e4m3_codes8(cw[u].z), e3 = e4m3_codes8(cw[u].w);
-                *reinterpret_cast<uint4 *>(a + umma::core_offset(r, 2 * u, kKB)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
-                *reinterpret_cast<uint4 *>(a + umma::core_offset(r, 2 * u + 1, kKB)) =
-                    make_uint4(e2.x, e2.y, e3.x, e3.y);
+                const uint32_t w4[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    v[8 * u + 2 * q] = w4[q] & 0x0F0F0F0Fu;
+                    v[8 * u + 2 * q + 1] = (w4[q] >> 4) & 0x0F0F0F0Fu;
+                }
             }
-            // activations: BN tokens x 64 bytes of nibbles -> BN x 128 E4M3 bytes
-            uint8_t *b = sm.b[s];
-            for (int c = tid; c < BN * 4; c += kProducers) {
-                const int t = c >> 2, u = c & 3, m = t0 + t;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (m < M) v = __ldg(reinterpret_cast<const uint4 *>(xq + (size_t)m * (K / 2) + (size_t)g * 64) + u);
-                const uint2 e0 = e4m3_acts8(v.x), e1 = e4m3_acts8(v.y), e2 = e4m3_acts8(v.z), e3 = e4m3_acts8(v.w);
-                *reinterpret_cast<uint4 *>(b + umma::core_offset(t, 2 * u, kKB)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
-                *reinterpret_cast<uint4 *>(b + umma::core_offset(t, 2 * u + 1, kKB)) =
-                    make_uint4(e2.x, e2.y, e3.x, e3.y);
+            if (l >= kSA && (timed_out() || !umma::mbar_wait(&sm.aempty[sa], ((l / kSA) - 1) & 1, wait_limit))) {
+                give_up();
+                break;
             }
-            umma::fence_proxy_async();
-            umma::mbar_arrive(&sm.full[s]);
+            umma::fence_after_sync();
+            umma::tmem_st32(tmem + lane_off + kAcol + (uint32_t)(sa * 32), v);
+            umma::tmem_st_wait();
+            umma::fence_before_sync();
+            umma::mbar_arrive(&sm.afull[sa]);
         }
-    } else if (warp < 12) {
+    } else if (warp < kBldWarp0) {
         // ------------------------------------------------------------ epilogue
         pdl_wait();
         constexpr int kHalf = BN / 2;                 // token columns per warpgroup
+        constexpr int kW = kHalf % 16 == 0 ? 16 : 8;
         const int eq = warp & 3;                      // TMEM lanes 32 eq .. 32 eq + 31
-        const int eh = (warp - 4) >> 2;               // column half
-        const int et = tid - kProducers;              // 0 .. 255
+        const int eh = (warp - kEpiWarp0) >> 2;       // column half
+        const int et = tid - kConv;                   // 0 .. 255
         const int n = n0 + eq * 32 + lane;
         const bool row_ok = n < N;
+        const uint64_t k18 = f2(262144.0f, 262144.0f);
         uint64_t acc[kHalf / 2];
 #pragma unroll
         for (int i = 0; i < kHalf / 2; ++i) acc[i] = 0;
         bool ok = true;
+        // thread et < BN loads token t0 + et's sx, qs one group ahead
+        const bool tok_ok = et < BN && t0 + et < M;
+        const float *sxp = sx + (size_t)(tok_ok ? t0 + et : 0) * G;
+        const int32_t *qsp = qs + (size_t)(tok_ok ? t0 + et : 0) * G;
+        float sx_n = tok_ok ? sxp[0] : 0.0f;
+        int32_t qs_n = tok_ok ? qsp[0] : 0;
         for (int g = 0; g < G; ++g) {
             const int buf = g & 1;
             // the group's token scales into the epilogue's own double buffer; the
             // barrier also orders this write after every epilogue thread's reads
             // of the same buffer two groups ago, and tells every epilogue thread
             // whether any of them has given up (all leave together)
-            for (int t = et; t < BN; t += kEpilogue) {
-                const int m = t0 + t;
-                sm.esx[buf][t] = m < M ? sx[(size_t)m * G + g] : 0.0f;
-                sm.enqs[buf][t] = m < M ? -(float)qs[(size_t)m * G + g] : 0.0f;
+            if (et < BN) {
+                sm.esx[buf][et] = sx_n;
+                sm.enqs[buf][et] = -(float)qs_n;
+                if (tok_ok && g + 1 < G) {
+                    sx_n = sxp[g + 1];
+                    qs_n = qsp[g + 1];
+                }
             }
             uint32_t any_failed;
             asm volatile(
@@ -227,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 : "memory");
             if (any_failed) break;
             if (timed_out() || !umma::mbar_wait(&sm.accf[buf], (g >> 1) & 1, wait_limit)) {
-                atomicExch(&sm.timeout, 1);
+                give_up();
                 ok = false;
                 continue;                             // to the barrier, where all leave
             }
@@ -237,22 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float zn = __half2float(__ushort_as_half((uint16_t)(szw >> 16)));
             const uint64_t s2 = f2(sn, sn), z2 = f2(zn, zn);
 #pragma unroll
-            for (int c0 = 0; c0 < kHalf; c0 += (kHalf < 32 ? kHalf : 32)) {
-                constexpr int kW = kHalf < 32 ? kHalf : 32;
-                uint32_t v[32];
+            for (int c0 = 0; c0 < kHalf; c0 += kW) {
+                uint32_t v[kW];
                 const uint32_t ta = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(buf * kBuf + eh * kHalf + c0);
-                if (kW == 32)
-                    umma::tmem_ld32(ta, *reinterpret_cast<uint32_t(*)[32]>(v));
-                else
-                    umma::tmem_ld16(ta, v);
+                umma::tmem_ld_cols<kW>(ta, *reinterpret_cast<uint32_t(*)[kW]>(v));
                 umma::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < kW; j += 2) {
                     const int t = eh * kHalf + c0 + j;
-                    // I = sum qW - z qs (exact), c = sx * s, acc = fma(I, c, acc)
+                    // I = D 2^18 - z qs (exact), c = sx * s, acc = fma(I, c, acc)
                     const uint64_t nqs2 = *reinterpret_cast<const uint64_t *>(&sm.enqs[buf][t]);
                     const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&sm.esx[buf][t]);
-                    const uint64_t I2 = fma2(z2, nqs2, f2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])));
+                    const uint64_t I2 = fma2(f2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), k18, mul2(z2, nqs2));
                     const uint64_t c2 = mul2(sx2, s2);
                     acc[(c0 + j) / 2] = fma2(I2, c2, acc[(c0 + j) / 2]);
                     if (dbg_I != nullptr && row_ok) {
@@ -274,43 +310,113 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (m + 1 < M) y[(size_t)(m + 1) * ldy + n] = float_to_bf16_bits(__uint_as_float((uint32_t)(acc[i] >> 32)));
             }
         }
-    } else {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp < kMmaWarp) {
+        // ------------------------------------------------------------ token builders
+        // task = (token row t, 16-byte quarter u of the group's 64 code bytes):
+        // 32 codes -> 32 E4M3 bytes, the 16-byte chunks 2 u and 2 u + 1 of row t
         pdl_wait();
+        const int bt = tid - kBldWarp0 * 32;
+        constexpr int kTasks = BN * 4, kPer = (kTasks + kBld - 1) / kBld;
+        auto load = [&](int l, uint4 (&xv)[kPer]) {
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int task = bt + i * kBld, t = task >> 2, u = task & 3, m = t0 + t;
+                xv[i] = (task < kTasks && m < M && l < G)
+                            ? __ldg(reinterpret_cast<const uint4 *>(xq + (size_t)m * (K / 2) + (size_t)l * 64) + u)
+                            : make_uint4(0, 0, 0, 0);
+            }
+        };
+        uint4 xn[kPer];
+        load(0, xn);
+        for (int l = 0; l < G; ++l) {
+            const int s = l % S;
+            uint4 xv[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) xv[i] = xn[i];
+            load(l + 1, xn);
+            if (l >= S && (timed_out() || !umma::mbar_wait(&sm.bempty[s], ((l / S) - 1) & 1, wait_limit))) {
+                give_up();
+                break;
+            }
+            uint8_t *b = stages + (size_t)s * kStage;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int task = bt + i * kBld, t = task >> 2, u = task & 3;
+                if (task >= kTasks) break;
+                const uint32_t w4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+                uint32_t e[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    e[2 * q] = e4m3_q4(w4[q] & 0x0F0F0F0Fu);
+                    e[2 * q + 1] = e4m3_q4((w4[q] >> 4) & 0x0F0F0F0Fu);
+                }
+                uint8_t *row = b + (size_t)(t >> 3) * 1024 + (size_t)(t & 7) * 128;
+                *reinterpret_cast<uint4 *>(row + (((2 * u) ^ (t & 7)) << 4)) = make_uint4(e[0], e[1], e[2], e[3]);
+                *reinterpret_cast<uint4 *>(row + (((2 * u + 1) ^ (t & 7)) << 4)) = make_uint4(e[4], e[5], e[6], e[7]);
+            }
+            umma::fence_proxy_async();
+            umma::mbar_arrive(&sm.bfull[s]);
+        }
+    } else if (warp < kTmaWarp) {
+        // ------------------------------------------------------------ MMA issuers
+        // issuer i takes groups l = i, i + 2, ...: accumulator i, A buffers and
+        // token stages of parity i (kSA and S are even), so each barrier it
+        // polls is at most one phase ahead of the last it saw
+        const int iss = warp - kMmaWarp;
         if (lane == 0) {
-            constexpr uint32_t idesc = umma::instr_desc(0, 0, kTileN, BN);
-            if (stall && !umma::mbar_wait(&sm.never, 0, wait_limit)) atomicExch(&sm.timeout, 1);
-            for (int g = 0; g < G; ++g) {
-                const int s = g % kStages, buf = g & 1;
-                if (timed_out() || !umma::mbar_wait(&sm.full[s], (g / kStages) & 1, wait_limit) ||
-                    (g >= 2 && !umma::mbar_wait(&sm.acce[buf], ((g >> 1) - 1) & 1, wait_limit))) {
-                    atomicExch(&sm.timeout, 1);
+            constexpr uint32_t idesc = umma::instr_desc(0, 0, kTileN, BN);   // e4m3 x e4m3 -> f32
+            if (stall && iss == 0 && !umma::mbar_wait(&sm.never, 0, wait_limit)) give_up();
+            for (int l = iss; l < G; l += 2) {
+                const int sa = l % kSA, sb = l % S, buf = l & 1;
+                if (timed_out() || !umma::mbar_wait(&sm.afull[sa], (l / kSA) & 1, wait_limit) ||
+                    !umma::mbar_wait(&sm.bfull[sb], (l / S) & 1, wait_limit) ||
+                    (l >= 2 && !umma::mbar_wait(&sm.acce[buf], ((l >> 1) - 1) & 1, wait_limit))) {
+                    give_up();
                     break;
                 }
                 umma::fence_after_sync();
-                const uint32_t a0 = umma::smem_addr(sm.a[s]), b0 = umma::smem_addr(sm.b[s]);
+                const uint64_t db = desc_sw128(umma::smem_addr(stages + (size_t)sb * kStage));
+                const uint32_t a0 = tmem + kAcol + (uint32_t)(sa * 32);
                 const uint32_t d = tmem + (uint32_t)(buf * kBuf);
 #pragma unroll
-                for (int j = 0; j < kKB / 32; ++j) {       // K = 32 E4M3 = 2 core matrices per MMA
-                    const uint64_t da = umma::smem_desc(a0 + j * 256, 128, (kKB / 16) * 128);
-                    const uint64_t db = umma::smem_desc(b0 + j * 256, 128, (kKB / 16) * 128);
-                    umma::mma_e4m3(d, da, db, idesc, j != 0);
-                }
-                umma::mma_commit(&sm.empty[s]);
+                for (int kk = 0; kk < 4; ++kk)   // K = 32 bytes: 8 TMEM columns of A, +2 in B's address field
+                    umma::mma_e4m3_ta(d, a0 + 8 * kk, db + 2 * kk, idesc, kk != 0 ? 1u : 0u);
+                umma::mma_commit(&sm.aempty[sa]);
+                umma::mma_commit(&sm.bempty[sb]);
                 umma::mma_commit(&sm.accf[buf]);
                 issued = true;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ code boxes
+        if (lane == 0) {
+            const int NP = (G + 1) / 2;
+            for (int p = 0; p < NP; ++p) {
+                const int c = p % kSC;
+                if (p >= kSC && (timed_out() || !umma::mbar_wait(&sm.cempty[c], ((p / kSC) - 1) & 1, wait_limit))) {
+                    give_up();
+                    break;
+                }
+                umma::mbar_arrive_expect_tx(&sm.cfull[c], (uint32_t)kCodeBox);
+                umma::tma_load_2d(codes + (size_t)c * kCodeBox, &tw, 2 * p * (kGroup / 2), n0, &sm.cfull[c]);
+                copies = p + 1;
             }
         }
         __syncwarp();
     }
     umma::fence_before_sync();
     __syncthreads();
-    // after a timeout, the MMAs already issued finish (bounded wait) before
-    // the TMEM they write is freed; sm.timeout is settled at this barrier
+    // after a timeout, the copies and MMAs already issued finish (bounded
+    // waits) before the shared and tensor memory are released; sm.timeout is
+    // settled at this barrier
     if (sm.timeout) {
-        if (warp == kThreads / 32 - 1 && lane == 0 && issued) {
-            umma::mma_commit(&sm.drain);
-            umma::mbar_wait(&sm.drain, 0, kWaitLimit);
+        if (warp == kTmaWarp && lane == 0)
+            for (int p = std::max(0, copies - kSC); p < copies; ++p)
+                umma::mbar_wait(&sm.cfull[p % kSC], (p / kSC) & 1, kWaitLimit);
+        if (warp >= kMmaWarp && warp < kTmaWarp && lane == 0 && issued) {
+            umma::mma_commit(&sm.drain[warp - kMmaWarp]);
+            umma::mbar_wait(&sm.drain[warp - kMmaWarp], 0, kWaitLimit);
         }
         __syncthreads();
     }
@@ -322,23 +428,38 @@ template <int BN>
 int launch_bn(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed, const uint32_t *sz,
               int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st, cudaStream_t stream,
               uint32_t wait_limit, int stall) {
-    const size_t smem = sizeof(Smem<BN>) + 1024;
+    CUtensorMap tw;
+    // the packed codes: rows of K / 2 bytes, boxes of 128 bytes x 128 channels
+    if (byte_tmap_sw128(&tw, packed, N, K / 2, (size_t)K / 2, kTileN)) return QSPEC_ERR_UNSUPPORTED;
+    const size_t smem = smem_total<BN>();
     int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN>), (int)smem);
     if (rc) return rc;
     dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + BN - 1) / BN));
-    return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, xq, sx, qs,
-                      packed, sz, M, N, K, y, ldy, dbg_I, st, wait_limit, stall);
+    return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, tw, xq, sx, qs,
+                      sz, M, N, K, y, ldy, dbg_I, st, wait_limit, stall);
 }
 
 }  // namespace
 
-// Larger-M W4A4 on the tensor cores: token tile of 32, 64 or 128.
+// Larger-M W4A4 on the tensor cores: below 256 tokens ceil(M / 128) token
+// tiles of BN tokens (a multiple of 16, 16 ... 128); from 256 tokens the
+// prefill kernel of w4a4_tc_wide.cu.
 int launch_w4a4_tc(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8_t *packed,
                    const uint32_t *sz, int M, int N, int K, uint16_t *y, int ldy, int32_t *dbg_I, int32_t *st,
                    cudaStream_t stream, uint32_t wait_limit, int stall) {
-    if (M <= 32) return launch_bn<32>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
-    if (M <= 64) return launch_bn<64>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
-    return launch_bn<128>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+    if (M >= 256)          // prefill-sized: the fold bounds it, see w4a4_tc_wide.cu
+        return launch_w4a4_tc_wide(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+    const int tiles = (M + 127) / 128, per = (M + tiles - 1) / tiles, bn = (per + 15) / 16 * 16;
+    switch (bn) {
+        case 16: return launch_bn<16>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+        case 32: return launch_bn<32>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+        case 48: return launch_bn<48>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+        case 64: return launch_bn<64>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+        case 80: return launch_bn<80>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+        case 96: return launch_bn<96>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+        case 112: return launch_bn<112>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+        default: return launch_bn<128>(xq, sx, qs, packed, sz, M, N, K, y, ldy, dbg_I, st, stream, wait_limit, stall);
+    }
 }
 
 }  // namespace qspec

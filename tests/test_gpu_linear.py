@@ -42,7 +42,9 @@ def run_w4a4(x, packed, sz, dev, want_I=True):
     # large K (one token per warp-MMA CTA): W4A4 at 13..32 tokens on the
     # tensor cores, fewer on the warp-MMA kernel with one CTA column per token
     (5, 150, 14336, 15), (16, 200, 14336, 16), (32, 130, 18944, 17), (4, 70, 14336, 18),
-    (12, 90, 14336, 19), (13, 90, 18944, 20)])
+    (12, 90, 14336, 19), (13, 90, 18944, 20),
+    # prefill-sized W4A4 (256 tokens and more) on its own kernel, ragged
+    (300, 130, 1152, 21)])
 def test_small_full_compare(M, N, K, seed):
     dev = need_gpu()
     packed, sz, po, szo = make_layer(N, K, seed, dev)
@@ -56,10 +58,12 @@ def test_small_full_compare(M, N, K, seed):
     assert_w4a16_close(y16, ref, "w4a16 M=%d N=%d K=%d" % (M, N, K))
 
 
-def test_extreme_codes_and_unit_scales():
-    """codes and activations at the ends of their ranges: |I| reaches 128*7*15."""
+@pytest.mark.parametrize("M", [3, 40, 300])
+def test_extreme_codes_and_unit_scales(M):
+    """codes and activations at the ends of their ranges: |I| reaches 128*7*15
+    (warp-MMA, decode-batch tensor-core and prefill tensor-core W4A4 paths)."""
     dev = need_gpu()
-    M, N, K = 3, 64, 512
+    N, K = 160 if M > 3 else 64, 512
     G = K // 128
     rng = np.random.default_rng(0)
     codes = torch.from_numpy(rng.choice([0, 15], (N, K)).astype(np.uint8))

@@ -55,7 +55,8 @@ def test_w4a16_tc_timeout_exit_then_regular_call(M, N, K):
 
 @pytest.mark.parametrize("kernel,M,N,K", [
     ("gemv", 5, 1000, 1024), ("gemv", 16, 20000, 4096),
-    ("gemm", 40, 1000, 1024), ("gemm", 130, 640, 2048)])
+    ("gemm", 16, 1000, 14336), ("gemm", 40, 1000, 1024), ("gemm", 130, 640, 2048),
+    ("gemm", 300, 384, 1024)])
 def test_w4a4_tc_timeout_exit_then_regular_call(kernel, M, N, K):
     dev = need_gpu()
     kid = q.KERNEL_W4A4_GEMV_TC if kernel == "gemv" else q.KERNEL_W4A4_TC
