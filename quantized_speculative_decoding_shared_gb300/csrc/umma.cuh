@@ -233,6 +233,13 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
+__device__ __forceinline__ int ld_peer_s16(const void *local_smem, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));
+    short v;
+    asm volatile("ld.shared::cluster.s16 %0, [%1];\n" : "=h"(v) : "r"(remote) : "memory");
+    return (int)v;
+}
 __device__ __forceinline__ float ld_peer_f32(const void *local_smem, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));

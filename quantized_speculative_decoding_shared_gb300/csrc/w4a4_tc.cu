@@ -38,6 +38,13 @@
 //     token columns each: per group, TMEM -> registers, I and the ordered
 //     fold in packed f32x2; finally bf16;
 //   - warp 18, lane 0, issues the code boxes.
+// When the 128-channel tiles alone would leave SMs idle, a cluster of C CTAs
+// (2 or 4) splits a tile's groups.  The fold must still run over all groups
+// in ascending order, so no rank folds its own part: each stores its groups'
+// exact I (|I| <= 128 * 8 * 15 fits 16 bits) in shared memory, and after a
+// cluster barrier every rank folds a slice of the tile's outputs over all
+// groups, reading the peers' I through distributed shared memory, then a
+// second barrier keeps every rank's I alive until all have read.
 // Bounded waits everywhere (the limit is a kernel argument; a test can also
 // make an MMA issuer wait on a barrier nothing arrives at).  After a timeout
 // (QSPEC_ERR_TIMEOUT) every role leaves its loop -- the epilogue warpgroups
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     w4a4_umma_kernel(const __grid_constant__ CUtensorMap tw, const uint8_t *__restrict__ xq,
                      const float *__restrict__ sx, const int32_t *__restrict__ qs, const uint32_t *__restrict__ sz,
                      int M, int N, int K, uint16_t *__restrict__ y, int ldy, int32_t *__restrict__ dbg_I,
-                     int32_t *st, uint32_t wait_limit, int stall) {
+                     int32_t *st, int C, uint32_t wait_limit, int stall) {
     constexpr int S = n_stages<BN>();
     constexpr int kStage = stage_bytes<BN>();
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128 && S >= 2, "token tile");
@@ -137,9 +144,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *codes = stages + (size_t)S * kStage;                 // kSC boxes of kCodeBox bytes
     Ctl<BN> &sm = *reinterpret_cast<Ctl<BN> *>(codes + (size_t)kSC * kCodeBox);
+    // split groups: this rank's exact I, int16 [group][channel][token]
+    int16_t *ibuf = reinterpret_cast<int16_t *>(reinterpret_cast<uint8_t *>(&sm) + ((sizeof(Ctl<BN>) + 15) & ~size_t(15)));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * kTileN, t0 = blockIdx.y * BN;
+    const int rank = C > 1 ? (int)umma::cluster_rank() : 0;
+    const int n0 = (blockIdx.x / C) * kTileN, t0 = blockIdx.y * BN;
     const int G = K / kGroup;
+    const int g_lo = (int)(((long long)rank * G) / C), g_hi = (int)(((long long)(rank + 1) * G) / C);
+    const int NG = g_hi - g_lo;                          // this CTA's groups
     // TMEM: two accumulators of kBuf columns, then kSA A buffers of 32
     constexpr uint32_t kBuf = BN <= 32 ? 32 : BN <= 64 ? 64 : 128;
     constexpr uint32_t kAcol = 2 * kBuf;
@@ -175,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem;
     bool issued = false;                          // MMAs issued (issuer lane 0)
+    bool epi_ok = false;                          // this epilogue thread saw every group
     int copies = 0;                               // code boxes issued (copy lane 0)
     auto timed_out = [&]() { return *reinterpret_cast<volatile int *>(&sm.timeout) != 0; };
     auto give_up = [&]() { atomicExch(&sm.timeout, 1); };
@@ -186,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // swizzle); rows past N arrive as zeros
         const int r = tid;
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        for (int l = 0; l < G; ++l) {
+        for (int l = 0; l < NG; ++l) {
             const int sa = l % kSA, c = (l >> 1) % kSC;
             if ((l & 1) == 0 && (timed_out() || !umma::mbar_wait(&sm.cfull[c], ((l >> 1) / kSC) & 1, wait_limit))) {
                 give_up();
@@ -199,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cw[u] = *reinterpret_cast<const uint4 *>(crow + (((4 * (l & 1) + u) ^ (r & 7)) << 4));
             // the box's next contents come by TMA (the async proxy): these
             // reads are fenced against it before the box is released
-            if ((l & 1) == 1 || l + 1 == G) {
+            if ((l & 1) == 1 || l + 1 == NG) {
                 umma::fence_proxy_async();
                 umma::mbar_arrive(&sm.cempty[c]);
             }
@@ -241,12 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         // thread et < BN loads token t0 + et's sx, qs one group ahead
         const bool tok_ok = et < BN && t0 + et < M;
-        const float *sxp = sx + (size_t)(tok_ok ? t0 + et : 0) * G;
-        const int32_t *qsp = qs + (size_t)(tok_ok ? t0 + et : 0) * G;
-        float sx_n = tok_ok ? sxp[0] : 0.0f;
-        int32_t qs_n = tok_ok ? qsp[0] : 0;
-        for (int g = 0; g < G; ++g) {
-            const int buf = g & 1;
+        const float *sxp = sx + (size_t)(tok_ok ? t0 + et : 0) * G + g_lo;
+        const int32_t *qsp = qs + (size_t)(tok_ok ? t0 + et : 0) * G + g_lo;
+        float sx_n = tok_ok && NG > 0 ? sxp[0] : 0.0f;
+        int32_t qs_n = tok_ok && NG > 0 ? qsp[0] : 0;
+        for (int l = 0; l < NG; ++l) {
+            const int buf = l & 1, g = g_lo + l;
             // the group's token scales into the epilogue's own double buffer; the
             // barrier also orders this write after every epilogue thread's reads
             // of the same buffer two groups ago, and tells every epilogue thread
@@ -254,9 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (et < BN) {
                 sm.esx[buf][et] = sx_n;
                 sm.enqs[buf][et] = -(float)qs_n;
-                if (tok_ok && g + 1 < G) {
-                    sx_n = sxp[g + 1];
-                    qs_n = qsp[g + 1];
+                if (tok_ok && l + 1 < NG) {
+                    sx_n = sxp[l + 1];
+                    qs_n = qsp[l + 1];
                 }
             }
             uint32_t any_failed;
@@ -266,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 : "r"(ok ? 1u : 0u), "r"(kEpilogue)
                 : "memory");
             if (any_failed) break;
-            if (timed_out() || !umma::mbar_wait(&sm.accf[buf], (g >> 1) & 1, wait_limit)) {
+            if (timed_out() || !umma::mbar_wait(&sm.accf[buf], (l >> 1) & 1, wait_limit)) {
                 give_up();
                 ok = false;
                 continue;                             // to the barrier, where all leave
@@ -289,8 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t nqs2 = *reinterpret_cast<const uint64_t *>(&sm.enqs[buf][t]);
                     const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&sm.esx[buf][t]);
                     const uint64_t I2 = fma2(f2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), k18, mul2(z2, nqs2));
-                    const uint64_t c2 = mul2(sx2, s2);
-                    acc[(c0 + j) / 2] = fma2(I2, c2, acc[(c0 + j) / 2]);
+                    if (C == 1) {
+                        const uint64_t c2 = mul2(sx2, s2);
+                        acc[(c0 + j) / 2] = fma2(I2, c2, acc[(c0 + j) / 2]);
+                    } else {                          // kept for the cross-rank fold
+                        const int row = eq * 32 + lane;
+                        ibuf[((size_t)l * kTileN + row) * BN + t] = (int16_t)__uint_as_float((uint32_t)I2);
+                        ibuf[((size_t)l * kTileN + row) * BN + t + 1] = (int16_t)__uint_as_float((uint32_t)(I2 >> 32));
+                    }
                     if (dbg_I != nullptr && row_ok) {
                         const int m0 = t0 + t;
                         if (m0 < M) dbg_I[((size_t)m0 * N + n) * G + g] = (int32_t)__uint_as_float((uint32_t)I2);
@@ -302,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::fence_before_sync();
             umma::mbar_arrive(&sm.acce[buf]);
         }
-        if (ok && row_ok) {
+        epi_ok = ok;
+        if (C == 1 && ok && row_ok) {
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {
                 const int m = t0 + eh * kHalf + 2 * i;
@@ -321,14 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kPer; ++i) {
                 const int task = bt + i * kBld, t = task >> 2, u = task & 3, m = t0 + t;
-                xv[i] = (task < kTasks && m < M && l < G)
-                            ? __ldg(reinterpret_cast<const uint4 *>(xq + (size_t)m * (K / 2) + (size_t)l * 64) + u)
+                xv[i] = (task < kTasks && m < M && l < NG)
+                            ? __ldg(reinterpret_cast<const uint4 *>(xq + (size_t)m * (K / 2) + (size_t)(g_lo + l) * 64) + u)
                             : make_uint4(0, 0, 0, 0);
             }
         };
         uint4 xn[kPer];
         load(0, xn);
-        for (int l = 0; l < G; ++l) {
+        for (int l = 0; l < NG; ++l) {
             const int s = l % S;
             uint4 xv[kPer];
 #pragma unroll
@@ -366,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = umma::instr_desc(0, 0, kTileN, BN);   // e4m3 x e4m3 -> f32
             if (stall && iss == 0 && !umma::mbar_wait(&sm.never, 0, wait_limit)) give_up();
-            for (int l = iss; l < G; l += 2) {
+            for (int l = iss; l < NG; l += 2) {
                 const int sa = l % kSA, sb = l % S, buf = l & 1;
                 if (timed_out() || !umma::mbar_wait(&sm.afull[sa], (l / kSA) & 1, wait_limit) ||
                     !umma::mbar_wait(&sm.bfull[sb], (l / S) & 1, wait_limit) ||
@@ -391,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ code boxes
         if (lane == 0) {
-            const int NP = (G + 1) / 2;
+            const int NP = (NG + 1) / 2;
             for (int p = 0; p < NP; ++p) {
                 const int c = p % kSC;
                 if (p >= kSC && (timed_out() || !umma::mbar_wait(&sm.cempty[c], ((p / kSC) - 1) & 1, wait_limit))) {
@@ -399,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 umma::mbar_arrive_expect_tx(&sm.cfull[c], (uint32_t)kCodeBox);
-                umma::tma_load_2d(codes + (size_t)c * kCodeBox, &tw, 2 * p * (kGroup / 2), n0, &sm.cfull[c]);
+                umma::tma_load_2d(codes + (size_t)c * kCodeBox, &tw, (g_lo + 2 * p) * (kGroup / 2), n0, &sm.cfull[c]);
                 copies = p + 1;
             }
         }
@@ -420,6 +440,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
     }
+    if (C > 1) {
+        // every rank's I is complete; this rank folds channels
+        // [rank * 128 / C, (rank + 1) * 128 / C) over all groups in ascending
+        // order, each group's I read from the rank that computed it.  The
+        // tokens' sx and the channels' s go to shared memory first (the code
+        // ring is free now).
+        umma::cluster_sync();
+        const bool all_ok = !sm.timeout;
+        const int rows = kTileN / C, r0 = rank * rows;
+        float *sxs = reinterpret_cast<float *>(codes);            // [BN][G]
+        float *ss = sxs + (size_t)BN * G;                          // [rows][G]
+        if (warp >= kEpiWarp0 && warp < kBldWarp0 && all_ok) {
+            const int et = tid - kConv;
+            for (int i = et; i < BN * G; i += kEpilogue) {
+                const int t = i / G, g = i - t * G, m = t0 + t;
+                sxs[i] = m < M ? sx[(size_t)m * G + g] : 0.0f;
+            }
+            for (int i = et; i < rows * G; i += kEpilogue) {
+                const int rr = i / G, g = i - rr * G, n = n0 + r0 + rr;
+                ss[i] = n < N ? __half2float(__ushort_as_half((uint16_t)(__ldg(sz + (size_t)n * G + g) & 0xFFFF)))
+                              : 0.0f;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kEpilogue) : "memory");
+            for (int e = et; e < rows * BN; e += kEpilogue) {
+                const int rr = e / BN, t = e % BN, row = r0 + rr, n = n0 + row, m = t0 + t;
+                if (n >= N || m >= M) continue;
+                const float *sxr = sxs + (size_t)t * G, *sr = ss + (size_t)rr * G;
+                float acc = 0.0f;
+                for (int q = 0; q < C; ++q) {
+                    const int qlo = (int)(((long long)q * G) / C), qhi = (int)(((long long)(q + 1) * G) / C);
+                    const int16_t *ib = &ibuf[(size_t)row * BN + t];
+                    int g = qlo;
+                    for (; g + 4 <= qhi; g += 4) {             // four remote reads in flight
+                        float I[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            I[u] = (float)umma::ld_peer_s16(ib + (size_t)(g + u - qlo) * kTileN * BN, (uint32_t)q);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) acc = __fmaf_rn(I[u], __fmul_rn(sxr[g + u], sr[g + u]), acc);
+                    }
+                    for (; g < qhi; ++g) {
+                        const float I = (float)umma::ld_peer_s16(ib + (size_t)(g - qlo) * kTileN * BN, (uint32_t)q);
+                        acc = __fmaf_rn(I, __fmul_rn(sxr[g], sr[g]), acc);
+                    }
+                }
+                y[(size_t)m * ldy + n] = float_to_bf16_bits(acc);
+            }
+        }
+        (void)epi_ok;
+        umma::cluster_sync();                    // peers' I stay until every rank has read
+    }
     if (tid == 0 && sm.timeout) flag(st, QSPEC_ERR_TIMEOUT);
     if (warp == 0) umma::tmem_free(tmem, kCols);
 }
@@ -431,12 +502,33 @@ int launch_bn(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8
     CUtensorMap tw;
     // the packed codes: rows of K / 2 bytes, boxes of 128 bytes x 128 channels
     if (byte_tmap_sw128(&tw, packed, N, K / 2, (size_t)K / 2, kTileN)) return QSPEC_ERR_UNSUPPORTED;
-    const size_t smem = smem_total<BN>();
-    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN>), (int)smem);
+    const int n_tiles = (N + kTileN - 1) / kTileN, token_tiles = (M + BN - 1) / BN, G = K / kGroup;
+    // split the groups over a cluster of 4 CTAs (one per SM) when the tiles
+    // alone leave SMs idle and a rank's I fits in shared memory -- at 16-token
+    // tiles only: measured 74 -> 39 us (4096 x 14336) and 23 -> 17 us
+    // (4096 x 4096) at 16 tokens, but slower with 2-CTA clusters (6144 x 4096:
+    // 23 -> 28 us) and at 32-token tiles (30 -> 62 us, 30 -> 33 us)
+    const size_t kIbufMax = 227 * 1024 - smem_total<BN>() - 16;
+    int C = 1;
+    if (BN == 16)
+        for (int c : {4})
+        if (n_tiles * token_tiles * c <= sm_count() && 2 * c <= G &&
+            (size_t)((G + c - 1) / c) * kTileN * BN * 2 <= kIbufMax &&
+            (size_t)(BN + kTileN / c) * G * 4 <= (size_t)kSC * kCodeBox) {   // the fold's scale tables
+            C = c;
+            break;
+        }
+    const size_t ibuf = C > 1 ? (size_t)((G + C - 1) / C) * kTileN * BN * 2 + 16 : 0;
+    const size_t smem = smem_total<BN>() + ibuf;
+    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN>), 227 * 1024);
     if (rc) return rc;
-    dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + BN - 1) / BN));
-    return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, tw, xq, sx, qs,
-                      sz, M, N, K, y, ldy, dbg_I, st, wait_limit, stall);
+    if (smem > 227 * 1024) return QSPEC_ERR_SHAPE;
+    dim3 grid((unsigned)(n_tiles * C), (unsigned)token_tiles);
+    if (C == 1)
+        return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, tw, xq, sx,
+                          qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
+    return launch_pdl_cluster("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, C, tw,
+                              xq, sx, qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
 }
 
 }  // namespace

@@ -382,3 +382,23 @@ def test_w4a16_tensor_core_token_tiles(M, N, K, seed):
     y16 = q.linear_w4a16(x.to(dev), packed, sz, dev_status=st)
     assert read_status(st) == 0
     assert_w4a16_close(y16, oracle.linear_w4a16(bits(x), po, szo), "w4a16 M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K,seed", [(16, 384, 1024, 90), (12, 600, 1152, 91), (16, 256, 2048, 92),
+                                        (16, 130, 14336, 93)])
+def test_w4a4_tc_split_groups_bit_exact(M, N, K, seed):
+    """The W4A4 tensor-core kernel with a tile's groups split over a cluster
+    (16-token tiles, few channel tiles; uneven splits at 9 groups): the
+    outputs bit-exact with the oracle's ordered fold."""
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100, outlier_frac=0.01)
+    st = status(dev)
+    xq, sx, qs = q.quant_act_int4(x.to(dev), dev_status=st)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    rc = q.qspec_debug_linear_bounded(q.KERNEL_W4A4_TC, None, xq, sx, qs, packed, sz, M, N, K, y, N, 1 << 22, 0, st)
+    assert rc == 0 and read_status(st) == 0
+    rc, xqo, sxo, qso = oracle.quant_act_int4(bits(x))
+    y4o, _ = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert np.array_equal(bits(y), y4o)
