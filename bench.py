@@ -79,6 +79,7 @@ WORKLOADS = {
                               T=4096, p_std=3.0, q_noise=QWEN_Q_NOISE, seed=3),
 }
 PREFILL = "llama3-8b-prefill-m4096"
+DEFAULT_WORKLOAD = "llama3-8b-decode-b1-g4"
 
 
 def parse_args():
@@ -88,8 +89,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + [PREFILL],
-                    default="llama3-8b-decode-b1-g4")
+                    default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the short timed runs of the other workloads (single-GPU default run)")
     ap.add_argument("--rounds", type=int, default=16, help="distinct captured rounds (RNG round ids)")
     ap.add_argument("--profile-case", choices=["w4a4_m1", "w4a16_m5", "w4a16_m80", "quant", "verify_sample",
                                                "verify_greedy", "kv", "fp8_m5", "w4a4_m4096", "w4a4_m32",
@@ -750,14 +753,12 @@ def cpu_baseline(wl, steps=3):
 
 
 # ---------------------------------------------------------------------------
-def prefill_bench(args):
+def prefill_numbers(dev, steps, warmup):
     """M = 4096 tokens through Llama-3-8B gate/up (4096 -> 14336, stacked as
     28672) and down (14336 -> 4096): W4A4 on the tensor cores (TOPS, exact
     integer products) and W4A16 (bf16 tensor cores); plus batch-256 sampled
-    verification over 128256 tokens at gamma 4."""
+    verification over 128256 tokens at gamma 4. Returns the timings."""
     from quantized_speculative_decoding_shared_gb300 import binding as q
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
     M = 4096
     shapes = [("gate_up_proj", 28672, 4096), ("down_proj", 4096, 14336)]
     mats = {}
@@ -784,29 +785,116 @@ def prefill_bench(args):
     torch.cuda.synchronize()
     flops = sum(2 * M * N * K for _, N, K in shapes)
     g4, g16 = capture(run4, stream), capture(run16, stream)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         time_graph(g4, 1, stream)
     clocks = ClockSampler(dev.index)
     clocks.start()
-    t4 = time_graph(g4, args.steps, stream)
-    t16 = time_graph(g16, args.steps, stream)
+    t4 = time_graph(g4, steps, stream)
+    t16 = time_graph(g16, steps, stream)
     clk = clocks.stop()
     P, Q, d = syn.logits_noisy_draft(256, 4, 128256, 4, device=dev)
     ws = q.verify_workspace(256, 4, 128256, dev)
     gv = capture(lambda: q.verify_sample(P, Q, d, 1, 0, workspace=ws), stream)
-    tv = time_graph(gv, args.steps, stream)
+    tv = time_graph(gv, steps, stream)
     vbytes = 2 * 256 * 9 * 128256
-    peak_hbm, kind = measured_peaks()
-    line = {"metric": "W4A4 INT TOPS (M = 4096)", "value": round(flops / (t4 / 1e3) / 1e12, 2),
-            "unit": "TOPS", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(t4, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int4 x int4 -> exact (e4m3 tensor operands, fp32 = exact int)",
-            "data": "synthetic", "config": {"workload": PREFILL, "M": M, "shapes": shapes},
-            "w4a16": {"TFLOPS": round(flops / (t16 / 1e3) / 1e12, 2), "ms": round(t16, 4)},
+    peak_hbm, _ = measured_peaks()
+    return {"M": M, "shapes": shapes, "w4a4_TOPS": round(flops / (t4 / 1e3) / 1e12, 2),
+            "w4a4_ms": round(t4, 4),
+            "w4a16_TFLOPS": round(flops / (t16 / 1e3) / 1e12, 2), "w4a16_ms": round(t16, 4),
             "verify_b256_g4": {"ms": round(tv, 4), "GB/s": round(vbytes / (tv / 1e3) / 1e9, 1),
                                "frac_hbm": round(vbytes / (tv / 1e3) / 1e9 / peak_hbm, 4)},
             "clocks": clk}
+
+
+def prefill_bench(args):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    r = prefill_numbers(dev, args.steps, args.warmup)
+    line = {"metric": "W4A4 INT TOPS (M = 4096)", "value": r["w4a4_TOPS"],
+            "unit": "TOPS", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": r["w4a4_ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int4 x int4 -> exact (e4m3 tensor operands, fp32 = exact int)",
+            "data": "synthetic", "config": {"workload": PREFILL, "M": r["M"], "shapes": r["shapes"]},
+            "w4a16": {"TFLOPS": r["w4a16_TFLOPS"], "ms": r["w4a16_ms"]},
+            "verify_b256_g4": r["verify_b256_g4"], "clocks": r["clocks"]}
     print(json.dumps(line))
+
+
+def timed_rounds(rnd_obj, stream, R, warmup, steps, barrier=lambda: None, clocks=None):
+    """Eager round (status check), R captured round graphs, W warm-up replays,
+    then K timed replays with CUDA events on the launching stream. Returns
+    (graphs, launches per round, device ms, accepted tokens, clock record)."""
+    from quantized_speculative_decoding_shared_gb300 import binding as qb
+    acc_log = torch.zeros((R, rnd_obj.B), dtype=torch.int32, device=rnd_obj.dev)
+    # eager round first: sets kernel attributes outside capture, checks status
+    with torch.cuda.stream(stream):
+        rnd_obj.run(0)
+    torch.cuda.synchronize()
+    if int(rnd_obj.status.item()) != 0:
+        raise RuntimeError("device status %d after the eager round" % int(rnd_obj.status.item()))
+    # the library's own count of the kernels one round launches (read around
+    # the capture of the first round's graph)
+    n_before = qb.qspec_kernel_launches()
+    graphs = [capture(lambda: rnd_obj.run(0, acc_log[0]), stream)]
+    launches_per_round = qb.qspec_kernel_launches() - n_before
+    graphs += [capture(lambda r=r: rnd_obj.run(r, acc_log[r]), stream) for r in range(1, R)]
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            graphs[i % R].replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(steps):
+            graphs[i % R].replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop() if clocks is not None else None
+    acc = acc_log.cpu().numpy()
+    tokens = int(sum((acc[i % R] + 1).sum() for i in range(steps)))
+    if int(rnd_obj.status.item()) != 0:
+        raise RuntimeError("device status %d" % int(rnd_obj.status.item()))
+    return graphs, launches_per_round, ms, tokens, clk
+
+
+def other_workloads(names, dev, steps=10, warmup=3, R=4):
+    """Short timed runs of the other decode workloads (one at a time, memory
+    released in between) and of the M = 4096 prefill linears, so that one
+    default run carries a device-timed figure for every configuration."""
+    out = {}
+    stream = torch.cuda.Stream(device=dev)
+    for name in names:
+        wl = WORKLOADS[name]
+        rnd_obj = GpuRound(wl, dev)
+        clocks = ClockSampler(dev.index)
+        graphs, lpr, ms, tokens, clk = timed_rounds(rnd_obj, stream, R, warmup, steps,
+                                                    clocks=clocks)
+        t4 = time_graph(capture(rnd_obj.draft_linears_only, stream), 5, stream)
+        t16 = time_graph(capture(rnd_obj.verify_linears_only, stream), 5, stream)
+        out[name] = {"value": round(tokens / (ms / 1e3), 2), "unit": "tokens/s",
+                     "steps": steps, "warmup": warmup, "ms_per_step": round(ms / steps, 4),
+                     "tokens_per_step": tokens / steps, "batch": wl["B"], "gamma": wl["gamma"],
+                     "gpu_launches": lpr * steps,
+                     "draft_step_linears_ms": round(t4, 4), "M_draft": wl["B"],
+                     "verify_pass_linears_ms": round(t16, 4),
+                     "M_verify": wl["B"] * (wl["gamma"] + 1),
+                     "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}}
+        del graphs, rnd_obj
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    r = prefill_numbers(dev, steps, warmup)
+    clk = r.pop("clocks")
+    r["clocks"] = {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+    out[PREFILL] = r
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -867,50 +955,14 @@ def main():
     rnd_obj = GpuRound(wl, dev)
     stream = torch.cuda.Stream(device=dev)
     R = max(1, args.rounds)
-    acc_log = torch.zeros((R, wl["B"]), dtype=torch.int32, device=dev)
-    # eager round first: sets kernel attributes outside capture, checks status
-    with torch.cuda.stream(stream):
-        rnd_obj.run(0)
-    torch.cuda.synchronize()
-    if int(rnd_obj.status.item()) != 0:
-        raise RuntimeError("device status %d after the eager round" % int(rnd_obj.status.item()))
-    # the library's own count of the kernels one round launches (read around
-    # the capture of the first round's graph)
-    from quantized_speculative_decoding_shared_gb300 import binding as qb
-    n_before = qb.qspec_kernel_launches()
-    graphs = [capture(lambda: rnd_obj.run(0, acc_log[0]), stream)]
-    launches_per_round = qb.qspec_kernel_launches() - n_before
-    graphs += [capture(lambda r=r: rnd_obj.run(r, acc_log[r]), stream) for r in range(1, R)]
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    # warm-up, then K timed steps
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % R].replay()
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for i in range(args.steps):
-            graphs[i % R].replay()
-        ev1.record(stream)
-    ev1.synchronize()
-    torch.cuda.synchronize()
-    barrier()
-    ms = ev0.elapsed_time(ev1)
-    clk = clocks.stop()
-    acc = acc_log.cpu().numpy()
-    tokens = int(sum((acc[i % R] + 1).sum() for i in range(args.steps)))
-    if int(rnd_obj.status.item()) != 0:
-        raise RuntimeError("device status %d" % int(rnd_obj.status.item()))
+    graphs, launches_per_round, ms, tokens, clk = timed_rounds(
+        rnd_obj, stream, R, args.warmup, args.steps, barrier, ClockSampler(local))
     sec, tokens = aggregate_over_ranks(ms / 1e3, tokens, dev)
     ms = sec * 1e3
     value = tokens / sec
@@ -983,6 +1035,11 @@ def main():
             "targets": targets(rnd_obj, dev, stream),
             "gpu_launches": launches_per_round * args.steps,
             "clocks": clk}
+    if world == 1 and args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+        del graphs, g4, g16, rnd_obj, dev_in
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["workloads"] = other_workloads([n for n in WORKLOADS if n != args.workload], dev)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line))

@@ -187,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem;
     bool issued = false;                          // MMAs issued (issuer lane 0)
-    bool epi_ok = false;                          // this epilogue thread saw every group
     int copies = 0;                               // code boxes issued (copy lane 0)
     auto timed_out = [&]() { return *reinterpret_cast<volatile int *>(&sm.timeout) != 0; };
     auto give_up = [&]() { atomicExch(&sm.timeout, 1); };
@@ -321,7 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::fence_before_sync();
             umma::mbar_arrive(&sm.acce[buf]);
         }
-        epi_ok = ok;
         if (C == 1 && ok && row_ok) {
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) {
@@ -488,7 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 y[(size_t)m * ldy + n] = float_to_bf16_bits(acc);
             }
         }
-        (void)epi_ok;
         umma::cluster_sync();                    // peers' I stay until every rank has read
     }
     if (tid == 0 && sm.timeout) flag(st, QSPEC_ERR_TIMEOUT);
