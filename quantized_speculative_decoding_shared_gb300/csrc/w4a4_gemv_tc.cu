@@ -311,12 +311,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int g = 2 * pp + gi;
                 const float zf = __half2float(__ushort_as_half((uint16_t)(zw[gi] >> 16)));
                 const float sf = __half2float(__ushort_as_half((uint16_t)(zw[gi] & 0xFFFF)));
+                // no branch inside the plain loop: the tokens' loads and FMAs
+                // interleave (the debug output takes its own loop)
+                if (dbg_I == nullptr) {
 #pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    const float2 xv = sxq[g * MT + t];
-                    const float I = __fmaf_rn(__uint_as_float(dg[t]), 262144.0f, -(zf * xv.y));
-                    acc[t] = __fmaf_rn(I, __fmul_rn(xv.x, sf), acc[t]);
-                    if (dbg_I && n < N && tok0 + t < M) dbg_I[((size_t)(tok0 + t) * N + n) * G + g] = (int32_t)I;
+                    for (int t = 0; t < MT; ++t) {
+                        const float2 xv = sxq[g * MT + t];
+                        const float I = __fmaf_rn(__uint_as_float(dg[t]), 262144.0f, -(zf * xv.y));
+                        acc[t] = __fmaf_rn(I, __fmul_rn(xv.x, sf), acc[t]);
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        const float2 xv = sxq[g * MT + t];
+                        const float I = __fmaf_rn(__uint_as_float(dg[t]), 262144.0f, -(zf * xv.y));
+                        acc[t] = __fmaf_rn(I, __fmul_rn(xv.x, sf), acc[t]);
+                        if (n < N && tok0 + t < M) dbg_I[((size_t)(tok0 + t) * N + n) * G + g] = (int32_t)I;
+                    }
                 }
             }
             if (++pp == P) {

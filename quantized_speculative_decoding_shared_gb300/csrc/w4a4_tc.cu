@@ -32,11 +32,15 @@
 //     activation codes into a B stage in shared memory (K-major, 128-byte
 //     swizzle: 16-byte chunk j of token row t at position j ^ (t % 8));
 //   - warps 16-17, lane 0 of each, issue the 4 MMAs (M = 128, N = BN,
-//     K = 32) of every other group into their own TMEM accumulator (a thread
-//     that issued MMAs waits for them on its own next shared-memory access);
+//     K = 32) of every other group (a thread that issued MMAs waits for them
+//     on its own next shared-memory access); each group has its own TMEM
+//     accumulator, in batches of NB groups (4 at up to 32 tokens, 2 at up to
+//     64, else 1) and two batches in flight;
 //   - warps 4-11, two warpgroups on the same TMEM lanes with half of the
-//     token columns each: per group, TMEM -> registers, I and the ordered
-//     fold in packed f32x2; finally bf16;
+//     token columns each: per batch one barrier round, then per group TMEM ->
+//     registers, I and the ordered fold in packed f32x2; finally bf16 (one
+//     round per group cost ~1 us at 32 tokens, mostly barrier, wait and
+//     scale-load latency);
 //   - warp 18, lane 0, issues the code boxes.
 // When the 128-channel tiles alone would leave SMs idle, a cluster of C CTAs
 // (2 or 4) splits a tile's groups.  The fold must still run over all groups
@@ -53,6 +57,7 @@
 // with bounded waits, and the tensor memory is freed (even if a drain ran
 // out: the next kernel on the SM would otherwise wait for it without bound).
 #include <algorithm>
+#include <type_traits>
 
 #include "qspec_device.cuh"
 #include "qspec_host.h"
@@ -111,14 +116,22 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// accumulator columns of one group and groups per epilogue batch: the
+// epilogue takes NB groups per barrier round, and two batches of NB
+// accumulators (256 TMEM columns) let the MMAs run a batch ahead of it
+template <int BN>
+constexpr int acc_cols() { return BN <= 32 ? 32 : BN <= 64 ? 64 : 128; }
+template <int BN>
+constexpr int batch_groups() { return 128 / acc_cols<BN>(); }
+
 template <int BN>
 struct Ctl {
-    float esx[2][BN];                  // epilogue-owned: sx of the group's tokens
-    float enqs[2][BN];                 // -qs as float (exact)
+    float esx[2][batch_groups<BN>() * BN];   // epilogue-owned: sx of the batch's tokens, [group][token]
+    float enqs[2][batch_groups<BN>() * BN];  // -qs as float (exact)
     uint64_t afull[kSA], aempty[kSA];  // A buffers: stored / read by the MMAs
     uint64_t bfull[4], bempty[4];      // token stages: built / read
     uint64_t cfull[kSC], cempty[kSC];  // code boxes: landed / read by every converter
-    uint64_t accf[2], acce[2];
+    uint64_t accf[2], acce[2];         // accumulator batches: computed / drained
     uint64_t drain[2];                 // after a timeout: each issuer's MMAs in flight have finished
     uint64_t never;                    // nothing arrives here (the stall test)
     uint32_t tmem;
@@ -130,7 +143,9 @@ constexpr size_t smem_total() {
     return (size_t)n_stages<BN>() * stage_bytes<BN>() + (size_t)kSC * kCodeBox + sizeof(Ctl<BN>) + 1024;
 }
 
-template <int BN>
+// kPlain: one rank (C == 1) and no debug output -- the fold then has no
+// branch inside and fewer live registers (no spills at up to 48 tokens)
+template <int BN, bool kPlain>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a4_umma_kernel(const __grid_constant__ CUtensorMap tw, const uint8_t *__restrict__ xq,
                      const float *__restrict__ sx, const int32_t *__restrict__ qs, const uint32_t *__restrict__ sz,
@@ -152,10 +167,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = K / kGroup;
     const int g_lo = (int)(((long long)rank * G) / C), g_hi = (int)(((long long)(rank + 1) * G) / C);
     const int NG = g_hi - g_lo;                          // this CTA's groups
-    // TMEM: two accumulators of kBuf columns, then kSA A buffers of 32
-    constexpr uint32_t kBuf = BN <= 32 ? 32 : BN <= 64 ? 64 : 128;
-    constexpr uint32_t kAcol = 2 * kBuf;
-    constexpr uint32_t kCols = kAcol + 32 * kSA <= 256 ? 256 : 512;
+    // TMEM: two batches of NB accumulators of kBuf columns (256 columns),
+    // then kSA A buffers of 32
+    constexpr uint32_t kBuf = acc_cols<BN>();
+    constexpr int NB = batch_groups<BN>();
+    constexpr uint32_t kAcol = 2 * NB * kBuf;
+    constexpr uint32_t kCols = 512;
+    static_assert(kAcol + 32 * kSA <= kCols && NB * BN <= kEpilogue, "tensor memory plan");
+    const int NBt = (NG + NB - 1) / NB;                  // batches
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem, kCols);
     if (tid == 0) {
@@ -172,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&sm.cempty[c], kConv);
         }
         for (int b = 0; b < 2; ++b) {
-            umma::mbar_init(&sm.accf[b], 1);
+            umma::mbar_init(&sm.accf[b], NB >= 2 ? 2 : 1);     // a commit from each issuer with a part in the batch
             umma::mbar_init(&sm.acce[b], kEpilogue);
             umma::mbar_init(&sm.drain[b], 1);
         }
@@ -251,24 +270,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kHalf / 2; ++i) acc[i] = 0;
         bool ok = true;
-        // thread et < BN loads token t0 + et's sx, qs one group ahead
-        const bool tok_ok = et < BN && t0 + et < M;
-        const float *sxp = sx + (size_t)(tok_ok ? t0 + et : 0) * G + g_lo;
-        const int32_t *qsp = qs + (size_t)(tok_ok ? t0 + et : 0) * G + g_lo;
-        float sx_n = tok_ok && NG > 0 ? sxp[0] : 0.0f;
-        int32_t qs_n = tok_ok && NG > 0 ? qsp[0] : 0;
-        for (int l = 0; l < NG; ++l) {
-            const int buf = l & 1, g = g_lo + l;
-            // the group's token scales into the epilogue's own double buffer; the
-            // barrier also orders this write after every epilogue thread's reads
-            // of the same buffer two groups ago, and tells every epilogue thread
-            // whether any of them has given up (all leave together)
-            if (et < BN) {
-                sm.esx[buf][et] = sx_n;
-                sm.enqs[buf][et] = -(float)qs_n;
-                if (tok_ok && l + 1 < NG) {
-                    sx_n = sxp[l + 1];
-                    qs_n = qsp[l + 1];
+        // thread et < NB * BN loads the sx, qs of token t0 + et % BN, group
+        // et / BN of the next batch, one batch ahead
+        const int tt = et % BN, tj = et / BN;
+        const bool tok_ok = et < NB * BN && t0 + tt < M;
+        const float *sxp = sx + (size_t)(tok_ok ? t0 + tt : 0) * G + g_lo + tj;
+        const int32_t *qsp = qs + (size_t)(tok_ok ? t0 + tt : 0) * G + g_lo + tj;
+        float sx_n = tok_ok && tj < NG ? sxp[0] : 0.0f;
+        int32_t qs_n = tok_ok && tj < NG ? qsp[0] : 0;
+        // the channel's scale words, one batch ahead
+        const uint32_t *szp = sz + (size_t)(row_ok ? n : 0) * G + g_lo;
+        uint32_t szn[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) szn[j] = row_ok && j < NG ? __ldg(szp + j) : 0u;
+        for (int b = 0; b < NBt; ++b) {
+            const int set = b & 1, lb = b * NB, nb = min(NB, NG - lb);
+            // the batch's token scales into the epilogue's own double buffer;
+            // the barrier also orders this write after every epilogue
+            // thread's reads of the same buffer two batches ago, and tells
+            // every epilogue thread whether any of them has given up (all
+            // leave together)
+            if (et < NB * BN) {
+                sm.esx[set][et] = sx_n;
+                sm.enqs[set][et] = -(float)qs_n;
+                if (tok_ok && lb + NB + tj < NG) {
+                    sx_n = sxp[lb + NB];
+                    qs_n = qsp[lb + NB];
                 }
             }
             uint32_t any_failed;
@@ -278,47 +305,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 : "r"(ok ? 1u : 0u), "r"(kEpilogue)
                 : "memory");
             if (any_failed) break;
-            if (timed_out() || !umma::mbar_wait(&sm.accf[buf], (l >> 1) & 1, wait_limit)) {
+            if (timed_out() || !umma::mbar_wait(&sm.accf[set], (b >> 1) & 1, wait_limit)) {
                 give_up();
                 ok = false;
                 continue;                             // to the barrier, where all leave
             }
             umma::fence_after_sync();
-            const uint32_t szw = row_ok ? __ldg(sz + (size_t)n * G + g) : 0u;
-            const float sn = __half2float(__ushort_as_half((uint16_t)(szw & 0xFFFF)));
-            const float zn = __half2float(__ushort_as_half((uint16_t)(szw >> 16)));
-            const uint64_t s2 = f2(sn, sn), z2 = f2(zn, zn);
+            uint32_t szc[NB];
 #pragma unroll
-            for (int c0 = 0; c0 < kHalf; c0 += kW) {
-                uint32_t v[kW];
-                const uint32_t ta = tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)(buf * kBuf + eh * kHalf + c0);
-                umma::tmem_ld_cols<kW>(ta, *reinterpret_cast<uint32_t(*)[kW]>(v));
-                umma::tmem_ld_wait();
+            for (int j = 0; j < NB; ++j) {
+                szc[j] = szn[j];
+                szn[j] = row_ok && lb + NB + j < NG ? __ldg(szp + lb + NB + j) : 0u;
+            }
 #pragma unroll
-                for (int j = 0; j < kW; j += 2) {
-                    const int t = eh * kHalf + c0 + j;
-                    // I = D 2^18 - z qs (exact), c = sx * s, acc = fma(I, c, acc)
-                    const uint64_t nqs2 = *reinterpret_cast<const uint64_t *>(&sm.enqs[buf][t]);
-                    const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&sm.esx[buf][t]);
-                    const uint64_t I2 = fma2(f2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), k18, mul2(z2, nqs2));
-                    if (C == 1) {
-                        const uint64_t c2 = mul2(sx2, s2);
-                        acc[(c0 + j) / 2] = fma2(I2, c2, acc[(c0 + j) / 2]);
-                    } else {                          // kept for the cross-rank fold
-                        const int row = eq * 32 + lane;
-                        ibuf[((size_t)l * kTileN + row) * BN + t] = (int16_t)__uint_as_float((uint32_t)I2);
-                        ibuf[((size_t)l * kTileN + row) * BN + t + 1] = (int16_t)__uint_as_float((uint32_t)(I2 >> 32));
+            for (int j = 0; j < NB; ++j) {
+                if (j >= nb) break;
+                const int l = lb + j, g = g_lo + l;
+                const float sn = __half2float(__ushort_as_half((uint16_t)(szc[j] & 0xFFFF)));
+                const float zn = __half2float(__ushort_as_half((uint16_t)(szc[j] >> 16)));
+                const uint64_t s2 = f2(sn, sn), z2 = f2(zn, zn);
+                const float *esx = &sm.esx[set][j * BN];
+                const float *enqs = &sm.enqs[set][j * BN];
+                // the plain fold has no branch inside, so the pairs' loads and
+                // packed operations interleave (a branch per pair measured
+                // 1.4x slower at 32 and 64 tokens); the split (cross-rank I)
+                // and debug paths take the general loop
+                auto fold = [&](auto plain) {
+#pragma unroll
+                    for (int c0 = 0; c0 < kHalf; c0 += kW) {
+                        uint32_t v[kW];
+                        const uint32_t ta = tmem + ((uint32_t)(eq * 32) << 16) +
+                                            (uint32_t)((set * NB + j) * kBuf + eh * kHalf + c0);
+                        umma::tmem_ld_cols<kW>(ta, *reinterpret_cast<uint32_t(*)[kW]>(v));
+                        umma::tmem_ld_wait();
+#pragma unroll
+                        for (int jj = 0; jj < kW; jj += 2) {
+                            const int t = eh * kHalf + c0 + jj;
+                            // I = D 2^18 - z qs (exact), c = sx * s, acc = fma(I, c, acc)
+                            const uint64_t nqs2 = *reinterpret_cast<const uint64_t *>(&enqs[t]);
+                            const uint64_t I2 =
+                                fma2(f2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])), k18, mul2(z2, nqs2));
+                            if constexpr (decltype(plain)::value) {
+                                const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&esx[t]);
+                                acc[(c0 + jj) / 2] = fma2(I2, mul2(sx2, s2), acc[(c0 + jj) / 2]);
+                            } else {
+                                if (C == 1) {
+                                    const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&esx[t]);
+                                    acc[(c0 + jj) / 2] = fma2(I2, mul2(sx2, s2), acc[(c0 + jj) / 2]);
+                                } else {              // kept for the cross-rank fold
+                                    const int row = eq * 32 + lane;
+                                    ibuf[((size_t)l * kTileN + row) * BN + t] = (int16_t)__uint_as_float((uint32_t)I2);
+                                    ibuf[((size_t)l * kTileN + row) * BN + t + 1] =
+                                        (int16_t)__uint_as_float((uint32_t)(I2 >> 32));
+                                }
+                                if (dbg_I != nullptr && row_ok) {
+                                    const int m0 = t0 + t;
+                                    if (m0 < M) dbg_I[((size_t)m0 * N + n) * G + g] = (int32_t)__uint_as_float((uint32_t)I2);
+                                    if (m0 + 1 < M)
+                                        dbg_I[((size_t)(m0 + 1) * N + n) * G + g] =
+                                            (int32_t)__uint_as_float((uint32_t)(I2 >> 32));
+                                }
+                            }
+                        }
                     }
-                    if (dbg_I != nullptr && row_ok) {
-                        const int m0 = t0 + t;
-                        if (m0 < M) dbg_I[((size_t)m0 * N + n) * G + g] = (int32_t)__uint_as_float((uint32_t)I2);
-                        if (m0 + 1 < M)
-                            dbg_I[((size_t)(m0 + 1) * N + n) * G + g] = (int32_t)__uint_as_float((uint32_t)(I2 >> 32));
-                    }
-                }
+                };
+                fold(std::integral_constant<bool, kPlain>());
             }
             umma::fence_before_sync();
-            umma::mbar_arrive(&sm.acce[buf]);
+            umma::mbar_arrive(&sm.acce[set]);
         }
         if (C == 1 && ok && row_ok) {
 #pragma unroll
@@ -377,31 +431,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kTmaWarp) {
         // ------------------------------------------------------------ MMA issuers
-        // issuer i takes groups l = i, i + 2, ...: accumulator i, A buffers and
-        // token stages of parity i (kSA and S are even), so each barrier it
-        // polls is at most one phase ahead of the last it saw
+        // issuer i takes groups l = i, i + 2, ...: A buffers and token stages
+        // of parity i (kSA and S are even), so each barrier it polls is at
+        // most one phase ahead of the last it saw; the accumulators of a batch
+        // are reused only after the epilogue has drained the batch two back
         const int iss = warp - kMmaWarp;
         if (lane == 0) {
             constexpr uint32_t idesc = umma::instr_desc(0, 0, kTileN, BN);   // e4m3 x e4m3 -> f32
             if (stall && iss == 0 && !umma::mbar_wait(&sm.never, 0, wait_limit)) give_up();
-            for (int l = iss; l < NG; l += 2) {
-                const int sa = l % kSA, sb = l % S, buf = l & 1;
-                if (timed_out() || !umma::mbar_wait(&sm.afull[sa], (l / kSA) & 1, wait_limit) ||
-                    !umma::mbar_wait(&sm.bfull[sb], (l / S) & 1, wait_limit) ||
-                    (l >= 2 && !umma::mbar_wait(&sm.acce[buf], ((l >> 1) - 1) & 1, wait_limit))) {
+            for (int b = 0; b < NBt; ++b) {
+                // batch b: groups lb .. lb + nb - 1 into accumulator set b & 1;
+                // with NB >= 2 both issuers take part (and commit) in every
+                // batch, with NB = 1 the batch's one group belongs to issuer b & 1
+                const int set = b & 1, lb = b * NB, nb = min(NB, NG - lb);
+                if (NB == 1 && set != iss) continue;
+                if (b >= 2 && (timed_out() || !umma::mbar_wait(&sm.acce[set], ((b >> 1) - 1) & 1, wait_limit))) {
                     give_up();
                     break;
                 }
-                umma::fence_after_sync();
-                const uint64_t db = desc_sw128(umma::smem_addr(stages + (size_t)sb * kStage));
-                const uint32_t a0 = tmem + kAcol + (uint32_t)(sa * 32);
-                const uint32_t d = tmem + (uint32_t)(buf * kBuf);
+                bool failed = false;
+                for (int l = lb + ((lb & 1) != iss ? 1 : 0); l < lb + nb; l += 2) {
+                    const int sa = l % kSA, sb = l % S;
+                    if (timed_out() || !umma::mbar_wait(&sm.afull[sa], (l / kSA) & 1, wait_limit) ||
+                        !umma::mbar_wait(&sm.bfull[sb], (l / S) & 1, wait_limit)) {
+                        failed = true;
+                        break;
+                    }
+                    umma::fence_after_sync();
+                    const uint64_t db = desc_sw128(umma::smem_addr(stages + (size_t)sb * kStage));
+                    const uint32_t a0 = tmem + kAcol + (uint32_t)(sa * 32);
+                    const uint32_t d = tmem + (uint32_t)((set * NB + (l - lb)) * kBuf);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)   // K = 32 bytes: 8 TMEM columns of A, +2 in B's address field
-                    umma::mma_e4m3_ta(d, a0 + 8 * kk, db + 2 * kk, idesc, kk != 0 ? 1u : 0u);
-                umma::mma_commit(&sm.aempty[sa]);
-                umma::mma_commit(&sm.bempty[sb]);
-                umma::mma_commit(&sm.accf[buf]);
+                    for (int kk = 0; kk < 4; ++kk)   // K = 32 bytes: 8 TMEM columns of A, +2 in B's address field
+                        umma::mma_e4m3_ta(d, a0 + 8 * kk, db + 2 * kk, idesc, kk != 0 ? 1u : 0u);
+                    umma::mma_commit(&sm.aempty[sa]);
+                    umma::mma_commit(&sm.bempty[sb]);
+                    issued = true;
+                }
+                if (failed) {
+                    give_up();
+                    break;
+                }
+                umma::mma_commit(&sm.accf[set]);   // arrives once this issuer's MMAs so far are done
                 issued = true;
             }
         }
@@ -517,15 +588,21 @@ int launch_bn(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8
         }
     const size_t ibuf = C > 1 ? (size_t)((G + C - 1) / C) * kTileN * BN * 2 + 16 : 0;
     const size_t smem = smem_total<BN>() + ibuf;
-    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN>), 227 * 1024);
-    if (rc) return rc;
     if (smem > 227 * 1024) return QSPEC_ERR_SHAPE;
     dim3 grid((unsigned)(n_tiles * C), (unsigned)token_tiles);
+    if (C == 1 && dbg_I == nullptr) {
+        int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN, true>), 227 * 1024);
+        if (rc) return rc;
+        return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN, true>, grid, dim3(kThreads), smem, stream, tw,
+                          xq, sx, qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
+    }
+    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN, false>), 227 * 1024);
+    if (rc) return rc;
     if (C == 1)
-        return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, tw, xq, sx,
-                          qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
-    return launch_pdl_cluster("qspec_linear_w4a4", w4a4_umma_kernel<BN>, grid, dim3(kThreads), smem, stream, C, tw,
-                              xq, sx, qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
+        return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN, false>, grid, dim3(kThreads), smem, stream, tw,
+                          xq, sx, qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
+    return launch_pdl_cluster("qspec_linear_w4a4", w4a4_umma_kernel<BN, false>, grid, dim3(kThreads), smem, stream,
+                              C, tw, xq, sx, qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
 }
 
 }  // namespace

@@ -251,20 +251,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     umma::tmem_ld16(ta, v);
                 umma::tmem_ld_wait();
+                // no branch inside the plain loop, so the pairs' loads and
+                // packed operations interleave; the debug output takes its own
+                if (dbg_I == nullptr) {
 #pragma unroll
-                for (int j = 0; j < kW; j += 2) {
-                    const int t = eh * kHalf + c0 + j;
-                    // I = sum qW - z qs (exact), c = sx * s, acc = fma(I, c, acc)
-                    const uint64_t nqs2 = *reinterpret_cast<const uint64_t *>(&sm.enqs[buf][t]);
-                    const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&sm.esx[buf][t]);
-                    const uint64_t I2 = fma2(z2, nqs2, f2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])));
-                    const uint64_t c2 = mul2(sx2, s2);
-                    acc[(c0 + j) / 2] = fma2(I2, c2, acc[(c0 + j) / 2]);
-                    if (dbg_I != nullptr && row_ok) {
-                        const int m0 = t0 + t;
-                        if (m0 < M) dbg_I[((size_t)m0 * N + n) * G + g] = (int32_t)__uint_as_float((uint32_t)I2);
-                        if (m0 + 1 < M)
-                            dbg_I[((size_t)(m0 + 1) * N + n) * G + g] = (int32_t)__uint_as_float((uint32_t)(I2 >> 32));
+                    for (int j = 0; j < kW; j += 2) {
+                        const int t = eh * kHalf + c0 + j;
+                        // I = sum qW - z qs (exact), c = sx * s, acc = fma(I, c, acc)
+                        const uint64_t nqs2 = *reinterpret_cast<const uint64_t *>(&sm.enqs[buf][t]);
+                        const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&sm.esx[buf][t]);
+                        const uint64_t I2 = fma2(z2, nqs2, f2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])));
+                        acc[(c0 + j) / 2] = fma2(I2, mul2(sx2, s2), acc[(c0 + j) / 2]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kW; j += 2) {
+                        const int t = eh * kHalf + c0 + j;
+                        const uint64_t nqs2 = *reinterpret_cast<const uint64_t *>(&sm.enqs[buf][t]);
+                        const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&sm.esx[buf][t]);
+                        const uint64_t I2 = fma2(z2, nqs2, f2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])));
+                        acc[(c0 + j) / 2] = fma2(I2, mul2(sx2, s2), acc[(c0 + j) / 2]);
+                        if (row_ok) {
+                            const int m0 = t0 + t;
+                            if (m0 < M) dbg_I[((size_t)m0 * N + n) * G + g] = (int32_t)__uint_as_float((uint32_t)I2);
+                            if (m0 + 1 < M)
+                                dbg_I[((size_t)(m0 + 1) * N + n) * G + g] =
+                                    (int32_t)__uint_as_float((uint32_t)(I2 >> 32));
+                        }
                     }
                 }
             }
