@@ -26,6 +26,7 @@
 // warps' partials in a fixed order and stores bf16.  Larger M: tcgen05
 // (w4a16_tc.cu).
 #include <algorithm>
+#include <type_traits>
 
 #include "qspec_device.cuh"
 #include "qspec_host.h"
@@ -278,32 +279,39 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
         }
     };
 
-    int cj = 0, cstep = 0;                                 // consumer cursor
-    int cur = 0;                                           // tile step being produced
-    for (int base = 0; base < n_items; base += kPrefetch) {
+    // with an even group count the second group of an item needs no test, so
+    // the two groups' unpack and MMAs form one straight block
+    auto consume = [&](auto even_tag) {
+        constexpr bool evenG = decltype(even_tag)::value;      // every item holds two groups
+        int cj = 0, cstep = 0;                                 // consumer cursor
+        int cur = 0;                                           // tile step being produced
+        for (int base = 0; base < n_items; base += kPrefetch) {
 #pragma unroll
-        for (int p = 0; p < kPrefetch; ++p) {
-            const int it = base + p;
-            if (it >= n_items) break;
-            if (cstep != cur) {                            // this warp's first item of the next tile
-                flush(cur);
-                tile_done(cur);
-                cur = cstep;
-            }
-            const int g0 = 2 * (warp + cj * kWarps);
-            const Item c = ring[p];
-            if (it + kPrefetch < n_items) {
-                load_item(pc, ring[p]);
-                advance_prod(pc);
-            }
-            group(c.w00, c.w10, c.z00, c.z10, g0);
-            if (g0 + 1 < G) group(c.w01, c.w11, c.z01, c.z11, g0 + 1);
-            if (++cj == ngw) {
-                cj = 0;
-                ++cstep;
+            for (int p = 0; p < kPrefetch; ++p) {
+                const int it = base + p;
+                if (it >= n_items) break;
+                if (cstep != cur) {                            // this warp's first item of the next tile
+                    flush(cur);
+                    tile_done(cur);
+                    cur = cstep;
+                }
+                const int g0 = 2 * (warp + cj * kWarps);
+                const Item c = ring[p];
+                if (it + kPrefetch < n_items) {
+                    load_item(pc, ring[p]);
+                    advance_prod(pc);
+                }
+                group(c.w00, c.w10, c.z00, c.z10, g0);
+                if (evenG || g0 + 1 < G) group(c.w01, c.w11, c.z01, c.z11, g0 + 1);
+                if (++cj == ngw) {
+                    cj = 0;
+                    ++cstep;
+                }
             }
         }
-    }
+        return cur;
+    };
+    int cur = (G % 2 == 0) ? consume(std::true_type()) : consume(std::false_type());
     // the last tile with items, then the remaining ones (warps without pairs)
     for (; cur < my_tiles; ++cur) {
         flush(cur);
