@@ -67,7 +67,7 @@ constexpr int kEpilogue = 256;
 constexpr int kMmaWarp = (kConv + kEpilogue) / 32, kTmaWarp = kMmaWarp + 2;   // two issuer warps
 constexpr int kThreads = kConv + kEpilogue + 96;
 constexpr int kCodeBox = kTileN * kAtom; // packed codes of two groups for 128 channels
-constexpr int kSC = 4;                   // code boxes in the ring
+constexpr int kSC = 4;                   // code boxes counted when sizing the token stages
 constexpr int kSA = 4;                   // A operand buffers in TMEM (64 columns: one group)
 
 template <int BN>
@@ -75,6 +75,14 @@ constexpr int stage_bytes() { return BN * 2 * kAtom; }       // activations of o
 template <int BN>
 constexpr int n_stages() {   // even: each issuer then uses its own stages
     return std::min(4, (212 * 1024 - kSC * kCodeBox) / stage_bytes<BN>()) & ~1;
+}
+
+// Code boxes in the ring: whatever shared memory the token stages leave (up
+// to 12 boxes, 24 groups in flight); with four boxes the DRAM latency of the
+// copies set the pace.
+template <int BN>
+constexpr int ring_boxes() {
+    return std::min(12, (227 * 1024 - 4096 - n_stages<BN>() * stage_bytes<BN>()) / kCodeBox);
 }
 
 __device__ __forceinline__ uint32_t bf2_sub(uint32_t a, uint32_t b) {
@@ -123,7 +131,7 @@ struct Ctl {
     uint64_t afull[kSA], aempty[kSA];                         // A buffers: converted / read by the MMAs
     uint64_t bfull[4], bempty[4];                             // activation stages: landed / read
     uint64_t accf[2], acce[2];
-    uint64_t cfull[kSC], cempty[kSC];                         // code boxes landed / read by every converter
+    uint64_t cfull[ring_boxes<BN>()], cempty[ring_boxes<BN>()];                         // code boxes landed / read by every converter
     uint64_t drain[2];                 // after a timeout: each issuer's MMAs in flight have finished
     uint64_t never;                    // nothing arrives here (the stall test)
     uint32_t tmem;
@@ -133,7 +141,7 @@ struct Ctl {
 
 template <int BN>
 constexpr size_t smem_total() {
-    return (size_t)n_stages<BN>() * stage_bytes<BN>() + (size_t)kSC * kCodeBox + sizeof(Ctl<BN>) + 1024;
+    return (size_t)n_stages<BN>() * stage_bytes<BN>() + (size_t)ring_boxes<BN>() * kCodeBox + sizeof(Ctl<BN>) + 1024;
 }
 
 template <int BN>
@@ -147,8 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // stages 1024-aligned (the swizzle pattern is a function of the address)
     uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *codes = stages + (size_t)S * kStage;                 // kSC boxes of kCodeBox bytes
-    Ctl<BN> &sm = *reinterpret_cast<Ctl<BN> *>(codes + (size_t)kSC * kCodeBox);
+    constexpr int SC = ring_boxes<BN>();
+    uint8_t *codes = stages + (size_t)S * kStage;                 // SC boxes of kCodeBox bytes
+    Ctl<BN> &sm = *reinterpret_cast<Ctl<BN> *>(codes + (size_t)SC * kCodeBox);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // cluster of C CTAs splits the groups of one 128-channel tile
     const int rank = C > 1 ? (int)umma::cluster_rank() : 0;
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(&sm.bfull[s], 1);
             umma::mbar_init(&sm.bempty[s], 1);
         }
-        for (int c = 0; c < kSC; ++c) {
+        for (int c = 0; c < SC; ++c) {
             umma::mbar_init(&sm.cfull[c], 1);
             umma::mbar_init(&sm.cempty[c], kConv);
         }
@@ -223,9 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int p = 0; p < kD; ++p) {
                 const int l = lb + p;
                 if (l >= NG) break;
-                const int sa = l % kSA, c = (l >> 1) % kSC;
+                const int sa = l % kSA, c = (l >> 1) % SC;
                 // this group's codes (the box holds groups 2 (l / 2), + 1)
-                if ((l & 1) == 0 && !role_wait(&sm.cfull[c], ((l >> 1) / kSC) & 1, wait_limit, &sm.timeout)) {
+                if ((l & 1) == 0 && !role_wait(&sm.cfull[c], ((l >> 1) / SC) & 1, wait_limit, &sm.timeout)) {
                     atomicExch(&sm.timeout, 1);
                     ok = false;
                     break;
@@ -359,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ copies
         const int NP = (NG + 1) / 2;                      // code boxes: two groups each
         if (lane == 0) {
-            // code boxes: the first kSC before the dependency wait
+            // code boxes: the first SC before the dependency wait
             for (int p = 0; p < NP; ++p) {
-                const int c = p % kSC;
-                if (p >= kSC && (timed_out() || !umma::mbar_wait(&sm.cempty[c], ((p / kSC) - 1) & 1, wait_limit))) {
+                const int c = p % SC;
+                if (p >= SC && (timed_out() || !umma::mbar_wait(&sm.cempty[c], ((p / SC) - 1) & 1, wait_limit))) {
                     atomicExch(&sm.timeout, 1);
                     break;
                 }
@@ -394,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // settled at this barrier
     if (sm.timeout) {
         if (warp == kTmaWarp && lane == 0)
-            for (int p = std::max(0, copies - kSC); p < copies; ++p)
-                if (!umma::mbar_wait(&sm.cfull[p % kSC], (p / kSC) & 1, kWaitLimit)) sm.drained = 0;
+            for (int p = std::max(0, copies - SC); p < copies; ++p)
+                if (!umma::mbar_wait(&sm.cfull[p % SC], (p / SC) & 1, kWaitLimit)) sm.drained = 0;
         if (warp == kTmaWarp && lane == 1)
             for (int l = std::max(0, copies - S); l < copies; ++l)
                 if (!umma::mbar_wait(&sm.bfull[l % S], (l / S) & 1, kWaitLimit)) sm.drained = 0;
