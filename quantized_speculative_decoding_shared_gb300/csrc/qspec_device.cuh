@@ -119,9 +119,12 @@ __device__ __forceinline__ float qexp(float x) {
 //     (p in [0.7, 1.5], n >= -47, so p 2^n is a normal number);
 //   - the value is at most 2^32, and below it at most 2^32 - 256, so a 32-bit
 //     conversion covers everything but the row maximum itself.
+//   - no branch: below -32 the weight is 0, selected at the end (the
+//     polynomial runs on -32 instead), so a thread's independent weights
+//     interleave.
 __device__ __forceinline__ uint64_t fixed_weight(float l, float m) {
-    const float x = __fsub_rn(l, m);
-    if (x < -32.0f) return 0;
+    const float x0 = __fsub_rn(l, m);
+    const float x = x0 < -32.0f ? -32.0f : x0;
     const float log2e = __uint_as_float(0x3FB8AA3Bu);
     const float ln2_hi = __uint_as_float(0x3F317200u);
     const float ln2_lo = __uint_as_float(0x35BFBE8Eu);
@@ -139,7 +142,8 @@ __device__ __forceinline__ uint64_t fixed_weight(float l, float m) {
     p = __fmaf_rn(p, r, 1.0f);
     const int e = (int)(__float_as_uint(t) - 0x4B400000u);   // n
     const float v = __fmul_rn(p, __int_as_float((e + 127 + 32) << 23));
-    return v >= 4294967296.0f ? (1ull << 32) : (uint64_t)__float2uint_rn(v);
+    const uint64_t w = v >= 4294967296.0f ? (1ull << 32) : (uint64_t)__float2uint_rn(v);
+    return x0 < -32.0f ? 0ull : w;
 }
 
 // Reciprocal of x within 1 ulp (the PTX rcp.approx instruction; subnormal x

@@ -33,6 +33,7 @@
 // HBM traffic: one read of every logit (B (2 gamma + 1) V bf16) plus L2
 // re-reads of the rows a later phase needs.
 #include <algorithm>
+#include <type_traits>
 
 #include <mutex>
 
@@ -447,21 +448,30 @@ __global__ void __launch_bounds__(kThreads) sample_residual_kernel(
     const int c0 = blockIdx.y * chunk, c1 = min(V, c0 + chunk);
     u128 r = 0;
     unsigned long long e = 0;
-    for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
-        float fp[8], fq[8];
-        load8<VEC>(prow, v0, c1, fp);
-        if (residual) load8<VEC>(qrow, v0, c1, fq);
+    // the residual test is uniform over the CTA: one loop for each case, no
+    // branch between the elements' weights
+    auto walk = [&](auto residual_tag) {
+        constexpr bool kRes = decltype(residual_tag)::value;
+        for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += kSub) {
+            float fp[8], fq[8];
+            load8<VEC>(prow, v0, c1, fp);
+            if constexpr (kRes) load8<VEC>(qrow, v0, c1, fq);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint64_t Ep = fixed_weight(fp[i], mp);
-            e += Ep;
-            if (residual) {
-                uint64_t Eq = fixed_weight(fq[i], mq);
-                u128 a = (u128)Ep * Sq, c = (u128)Eq * Sp;
-                r += a > c ? a - c : (u128)0;
+            for (int i = 0; i < 8; ++i) {
+                uint64_t Ep = fixed_weight(fp[i], mp);
+                e += Ep;
+                if constexpr (kRes) {
+                    uint64_t Eq = fixed_weight(fq[i], mq);
+                    u128 a = (u128)Ep * Sq, c = (u128)Eq * Sp;
+                    r += a > c ? a - c : (u128)0;
+                }
             }
         }
-    }
+    };
+    if (residual)
+        walk(std::true_type());
+    else
+        walk(std::false_type());
     // block sums (u128 via two halves with carry handled by the scan helper)
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
