@@ -428,10 +428,13 @@ int tokens_per_cta(int M, int K) {
 // times (large K leaves room for few tokens per warp-MMA CTA), and 17..32
 // tokens on the larger layers (N >= 6144), where it measured 1.2-2.5x faster
 // than the warp-MMA kernel's several token tiles (LM head at 32 tokens: 216
-// vs 547 us) even with its separate quantiser launch
+// vs 547 us) even with its separate quantiser launch; and from 9 tokens on
+// every layer, where its 16-token tiles with the groups split over 2- or
+// 4-CTA clusters beat two warp-MMA token tiles (16 tokens: 6144 x 4096 30 ->
+// 27 us, 4096 x 4096 25 -> 18 us; 12 tokens, 4096 x 14336: 97 -> 35 us)
 bool use_tc(int M, int N, int K) {
     const int mt = tokens_per_cta(M, K);
-    return (M + mt - 1) / mt > 12 || (M > 16 && N >= 6144);
+    return M >= 9 || (M + mt - 1) / mt > 12 || (M > 16 && N >= 6144);
 }
 
 // warp-MMA path for M <= 32: QSPEC_ERR_SHAPE when the shape does not fit

@@ -571,15 +571,16 @@ int launch_bn(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8
     // the packed codes: rows of K / 2 bytes, boxes of 128 bytes x 128 channels
     if (byte_tmap_sw128(&tw, packed, N, K / 2, (size_t)K / 2, kTileN)) return QSPEC_ERR_UNSUPPORTED;
     const int n_tiles = (N + kTileN - 1) / kTileN, token_tiles = (M + BN - 1) / BN, G = K / kGroup;
-    // split the groups over a cluster of 4 CTAs (one per SM) when the tiles
-    // alone leave SMs idle and a rank's I fits in shared memory -- at 16-token
-    // tiles only: measured 74 -> 39 us (4096 x 14336) and 23 -> 17 us
-    // (4096 x 4096) at 16 tokens, but slower with 2-CTA clusters (6144 x 4096:
-    // 23 -> 28 us) and at 32-token tiles (30 -> 62 us, 30 -> 33 us)
+    // split the groups over a cluster of 4 (else 2) CTAs, one per SM, when
+    // the tiles alone leave SMs idle and a rank's I fits in shared memory --
+    // at 16-token tiles only: measured 74 -> 39 us (4096 x 14336) and 23 -> 17
+    // us (4096 x 4096) at 16 tokens with 4 CTAs, 6144 x 4096 with 2 faster
+    // than unsplit since the folds lost their per-element branches, but
+    // slower at 32-token tiles (6144 x 4096: 23 -> 61 us)
     const size_t kIbufMax = 227 * 1024 - smem_total<BN>() - 16;
     int C = 1;
     if (BN == 16)
-        for (int c : {4})
+        for (int c : {4, 2})
         if (n_tiles * token_tiles * c <= sm_count() && 2 * c <= G &&
             (size_t)((G + c - 1) / c) * kTileN * BN * 2 <= kIbufMax &&
             (size_t)(BN + kTileN / c) * G * 4 <= (size_t)kSC * kCodeBox) {   // the fold's scale tables

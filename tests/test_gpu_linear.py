@@ -386,11 +386,12 @@ def test_w4a16_tensor_core_token_tiles(M, N, K, seed):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("M,N,K,seed", [(16, 384, 1024, 90), (12, 600, 1152, 91), (16, 256, 2048, 92),
-                                        (16, 130, 14336, 93)])
+                                        (16, 130, 14336, 93), (16, 6144, 1024, 94), (11, 5000, 1152, 95)])
 def test_w4a4_tc_split_groups_bit_exact(M, N, K, seed):
     """The W4A4 tensor-core kernel with a tile's groups split over a cluster
-    (16-token tiles, few channel tiles; uneven splits at 9 groups): the
-    outputs bit-exact with the oracle's ordered fold."""
+    (16-token tiles, few channel tiles: 4-CTA clusters, and 2-CTA clusters
+    where 4 would not fit in one wave (39..76 channel tiles); uneven splits
+    at 9 groups): the outputs bit-exact with the oracle's ordered fold."""
     dev = need_gpu()
     packed, sz, po, szo = make_layer(N, K, seed, dev)
     x = syn.activations(M, K, seed + 100, outlier_frac=0.01)
