@@ -240,6 +240,17 @@ __device__ __forceinline__ int ld_peer_s16(const void *local_smem, uint32_t rank
     asm volatile("ld.shared::cluster.s16 %0, [%1];\n" : "=h"(v) : "r"(remote) : "memory");
     return (int)v;
 }
+// 16 bytes (16-byte aligned) from the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint4 ld_peer_v4(const void *local_smem, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
 __device__ __forceinline__ float ld_peer_f32(const void *local_smem, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));

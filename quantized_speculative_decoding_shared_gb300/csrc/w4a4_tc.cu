@@ -143,8 +143,8 @@ constexpr size_t smem_total() {
     return (size_t)n_stages<BN>() * stage_bytes<BN>() + (size_t)kSC * kCodeBox + sizeof(Ctl<BN>) + 1024;
 }
 
-// kPlain: one rank (C == 1) and no debug output -- the fold then has no
-// branch inside and fewer live registers (no spills at up to 48 tokens)
+// kPlain: no debug output -- the folds then have no branch inside and fewer
+// live registers (no spills at up to 48 tokens)
 template <int BN, bool kPlain>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a4_umma_kernel(const __grid_constant__ CUtensorMap tw, const uint8_t *__restrict__ xq,
@@ -330,7 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // packed operations interleave (a branch per pair measured
                 // 1.4x slower at 32 and 64 tokens); the split (cross-rank I)
                 // and debug paths take the general loop
-                auto fold = [&](auto plain) {
+                // mode 0: one rank, the ordered fold; mode 1: split groups,
+                // the exact I kept for the cross-rank fold; mode 2: either,
+                // with the debug output
+                auto fold = [&](auto mode_tag) {
+                    constexpr int kMode = decltype(mode_tag)::value;
 #pragma unroll
                     for (int c0 = 0; c0 < kHalf; c0 += kW) {
                         uint32_t v[kW];
@@ -345,9 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint64_t nqs2 = *reinterpret_cast<const uint64_t *>(&enqs[t]);
                             const uint64_t I2 =
                                 fma2(f2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])), k18, mul2(z2, nqs2));
-                            if constexpr (decltype(plain)::value) {
+                            if constexpr (kMode == 0) {
                                 const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&esx[t]);
                                 acc[(c0 + jj) / 2] = fma2(I2, mul2(sx2, s2), acc[(c0 + jj) / 2]);
+                            } else if constexpr (kMode == 1) {
+                                const int row = eq * 32 + lane;
+                                ibuf[((size_t)l * kTileN + row) * BN + t] = (int16_t)__uint_as_float((uint32_t)I2);
+                                ibuf[((size_t)l * kTileN + row) * BN + t + 1] =
+                                    (int16_t)__uint_as_float((uint32_t)(I2 >> 32));
                             } else {
                                 if (C == 1) {
                                     const uint64_t sx2 = *reinterpret_cast<const uint64_t *>(&esx[t]);
@@ -369,7 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 };
-                fold(std::integral_constant<bool, kPlain>());
+                if constexpr (!kPlain)
+                    fold(std::integral_constant<int, 2>());
+                else if (C == 1)
+                    fold(std::integral_constant<int, 0>());
+                else
+                    fold(std::integral_constant<int, 1>());
             }
             umma::fence_before_sync();
             umma::mbar_arrive(&sm.acce[set]);
@@ -518,12 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma::cluster_sync();
         const bool all_ok = !sm.timeout;
         const int rows = kTileN / C, r0 = rank * rows;
-        float *sxs = reinterpret_cast<float *>(codes);            // [BN][G]
+        float *sxs = reinterpret_cast<float *>(codes);            // [G][BN]
         float *ss = sxs + (size_t)BN * G;                          // [rows][G]
         if (warp >= kEpiWarp0 && warp < kBldWarp0 && all_ok) {
             const int et = tid - kConv;
             for (int i = et; i < BN * G; i += kEpilogue) {
-                const int t = i / G, g = i - t * G, m = t0 + t;
+                const int g = i / BN, t = i - g * BN, m = t0 + t;
                 sxs[i] = m < M ? sx[(size_t)m * G + g] : 0.0f;
             }
             for (int i = et; i < rows * G; i += kEpilogue) {
@@ -532,29 +546,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                               : 0.0f;
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kEpilogue) : "memory");
-            for (int e = et; e < rows * BN; e += kEpilogue) {
-                const int rr = e / BN, t = e % BN, row = r0 + rr, n = n0 + row, m = t0 + t;
-                if (n >= N || m >= M) continue;
-                const float *sxr = sxs + (size_t)t * G, *sr = ss + (size_t)rr * G;
-                float acc = 0.0f;
+            // task = (channel, 8 consecutive tokens): one 16-byte read of the
+            // eight I per group, four groups' reads in flight
+            constexpr int kCh = BN / 8;
+            for (int e = et; e < rows * kCh; e += kEpilogue) {
+                const int rr = e / kCh, tb = (e - rr * kCh) * 8, row = r0 + rr, n = n0 + row;
+                if (n >= N) continue;
+                const float *sr = ss + (size_t)rr * G;
+                float acc[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
                 for (int q = 0; q < C; ++q) {
                     const int qlo = (int)(((long long)q * G) / C), qhi = (int)(((long long)(q + 1) * G) / C);
-                    const int16_t *ib = &ibuf[(size_t)row * BN + t];
-                    int g = qlo;
-                    for (; g + 4 <= qhi; g += 4) {             // four remote reads in flight
-                        float I[4];
+                    const int16_t *ib = &ibuf[(size_t)row * BN + tb];
+                    for (int g = qlo; g < qhi; g += 4) {
+                        uint4 I8[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
-                            I[u] = (float)umma::ld_peer_s16(ib + (size_t)(g + u - qlo) * kTileN * BN, (uint32_t)q);
+                            I8[u] = g + u < qhi ? umma::ld_peer_v4(ib + (size_t)(g + u - qlo) * kTileN * BN, (uint32_t)q)
+                                                : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) acc = __fmaf_rn(I[u], __fmul_rn(sxr[g + u], sr[g + u]), acc);
-                    }
-                    for (; g < qhi; ++g) {
-                        const float I = (float)umma::ld_peer_s16(ib + (size_t)(g - qlo) * kTileN * BN, (uint32_t)q);
-                        acc = __fmaf_rn(I, __fmul_rn(sxr[g], sr[g]), acc);
+                        for (int u = 0; u < 4; ++u) {
+                            if (g + u >= qhi) break;
+                            const float s = sr[g + u];
+                            const float *sxg = sxs + (size_t)(g + u) * BN + tb;
+                            const uint32_t w[4] = {I8[u].x, I8[u].y, I8[u].z, I8[u].w};
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float I = (float)(int16_t)(uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+                                acc[j] = __fmaf_rn(I, __fmul_rn(sxg[j], s), acc[j]);
+                            }
+                        }
                     }
                 }
-                y[(size_t)m * ldy + n] = float_to_bf16_bits(acc);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (t0 + tb + j < M) y[(size_t)(t0 + tb + j) * ldy + n] = float_to_bf16_bits(acc[j]);
             }
         }
         umma::cluster_sync();                    // peers' I stay until every rank has read
@@ -591,19 +618,16 @@ int launch_bn(const uint8_t *xq, const float *sx, const int32_t *qs, const uint8
     const size_t smem = smem_total<BN>() + ibuf;
     if (smem > 227 * 1024) return QSPEC_ERR_SHAPE;
     dim3 grid((unsigned)(n_tiles * C), (unsigned)token_tiles);
-    if (C == 1 && dbg_I == nullptr) {
-        int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN, true>), 227 * 1024);
+    auto go = [&](auto kern) {
+        int rc = smem_limit_once(reinterpret_cast<const void *>(kern), 227 * 1024);
         if (rc) return rc;
-        return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN, true>, grid, dim3(kThreads), smem, stream, tw,
-                          xq, sx, qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
-    }
-    int rc = smem_limit_once(reinterpret_cast<const void *>(&w4a4_umma_kernel<BN, false>), 227 * 1024);
-    if (rc) return rc;
-    if (C == 1)
-        return launch_pdl("qspec_linear_w4a4", w4a4_umma_kernel<BN, false>, grid, dim3(kThreads), smem, stream, tw,
-                          xq, sx, qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
-    return launch_pdl_cluster("qspec_linear_w4a4", w4a4_umma_kernel<BN, false>, grid, dim3(kThreads), smem, stream,
-                              C, tw, xq, sx, qs, sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
+        if (C == 1)
+            return launch_pdl("qspec_linear_w4a4", kern, grid, dim3(kThreads), smem, stream, tw, xq, sx, qs, sz, M, N,
+                              K, y, ldy, dbg_I, st, C, wait_limit, stall);
+        return launch_pdl_cluster("qspec_linear_w4a4", kern, grid, dim3(kThreads), smem, stream, C, tw, xq, sx, qs,
+                                  sz, M, N, K, y, ldy, dbg_I, st, C, wait_limit, stall);
+    };
+    return dbg_I == nullptr ? go(&w4a4_umma_kernel<BN, true>) : go(&w4a4_umma_kernel<BN, false>);
 }
 
 }  // namespace
