@@ -204,6 +204,40 @@ def test_fused_quant_linear_equals_two_calls(M, N, K, seed):
     assert np.array_equal(bits(y), y4o)
 
 
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K,seed", [(16, 4096, 1024, 60), (16, 6144, 1024, 61), (9, 4096, 1152, 62),
+                                        (24, 19533, 1152, 63), (32, 300, 14336, 64), (13, 600, 2048, 65)])
+def test_fused_quant_tensor_core_plain(M, N, K, seed):
+    """9..32 tokens through qspec_linear_w4a4_bf16 on the tensor-core kernel
+    (16-token tiles, groups split over 4- and 2-CTA clusters, uneven splits;
+    32-token tiles), without the debug output: y, xq, sx and qs bit for bit
+    as the two calls and the oracle."""
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100, outlier_frac=0.01).to(dev)
+    st = status(dev)
+    y, xq, sx, qs = q.linear_w4a4_bf16(x, packed, sz, dev_status=st)
+    assert read_status(st) == 0
+    xq2, sx2, qs2 = q.quant_act_int4(x)
+    y2 = q.linear_w4a4(xq2, sx2, qs2, packed, sz)
+    assert torch.equal(xq, xq2) and torch.equal(qs, qs2) and torch.equal(sx, sx2)
+    assert np.array_equal(bits(y), bits(y2))
+    rc, xqo, sxo, qso = oracle.quant_act_int4(bits(x.cpu()))
+    y4o, _ = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert np.array_equal(bits(y), y4o)
+
+
+@pytest.mark.gpu
+def test_fused_quant_tensor_core_flags_nonfinite():
+    dev = need_gpu()
+    packed, sz, _, _ = make_layer(4096, 1024, 66, dev)
+    x = syn.activations(16, 1024, 67).to(dev)
+    x[7, 300] = float("inf")
+    st = status(dev)
+    q.linear_w4a4_bf16(x, packed, sz, dev_status=st)
+    assert q.STATUS[read_status(st)] == "QSPEC_ERR_NONFINITE"
+
+
 def test_fused_quant_linear_flags_nonfinite():
     dev = need_gpu()
     packed, sz, _, _ = make_layer(64, 256, 37, dev)
