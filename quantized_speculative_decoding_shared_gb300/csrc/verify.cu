@@ -78,6 +78,64 @@ Layout make_layout(int B, int gamma, int V) {
 }
 
 // -------------------------------------------------------------------------
+// Two fixed-point weights at once: the same fp32 operations, rounded the
+// same way, as fixed_weight for each element, with the floating-point steps
+// as packed f32x2 instructions (each lane rounds exactly as the scalar
+// instruction), so the row pass issues fewer instructions per logit.
+// -------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ void fixed_weight2(float l0, float l1, float m, uint64_t &w0, uint64_t &w1) {
+    const uint64_t x0 = sub2(pk2(l0, l1), pk2(m, m));
+    const float xa = lo2(x0) < -32.0f ? -32.0f : lo2(x0), xb = hi2(x0) < -32.0f ? -32.0f : hi2(x0);
+    const uint64_t x = pk2(xa, xb);
+    const uint64_t magic = pk2(12582912.0f, 12582912.0f);
+    const uint64_t t = add2(mul2(x, pk2(__uint_as_float(0x3FB8AA3Bu), __uint_as_float(0x3FB8AA3Bu))), magic);
+    const uint64_t nn = sub2(t, magic) ^ 0x8000000080000000ull;           // -n, exactly
+    uint64_t r = fma2(nn, pk2(__uint_as_float(0x3F317200u), __uint_as_float(0x3F317200u)), x);
+    r = fma2(nn, pk2(__uint_as_float(0x35BFBE8Eu), __uint_as_float(0x35BFBE8Eu)), r);
+    uint64_t p = pk2(__uint_as_float(0x39500D01u), __uint_as_float(0x39500D01u));          // 1/7!
+    p = fma2(p, r, pk2(__uint_as_float(0x3AB60B61u), __uint_as_float(0x3AB60B61u)));      // 1/6!
+    p = fma2(p, r, pk2(__uint_as_float(0x3C088889u), __uint_as_float(0x3C088889u)));      // 1/5!
+    p = fma2(p, r, pk2(__uint_as_float(0x3D2AAAABu), __uint_as_float(0x3D2AAAABu)));      // 1/4!
+    p = fma2(p, r, pk2(__uint_as_float(0x3E2AAAABu), __uint_as_float(0x3E2AAAABu)));      // 1/3!
+    p = fma2(p, r, pk2(0.5f, 0.5f));
+    p = fma2(p, r, pk2(1.0f, 1.0f));
+    p = fma2(p, r, pk2(1.0f, 1.0f));
+    const int ea = (int)(__float_as_uint(lo2(t)) - 0x4B400000u), eb = (int)(__float_as_uint(hi2(t)) - 0x4B400000u);
+    const uint64_t v = mul2(p, pk2(__int_as_float((ea + 127 + 32) << 23), __int_as_float((eb + 127 + 32) << 23)));
+    const float va = lo2(v), vb = hi2(v);
+    const uint64_t wa = va >= 4294967296.0f ? (1ull << 32) : (uint64_t)__float2uint_rn(va);
+    const uint64_t wb = vb >= 4294967296.0f ? (1ull << 32) : (uint64_t)__float2uint_rn(vb);
+    w0 = lo2(x0) < -32.0f ? 0ull : wa;
+    w1 = hi2(x0) < -32.0f ? 0ull : wb;
+}
+
+// -------------------------------------------------------------------------
 // helpers: load 8 logits of a row starting at element v0 (V % 8 == 0 path,
 // else element-wise); missing elements read as -inf.
 // -------------------------------------------------------------------------
@@ -368,7 +426,11 @@ __global__ void __launch_bounds__(kRowThreads, 2) sample_rowstats_kernel(const u
 #pragma unroll
         for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) sum += fixed_weight(f[u][i], m);
+            for (int i = 0; i < 8; i += 2) {
+                uint64_t w0, w1;
+                fixed_weight2(f[u][i], f[u][i + 1], m, w0, w1);
+                sum += w0 + w1;
+            }
     }
     sum = row_reduce(sum, shs, 0ull, [](unsigned long long a, unsigned long long b) { return a + b; });
     if (threadIdx.x == 0) sums[row] = sum;
@@ -457,13 +519,17 @@ __global__ void __launch_bounds__(kThreads) sample_residual_kernel(
             load8<VEC>(prow, v0, c1, fp);
             if constexpr (kRes) load8<VEC>(qrow, v0, c1, fq);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint64_t Ep = fixed_weight(fp[i], mp);
-                e += Ep;
+            for (int i = 0; i < 8; i += 2) {
+                uint64_t Ep[2], Eq[2];
+                fixed_weight2(fp[i], fp[i + 1], mp, Ep[0], Ep[1]);
+                e += Ep[0] + Ep[1];
                 if constexpr (kRes) {
-                    uint64_t Eq = fixed_weight(fq[i], mq);
-                    u128 a = (u128)Ep * Sq, c = (u128)Eq * Sp;
-                    r += a > c ? a - c : (u128)0;
+                    fixed_weight2(fq[i], fq[i + 1], mq, Eq[0], Eq[1]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        u128 a = (u128)Ep[h] * Sq, c = (u128)Eq[h] * Sp;
+                        r += a > c ? a - c : (u128)0;
+                    }
                 }
             }
         }
