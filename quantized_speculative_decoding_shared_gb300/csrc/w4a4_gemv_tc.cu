@@ -274,11 +274,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
         // scale words of the next pair (rows past N read row 0)
         int zstep = 0, zpp = 0;
+        // (both words in one 8-byte load when G is even and sz 8-byte aligned)
+        const bool z64 = (G % 2) == 0 && (reinterpret_cast<uintptr_t>(sz) & 7) == 0;
         auto zload = [&](uint32_t &z0, uint32_t &z1) {
             const int n = (blockIdx.x + zstep * gridDim.x) * 128 + erow;
             const uint32_t *zp = sz + (size_t)(n < N ? n : 0) * G + 2 * zpp;
-            z0 = __ldg(zp);
-            z1 = 2 * zpp + 1 < G ? __ldg(zp + 1) : 0u;
+            if (z64) {
+                const uint2 w = __ldg(reinterpret_cast<const uint2 *>(zp));
+                z0 = w.x;
+                z1 = w.y;
+            } else {
+                z0 = __ldg(zp);
+                z1 = 2 * zpp + 1 < G ? __ldg(zp + 1) : 0u;
+            }
             if (++zpp == P) {
                 zpp = 0;
                 ++zstep;
