@@ -217,12 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // swizzle); rows past N arrive as zeros
         const int r = tid;
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        for (int l = 0; l < NG; ++l) {
-            const int sa = l % kSA, c = (l >> 1) % kSC;
-            if ((l & 1) == 0 && (timed_out() || !umma::mbar_wait(&sm.cfull[c], ((l >> 1) / kSC) & 1, wait_limit))) {
-                give_up();
-                break;
-            }
+        // group l's 128 codes -> 32 words of bytes (per code word, even k then
+        // odd k); false if its code box did not arrive in time
+        auto convert = [&](int l, uint32_t (&v)[32]) {
+            const int c = (l >> 1) % kSC;
+            if ((l & 1) == 0 && (timed_out() || !umma::mbar_wait(&sm.cfull[c], ((l >> 1) / kSC) & 1, wait_limit)))
+                return false;
             const uint8_t *crow = codes + (size_t)c * kCodeBox + (size_t)r * kAtom;
             uint4 cw[4];
 #pragma unroll
@@ -234,8 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma::fence_proxy_async();
                 umma::mbar_arrive(&sm.cempty[c]);
             }
-            // 128 codes -> 32 words of bytes: per code word, even k then odd k
-            uint32_t v[32];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const uint32_t w4[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
@@ -245,16 +243,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[8 * u + 2 * q + 1] = (w4[q] >> 4) & 0x0F0F0F0Fu;
                 }
             }
-            if (l >= kSA && (timed_out() || !umma::mbar_wait(&sm.aempty[sa], ((l / kSA) - 1) & 1, wait_limit))) {
-                give_up();
-                break;
-            }
+            return true;
+        };
+        // group l from cur into its A buffer; the next group is loaded and
+        // unpacked into nxt while the copy to tensor memory is in flight
+        auto step = [&](int l, const uint32_t (&cur)[32], uint32_t (&nxt)[32]) {
+            const int sa = l % kSA;
+            if (l >= kSA && (timed_out() || !umma::mbar_wait(&sm.aempty[sa], ((l / kSA) - 1) & 1, wait_limit)))
+                return false;
             umma::fence_after_sync();
-            umma::tmem_st32(tmem + lane_off + kAcol + (uint32_t)(sa * 32), v);
+            umma::tmem_st32(tmem + lane_off + kAcol + (uint32_t)(sa * 32), cur);
+            const bool next_ok = l + 1 >= NG || convert(l + 1, nxt);
             umma::tmem_st_wait();
             umma::fence_before_sync();
             umma::mbar_arrive(&sm.afull[sa]);
+            return next_ok;
+        };
+        uint32_t va[32], vb[32];
+        bool ok = NG == 0 || convert(0, va);
+        for (int l = 0; ok && l < NG; l += 2) {
+            ok = step(l, va, vb);
+            if (ok && l + 1 < NG) ok = step(l + 1, vb, va);
         }
+        if (!ok) give_up();
     } else if (warp < kBldWarp0) {
         // ------------------------------------------------------------ epilogue
         pdl_wait();
