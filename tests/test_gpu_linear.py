@@ -419,6 +419,27 @@ def test_w4a16_tensor_core_token_tiles(M, N, K, seed):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K,seed", [(3, 19533, 1152, 96), (8, 19533, 1152, 97), (9, 19533, 1152, 98),
+                                        (16, 20000, 2048, 99)])
+def test_w4a4_gemv_tc_forced_bit_exact(M, N, K, seed):
+    """The tensor-memory GEMV (3..16 tokens; 9..16 in a second core-matrix
+    row) forced through the bounded entry, on shapes the dispatcher may now
+    send to the tensor-core kernel: outputs bit-exact with the oracle."""
+    dev = need_gpu()
+    packed, sz, po, szo = make_layer(N, K, seed, dev)
+    x = syn.activations(M, K, seed + 100, outlier_frac=0.01)
+    st = status(dev)
+    xq, sx, qs = q.quant_act_int4(x.to(dev), dev_status=st)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    rc = q.qspec_debug_linear_bounded(q.KERNEL_W4A4_GEMV_TC, None, xq, sx, qs, packed, sz, M, N, K, y, N, 1 << 22, 0,
+                                      st)
+    assert rc == 0 and read_status(st) == 0
+    rc, xqo, sxo, qso = oracle.quant_act_int4(bits(x))
+    y4o, _ = oracle.linear_w4a4(xqo, sxo, po, szo, want_I=True)
+    assert np.array_equal(bits(y), y4o)
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("M,N,K,seed", [(16, 384, 1024, 90), (12, 600, 1152, 91), (16, 256, 2048, 92),
                                         (16, 130, 14336, 93), (16, 6144, 1024, 94), (11, 5000, 1152, 95)])
 def test_w4a4_tc_split_groups_bit_exact(M, N, K, seed):
