@@ -49,6 +49,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from quantized_speculative_decoding_shared_gb300 import synthetic as syn  # noqa: E402
+from quantized_speculative_decoding_shared_gb300.round import QspecRound  # noqa: E402
 
 GROUP = 128
 FALLBACK_HBM_GBS = 6800.0
@@ -299,97 +300,19 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the round on the GPU
 # ---------------------------------------------------------------------------
-class GpuRound:
+class GpuRound(QspecRound):
+    """The library's round harness on a bench workload, plus the algorithmic
+    bytes of its passes (for the roofline)."""
+
     def __init__(self, wl, dev):
-        from quantized_speculative_decoding_shared_gb300 import binding as q
-        self.q = q
-        self.dev = dev
-        sh = wl["shape"]
-        self.B, self.gamma, self.T = wl["B"], wl["gamma"], wl["T"]
-        self.L, self.hidden, self.V = sh["layers"], sh["hidden"], sh["vocab"]
-        self.H, self.D = sh["kv_heads"], sh["head_dim"]
-        self.linears = syn.fused_layer_linears(sh)
-        seed = wl["seed"]
-        B, g, L = self.B, self.gamma, self.L
-        Mv = B * (g + 1)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        # weights: one packed INT4 set per linear, shared by both passes
-        self.w = []
-        for l in range(L):
-            lw = {}
-            for j, (name, N, K) in enumerate(self.linears):
-                codes, s, z = syn.weights(N, K, seed * 100003 + l * 8 + j, device=dev)
-                lw[name] = q.pack_weights(codes, s, z, dev_status=self.status)
-                del codes, s, z
-            self.w.append(lw)
-        codes, s, z = syn.weights(self.V, self.hidden, seed * 100003 + 7777, device=dev)
-        self.lm = q.pack_weights(codes, s, z, dev_status=self.status)
-        del codes, s, z
-        # inputs: draft activations [gamma][L][B][K] per linear, verify [L][Mv][K]
-        self.xd, self.xv = {}, {}
-        for j, (name, N, K) in enumerate(self.linears):
-            self.xd[name] = syn.activations(g * L * B, K, seed * 7 + j, device=dev,
-                                            outlier_frac=wl["outliers"]).view(g, L, B, K)
-            self.xv[name] = syn.activations(L * Mv, K, seed * 11 + j, device=dev,
-                                            outlier_frac=wl["outliers"]).view(L, Mv, K)
-        self.xd_lm = syn.activations(g * B, self.hidden, seed * 13, device=dev,
-                                     outlier_frac=wl["outliers"]).view(g, B, self.hidden)
-        self.xv_lm = syn.activations(Mv, self.hidden, seed * 17, device=dev,
-                                     outlier_frac=wl["outliers"])
-        P, Q, d = syn.logits_noisy_draft(B, g, self.V, seed * 19, device=dev,
-                                         p_std=wl["p_std"], q_noise=wl["q_noise"])
-        self.P, self.Q, self.drafts = P, Q, d
-        self.kc, self.vc = syn.kv_cache(L, B, self.H, self.T, self.D, seed * 23, device=dev)
-        self.kn, self.vn = syn.kv_new(L, B, g, self.H, self.D, seed * 29, device=dev)
-        self.base = syn.base_positions(B, self.T, g, seed * 31, device=dev)
-        # scratch and outputs
-        Ks = sorted({K for _, _, K in self.linears} | {self.hidden})
-        self.qbuf = {K: (torch.empty((B, K // 2), dtype=torch.uint8, device=dev),
-                         torch.empty((B, K // GROUP), dtype=torch.float32, device=dev),
-                         torch.empty((B, K // GROUP), dtype=torch.int32, device=dev)) for K in Ks}
-        self.yd = {name: torch.empty((B, N), dtype=torch.bfloat16, device=dev)
-                   for name, N, _ in self.linears}
-        self.yv = {name: torch.empty((Mv, N), dtype=torch.bfloat16, device=dev)
-                   for name, N, _ in self.linears}
-        self.yd_lm = torch.empty((B, self.V), dtype=torch.bfloat16, device=dev)
-        self.yv_lm = torch.empty((Mv, self.V), dtype=torch.bfloat16, device=dev)
-        self.ws = q.verify_workspace(B, g, self.V, dev)
-        self.n_acc = torch.zeros(B, dtype=torch.int32, device=dev)
-        self.out = torch.zeros((B, g + 1), dtype=torch.int32, device=dev)
-        torch.cuda.synchronize()
-
-    def _check(self, rc, what):
-        if rc != 0:
-            raise RuntimeError("%s returned %s" % (what, self.q.STATUS.get(rc, rc)))
-
-    def _w4a4(self, x, pk, N, K, y):
-        """a2 + a3: quantise the bf16 activations and run the W4A4 linear (one
-        launch on the warp-MMA path; the quantised activations are kept)."""
-        q = self.q
-        xq, sx, qs = self.qbuf[K]
-        M = x.shape[0]
-        self._check(q.qspec_linear_w4a4_bf16(x, K, pk[0], pk[1], M, N, K, y, N, xq, sx, qs, None,
-                                             self.status), "w4a4_bf16")
+        super().__init__(wl["shape"], wl["B"], wl["gamma"], wl["T"], wl["seed"], dev,
+                         outliers=wl["outliers"], p_std=wl["p_std"], q_noise=wl["q_noise"])
 
     def draft_linears_only(self, j=0):
-        """One draft step's W4A4 launches, exactly as the round makes them
-        (kernel timing)."""
-        for l in range(self.L):
-            for name, N, K in self.linears:
-                self._w4a4(self.xd[name][j, l], self.w[l][name], N, K, self.yd[name])
-        self._w4a4(self.xd_lm[j], self.lm, self.V, self.hidden, self.yd_lm)
+        self.draft_linears(j)
 
     def verify_linears_only(self):
-        q = self.q
-        Mv = self.B * (self.gamma + 1)
-        for l in range(self.L):
-            for name, N, K in self.linears:
-                self._check(q.qspec_linear_w4a16(self.xv[name][l], K, self.w[l][name][0],
-                                                 self.w[l][name][1], Mv, N, K, self.yv[name], N,
-                                                 self.status), "w4a16")
-        self._check(q.qspec_linear_w4a16(self.xv_lm, self.hidden, self.lm[0], self.lm[1], Mv,
-                                         self.V, self.hidden, self.yv_lm, self.V, self.status),
-                    "w4a16")
+        self.verify_linears()
 
     def bytes_draft_linears(self):
         b = sum(bytes_w4a4_bf16(self.B, N, K) for _, N, K in self.linears) * self.L
@@ -399,29 +322,6 @@ class GpuRound:
         Mv = self.B * (self.gamma + 1)
         b = sum(bytes_w4a16(Mv, N, K) for _, N, K in self.linears) * self.L
         return b + bytes_w4a16(Mv, self.V, self.hidden)
-
-    def run(self, rnd, acc_slot=None):
-        q = self.q
-        for j in range(self.gamma):
-            for l in range(self.L):
-                for name, N, K in self.linears:
-                    self._w4a4(self.xd[name][j, l], self.w[l][name], N, K, self.yd[name])
-            self._w4a4(self.xd_lm[j], self.lm, self.V, self.hidden, self.yd_lm)
-        self.verify_linears_only()
-        self._check(q.qspec_verify_sample(self.P, self.Q, self.drafts, self.B, self.gamma, self.V,
-                                          1234, rnd, self.n_acc, self.out, self.ws,
-                                          self.ws.numel(), self.status), "verify_sample")
-        self._check(q.qspec_kv_overwrite(self.kc, self.vc, self.kn, self.vn, self.base, self.n_acc,
-                                         self.L, self.B, self.H, self.T, self.D, self.gamma,
-                                         self.status), "kv_overwrite")
-        if acc_slot is not None:
-            acc_slot.copy_(self.n_acc, non_blocking=True)
-
-    def host_inputs(self):
-        """The tensors a step reads from outside: all activations, logits,
-        drafts and cache positions (weights and the cache stay resident)."""
-        t = [self.xd[n] for n, _, _ in self.linears] + [self.xv[n] for n, _, _ in self.linears]
-        return t + [self.xd_lm, self.xv_lm, self.P, self.Q, self.drafts, self.base]
 
 
 def aggregate_over_ranks(seconds, tokens, device):
@@ -839,6 +739,10 @@ def timed_rounds(rnd_obj, stream, R, warmup, steps, barrier=lambda: None, clocks
     launches_per_round = qb.qspec_kernel_launches() - n_before
     graphs += [capture(lambda r=r: rnd_obj.run(r, acc_log[r]), stream) for r in range(1, R)]
     with torch.cuda.stream(stream):
+        # setup: the first launch of a captured graph also uploads it, so
+        # every graph is launched once before the warm-up steps
+        for gr in graphs:
+            gr.replay()
         for i in range(warmup):
             graphs[i % R].replay()
     torch.cuda.synchronize()
