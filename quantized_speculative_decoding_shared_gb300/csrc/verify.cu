@@ -25,7 +25,12 @@
 //            row hitting L2; else memset, then chunk x row kernels for each
 //            with atomics), decisions + residual chunk sums (chunk x
 //            sequence), draw (per sequence)
-//   draft  : the same row statistics over the B draft rows, weight sums and
+//   draft  : rows of at least kDraftClusterMinV logits and fewer than two
+//            rows per SM: one launch, a cluster of 16 (else 8) CTAs per row
+//            (each a slice of the row; the slices' maxima, weight sums and
+//            entropy parts exchanged through distributed shared memory, the
+//            draw in the slice that holds the threshold); otherwise the same
+//            row statistics as above over the B draft rows, weight sums and
 //            entropy parts (chunk x row), the draw on the row's own weights
 //            (Philox slot 16 + step), the features (per row).  SpecKV blog,
 //            architecture section: the confidence and entropy of the draft
@@ -39,6 +44,7 @@
 
 #include "qspec_device.cuh"
 #include "qspec_host.h"
+#include "umma.cuh"
 
 namespace qspec {
 
@@ -157,7 +163,7 @@ __device__ __forceinline__ void load8(const uint16_t *row, int v0, int V, float 
     for (int i = 0; i < 8; ++i) f[i] = (v0 + i < V) ? bf16_bits_to_float(row[v0 + i]) : -INFINITY;
 }
 
-template <typename T>
+template <typename T, int NT = kThreads>
 __device__ __forceinline__ T block_reduce_max(T v, T *sh) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
@@ -167,7 +173,7 @@ __device__ __forceinline__ T block_reduce_max(T v, T *sh) {
     if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
     __syncthreads();
     if (threadIdx.x < 32) {
-        v = threadIdx.x < kThreads / 32 ? sh[threadIdx.x] : sh[0];
+        v = threadIdx.x < NT / 32 ? sh[threadIdx.x] : sh[0];
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
             T u = __shfl_xor_sync(0xffffffffu, v, o);
@@ -178,6 +184,7 @@ __device__ __forceinline__ T block_reduce_max(T v, T *sh) {
     return v;   // valid in thread 0
 }
 
+template <int NT = kThreads>
 __device__ __forceinline__ unsigned long long block_reduce_sum(unsigned long long v,
                                                                unsigned long long *sh) {
 #pragma unroll
@@ -185,7 +192,7 @@ __device__ __forceinline__ unsigned long long block_reduce_sum(unsigned long lon
     if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
     __syncthreads();
     if (threadIdx.x < 32) {
-        v = threadIdx.x < kThreads / 32 ? sh[threadIdx.x] : 0ull;
+        v = threadIdx.x < NT / 32 ? sh[threadIdx.x] : 0ull;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     }
@@ -741,6 +748,246 @@ __global__ void draft_features_kernel(int B, int n_chunks, const uint32_t *__res
     confidence[b] = S ? (float)((double)fixed_weight(m, m) / (double)S) : 0.0f;
 }
 
+// One launch per draft position: a cluster of C CTAs of NT threads per row
+// (16 where the device schedules clusters of 16, else 8), CTA r over the
+// slice [r span, (r + 1) span) of the row (span a multiple of 8).  Each
+// thread loads its pieces of the slice once (all loads in flight together)
+// and keeps them in registers: the maximum, then E_v, their sum, and E_v
+// kept in shared memory (8 span bytes); from those, the entropy part and, in
+// the one CTA whose slice holds the threshold, the draw.  Between the passes every CTA reads
+// the others' partial results out of their shared memory.  The sums are the
+// same integers as in the chunked kernels, so tokens and confidences are the
+// same bits; the entropy's fp32 parts are added per slice.
+constexpr int kDraftClusterMinV = 2048;
+constexpr int kDraftThreads = 256;
+constexpr int kDraftCacheMax = 200 * 1024;   // bytes of E_v one CTA keeps (its slice, 8 bytes each)
+constexpr int kDraftIt = 6;                  // 8-logit pieces a thread holds (span <= kDraftIt * 8 NT)
+
+// inclusive scan of one uint64 per thread over the block (warp shuffles,
+// then the warps' totals in order); `total` gets the block's sum
+template <int NT>
+__device__ __forceinline__ unsigned long long block_scan_u64(unsigned long long v, unsigned long long *wsum,
+                                                             unsigned long long &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    unsigned long long off = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const unsigned long long t = wsum[w];
+        off += w < warp ? t : 0ull;
+        tot += t;
+    }
+    __syncthreads();                           // wsum is free again
+    total = tot;
+    return v + off;
+}
+
+struct __align__(16) DraftPart {
+    uint32_t maxe;              // the slice's largest logit, ordered bits
+    float h;                    // the slice's sum of p log(p + 1e-9)
+    unsigned long long sum;     // the slice's sum of E_v
+};
+
+template <bool VEC, int C, int NT>
+__global__ void __launch_bounds__(NT) draft_cluster_kernel(const uint16_t *__restrict__ Q, int V, int span,
+                                                                 uint64_t seed, uint64_t round, uint32_t slot,
+                                                                 int32_t *__restrict__ token,
+                                                                 float *__restrict__ confidence,
+                                                                 float *__restrict__ entropy, int32_t *st) {
+    pdl_launch_dependents();
+    pdl_wait();
+    extern __shared__ __align__(16) unsigned long long ecache[];   // E_v of the slice, v - c0
+    __shared__ DraftPart part;
+    __shared__ uint32_t shm[NT / 32];
+    __shared__ unsigned long long shs[NT / 32];
+    __shared__ float shh[NT / 32];
+    __shared__ float s_m;
+    __shared__ unsigned long long s_S, s_base, s_own;
+    __shared__ int s_tok;
+    const uint32_t r = umma::cluster_rank();
+    const int b = blockIdx.y;
+    const uint16_t *row = Q + (size_t)b * V;
+    const int c0 = min(V, (int)r * span), c1 = min(V, c0 + span);
+
+    // this thread's pieces: logits v0(it) .. v0(it) + 7, bf16 bits, -inf
+    // past the slice
+    uint4 raw[kDraftIt];
+#pragma unroll
+    for (int it = 0; it < kDraftIt; ++it) {
+        const int v0 = c0 + (it * NT + (int)threadIdx.x) * 8;
+        if (VEC && v0 + 8 <= c1) {
+            raw[it] = __ldg(reinterpret_cast<const uint4 *>(row + v0));
+        } else {
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = v0 + i < c1 ? (uint32_t)row[v0 + i] : 0xFF80u;
+            raw[it] = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+        }
+    }
+    auto unpack = [](const uint4 &u, float (&f)[8]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    };
+
+    // the row maximum (NaN and +inf flagged, as in the row statistics)
+    float m = -INFINITY;
+    bool bad = false;
+#pragma unroll
+    for (int it = 0; it < kDraftIt; ++it) {
+        float f[8];
+        unpack(raw[it], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            bad |= isnan(f[i]) || f[i] == INFINITY;
+            m = fmaxf(m, f[i]);
+        }
+    }
+    if (bad) flag(st, QSPEC_ERR_NONFINITE);
+    const uint32_t me = block_reduce_max<uint32_t, NT>(ordered_bits(m), shm);
+    if (threadIdx.x == 0) part.maxe = me;
+    umma::cluster_sync();
+    if (threadIdx.x == 0) {
+        uint32_t mx = 0;
+        for (int q = 0; q < C; ++q) mx = max(mx, umma::ld_peer_v4(&part, (uint32_t)q).x);
+        s_m = from_ordered_bits(mx);
+    }
+    __syncthreads();
+    const float mrow = s_m;
+    if (mrow == -INFINITY && r == 0 && threadIdx.x == 0) flag(st, QSPEC_ERR_NONFINITE);   // no mass
+
+    // S = sum of E_v, and the sum of the slices before this one
+    unsigned long long s = 0;
+    if (mrow != -INFINITY)
+#pragma unroll
+        for (int it = 0; it < kDraftIt; ++it) {
+            const int v0 = c0 + (it * NT + (int)threadIdx.x) * 8;
+            if (v0 >= c1) break;
+            float f[8];
+            unpack(raw[it], f);
+            unsigned long long E[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                E[i] = fixed_weight(f[i], mrow);   // 0 past the slice (-inf)
+                s += E[i];
+            }
+            ulonglong2 *dst = reinterpret_cast<ulonglong2 *>(ecache + (v0 - c0));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_ulonglong2(E[2 * i], E[2 * i + 1]);
+        }
+    s = block_reduce_sum<NT>(s, shs);
+    if (threadIdx.x == 0) part.sum = s;
+    umma::cluster_sync();
+    if (threadIdx.x == 0) {
+        unsigned long long S = 0, base = 0;
+        for (int q = 0; q < C; ++q) {
+            const uint4 w = umma::ld_peer_v4(&part, (uint32_t)q);
+            const unsigned long long sq = (unsigned long long)w.z | ((unsigned long long)w.w << 32);
+            if (q < (int)r) base += sq;
+            S += sq;
+        }
+        s_S = S;
+        s_base = base;
+        s_own = s;
+    }
+    __syncthreads();
+    const unsigned long long S = s_S;
+
+    // the slice's entropy part, p_v = E_v / S in fp32
+    const float inv = S ? (float)(1.0 / (double)S) : 0.0f;
+    float h = 0.0f;
+    if (S)
+        for (int v0 = c0 + threadIdx.x * 8; v0 < c1; v0 += NT * 8) {
+            const ulonglong2 *src = reinterpret_cast<const ulonglong2 *>(ecache + (v0 - c0));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const ulonglong2 e2 = src[i >> 1];
+                const float p = (float)(i & 1 ? e2.y : e2.x) * inv;
+                h += p * logf(p + 1e-9f);
+            }
+        }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+    if ((threadIdx.x & 31) == 0) shh[threadIdx.x >> 5] = h;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float ht = 0.0f;
+        for (int w = 0; w < NT / 32; ++w) ht += shh[w];
+        part.h = ht;
+    }
+
+    // the draw: v* = min{v : sum_{u<=v} E_u > T}, T = floor(U S / 2^24), in
+    // the slice whose range of prefix sums holds T (every prefix sum is below
+    // S < V 2^33, so 64 bits hold them)
+    const unsigned long long T =
+        (unsigned long long)(((u128)uniform24(seed, round, slot, (uint32_t)b) * S) >> 24);
+    const unsigned long long base = s_base, own = s_own;
+    if (S != 0 && base <= T && T - base < own) {
+        if (threadIdx.x == 0) s_tok = -1;
+        __syncthreads();
+        unsigned long long running = base;
+        for (int s0 = c0; s0 < c1; s0 += NT * 8) {
+            const int v0 = s0 + threadIdx.x * 8;
+            unsigned long long w[8];
+            unsigned long long tsum = 0;
+            if (v0 < c1) {
+                const ulonglong2 *src = reinterpret_cast<const ulonglong2 *>(ecache + (v0 - c0));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const ulonglong2 e2 = src[i];
+                    w[2 * i] = e2.x;
+                    w[2 * i + 1] = e2.y;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = 0;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tsum += w[i];
+            unsigned long long total;
+            const unsigned long long tinc = block_scan_u64<NT>(tsum, shs, total);
+            const unsigned long long texc = running + tinc - tsum;
+            if (running + tinc > T && texc <= T) {
+                unsigned long long cum = texc;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    cum += w[i];
+                    if (cum > T) {
+                        s_tok = v0 + i;
+                        break;
+                    }
+                }
+            }
+            __syncthreads();
+            if (s_tok >= 0) break;
+            running += total;
+        }
+        if (threadIdx.x == 0) token[b] = s_tok >= 0 ? s_tok : c1 - 1;
+    } else if (S == 0 && r == C - 1 && threadIdx.x == 0) {
+        token[b] = V - 1;                      // a row without mass (flagged above)
+    }
+
+    // the features: entropy from the slices' parts in slice order, the
+    // confidence max_v E_v / S as in the chunked path
+    umma::cluster_sync();
+    if (r == 0 && threadIdx.x == 0) {
+        float ht = 0.0f;
+        for (int q = 0; q < C; ++q) ht += umma::ld_peer_f32(&part.h, (uint32_t)q);
+        entropy[b] = -ht;
+        confidence[b] = S ? (float)((double)fixed_weight(mrow, mrow) / (double)S) : 0.0f;
+    }
+    umma::cluster_sync();                      // every CTA's shared memory stays until CTA 0 has read it
+}
+
 }  // namespace
 
 }  // namespace qspec
@@ -975,6 +1222,44 @@ extern "C" size_t qspec_draft_workspace_bytes(int B, int V) {
     return make_layout(B, 0, V).total;
 }
 
+// 16 when clusters of 16 CTAs (a size above the portable 8) can be
+// scheduled for the draft kernel on this device, else 8; settled once per
+// device (both instances get the attribute), before any capture
+static int draft_cluster_size() {
+    static std::mutex mu;
+    static int known[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+    std::lock_guard<std::mutex> lock(mu);
+    if (known[dev] == 0) {
+        const void *k1 = reinterpret_cast<const void *>(draft_cluster_kernel<true, 16, kDraftThreads>);
+        const void *k0 = reinterpret_cast<const void *>(draft_cluster_kernel<false, 16, kDraftThreads>);
+        int c = 8;
+        if (cudaFuncSetAttribute(k1, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+            cudaFuncSetAttribute(k0, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+            smem_limit_once(k1, kDraftCacheMax) == QSPEC_OK && smem_limit_once(k0, kDraftCacheMax) == QSPEC_OK) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(16, 1);
+            cfg.blockDim = dim3(kDraftThreads);
+            cfg.dynamicSmemBytes = kDraftCacheMax;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 16;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n0 = 0, n1 = 0;
+            if (cudaOccupancyMaxActiveClusters(&n1, k1, &cfg) == cudaSuccess && n1 >= 1 &&
+                cudaOccupancyMaxActiveClusters(&n0, k0, &cfg) == cudaSuccess && n0 >= 1)
+                c = 16;
+        }
+        cudaGetLastError();                    // a refused size leaves no error behind
+        known[dev] = c;
+    }
+    return known[dev];
+}
+
 template <bool VEC>
 static int launch_draft(const uint16_t *Q, int B, int V, uint64_t seed, uint64_t round, int step, int32_t *token,
                         float *confidence, float *entropy, const Layout &L, char *ws, int32_t *dev_status,
@@ -987,6 +1272,22 @@ static int launch_draft(const uint16_t *Q, int B, int V, uint64_t seed, uint64_t
     auto *accbuf = reinterpret_cast<int32_t *>(ws + L.off_acc);
     const char *w = "qspec_draft_sample";
     int rc;
+    const int C = B < 2 * sm_count() && V >= kDraftClusterMinV ? draft_cluster_size() : 0;
+    const int span = C ? ((V + C - 1) / C + 7) / 8 * 8 : 0;
+    if (C && (size_t)span * 8 <= (size_t)kDraftCacheMax && span <= kDraftIt * 8 * kDraftThreads) {
+        const uint32_t slot = (uint32_t)(QSPEC_MAX_GAMMA + step);
+        const size_t smem = (size_t)span * 8;
+        if (C == 16)
+            return launch_pdl_cluster(w, draft_cluster_kernel<VEC, 16, kDraftThreads>, dim3(16, (unsigned)B),
+                                      dim3(kDraftThreads), smem, st, 16, Q, V, span, seed, round, slot, token,
+                                      confidence, entropy, dev_status);
+        rc = smem_limit_once(reinterpret_cast<const void *>(draft_cluster_kernel<VEC, 8, kDraftThreads>),
+                             kDraftCacheMax);
+        if (rc) return rc;
+        return launch_pdl_cluster(w, draft_cluster_kernel<VEC, 8, kDraftThreads>, dim3(8, (unsigned)B),
+                                  dim3(kDraftThreads), smem, st, 8, Q, V, span, seed, round, slot, token, confidence,
+                                  entropy, dev_status);
+    }
     if (B >= 2 * sm_count()) {
         rc = launch_pdl(w, sample_rowstats_kernel<VEC>, dim3(B), dim3(kRowThreads), 0, st, Q, Q, B, 0, V, maxenc,
                         sums, dev_status);

@@ -1,8 +1,10 @@
 """Draft-side sampling with the draft statistics: tokens and confidence
 bit-exact against the oracle, entropy within 1e-4 (1 + H) of the oracle's
-fp64 value, on the chunked and the row-per-CTA paths, with V a multiple of 8
-or not; special rows, status codes, and a full round (drafts drawn here,
-then sampled verification) against the oracle."""
+fp64 value, on the one-launch cluster path (V >= 2048, fewer than two rows
+per SM), the chunked path (shorter rows) and the row-per-CTA path (many
+rows), with V a multiple of 8 or not; special rows, status codes on each
+path, and a full round (drafts drawn here, then sampled verification)
+against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -33,9 +35,12 @@ def compare(Q, seed, rnd, step, dev):
 
 
 # (320, 4096) and (310, 999): at least two rows per SM, one CTA per row;
-# the others: rows split into chunks.  V = 1001, 999, 7: element-wise loads.
+# V >= 2048 below that: a cluster of CTAs per row (2048 the smallest, 20001
+# with element-wise loads); shorter rows: rows split into chunks (2047 the
+# longest).  V = 1001, 999, 7: element-wise loads.
 @pytest.mark.parametrize("B,V,seed", [(1, 1024, 0), (3, 1001, 1), (1, 128256, 2), (16, 128256, 3),
-                                      (5, 7, 4), (320, 4096, 5), (310, 999, 6), (32, 152064, 7)])
+                                      (5, 7, 4), (320, 4096, 5), (310, 999, 6), (32, 152064, 7),
+                                      (2, 2048, 8), (2, 2047, 9), (7, 20001, 10)])
 def test_draft_sample_matches_oracle(B, V, seed):
     dev = need_gpu()
     g = torch.Generator().manual_seed(seed)
@@ -74,12 +79,13 @@ def test_draft_deterministic_and_slots():
     assert np.array_equal(a[2], c[2]) and np.array_equal(a[3], c[3])   # statistics do not depend on the uniform
 
 
-def test_draft_status():
+@pytest.mark.parametrize("V", [3000, 1500])            # the cluster path, the chunked path
+def test_draft_status(V):
     dev = need_gpu()
-    Q = torch.randn((4, 3000), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    Q = torch.randn((4, V), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
     for bad in (float("nan"), float("inf")):
         Q2 = Q.clone()
-        Q2[2, 1234] = bad
+        Q2[2, V - 1234] = bad
         assert run(Q2, 0, 0, 1, dev)[0] == q.ERR_NONFINITE
         assert oracle.draft_sample(bits(Q2), 0, 0, 1)[0] == oracle.ERR_NONFINITE
     Q3 = Q.clone()
