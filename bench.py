@@ -97,7 +97,7 @@ def parse_args():
     ap.add_argument("--rounds", type=int, default=16, help="distinct captured rounds (RNG round ids)")
     ap.add_argument("--profile-case", choices=["w4a4_m1", "w4a16_m5", "w4a16_m80", "quant", "verify_sample",
                                                "verify_greedy", "kv", "fp8_m5", "w4a4_m4096", "w4a4_m32",
-                                              "w4a4_m16_down", "w4a4_m16"],
+                                              "w4a4_m16_down", "w4a4_m16", "draft_sample"],
                     help="run one kernel a few times on a single LM-head-sized case (for ncu)")
     ap.add_argument("--profile-reps", type=int, default=3)
     return ap.parse_args()
@@ -152,6 +152,12 @@ def profile_case(name, reps):
         xq, sx, qs = q.quant_act_int4(syn.activations(M, Kk, 51, device=dev))
         for _ in range(reps):
             q.linear_w4a4(xq, sx, qs, packed, sz)
+    elif name == "draft_sample":
+        # one draft position's logits, 16 x 128256 (4 MB: the real size, in L2)
+        Qd = syn.logits_noisy_draft(16, 1, 128256, 98, device=dev)[1][:, 0, :].contiguous()
+        ws = q.draft_workspace(16, 128256, dev)
+        for r in range(reps):
+            q.draft_sample(Qd, 5, r, 1, workspace=ws)
     elif name in ("verify_sample", "verify_greedy"):
         P, Q, d = syn.logits_noisy_draft(256, 4, 128256, 4, device=dev)
         ws = q.verify_workspace(256, 4, 128256, dev)

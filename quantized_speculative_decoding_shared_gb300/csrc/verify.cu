@@ -856,10 +856,12 @@ __global__ void __launch_bounds__(NT) draft_cluster_kernel(const uint16_t *__res
     const uint32_t me = block_reduce_max<uint32_t, NT>(ordered_bits(m), shm);
     if (threadIdx.x == 0) part.maxe = me;
     umma::cluster_sync();
-    if (threadIdx.x == 0) {
-        uint32_t mx = 0;
-        for (int q = 0; q < C; ++q) mx = max(mx, umma::ld_peer_v4(&part, (uint32_t)q).x);
-        s_m = from_ordered_bits(mx);
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {                    // lane q reads CTA q's part: one round trip
+        uint32_t mx = lane < C ? umma::ld_peer_v4(&part, (uint32_t)lane).x : 0u;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) s_m = from_ordered_bits(mx);
     }
     __syncthreads();
     const float mrow = s_m;
@@ -887,17 +889,23 @@ __global__ void __launch_bounds__(NT) draft_cluster_kernel(const uint16_t *__res
     s = block_reduce_sum<NT>(s, shs);
     if (threadIdx.x == 0) part.sum = s;
     umma::cluster_sync();
-    if (threadIdx.x == 0) {
-        unsigned long long S = 0, base = 0;
-        for (int q = 0; q < C; ++q) {
-            const uint4 w = umma::ld_peer_v4(&part, (uint32_t)q);
-            const unsigned long long sq = (unsigned long long)w.z | ((unsigned long long)w.w << 32);
-            if (q < (int)r) base += sq;
-            S += sq;
+    if (threadIdx.x < 32) {
+        unsigned long long sq = 0;
+        if (lane < C) {
+            const uint4 w = umma::ld_peer_v4(&part, (uint32_t)lane);
+            sq = (unsigned long long)w.z | ((unsigned long long)w.w << 32);
         }
-        s_S = S;
-        s_base = base;
-        s_own = s;
+        unsigned long long S = sq, below = lane < (int)r ? sq : 0ull;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            S += __shfl_xor_sync(0xffffffffu, S, o);
+            below += __shfl_xor_sync(0xffffffffu, below, o);
+        }
+        if (lane == 0) {
+            s_S = S;
+            s_base = below;
+            s_own = s;                         // thread 0 holds the block's sum
+        }
     }
     __syncthreads();
     const unsigned long long S = s_S;
@@ -911,7 +919,10 @@ __global__ void __launch_bounds__(NT) draft_cluster_kernel(const uint16_t *__res
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const ulonglong2 e2 = src[i >> 1];
-                const float p = (float)(i & 1 ? e2.y : e2.x) * inv;
+                const unsigned long long E = i & 1 ? e2.y : e2.x;
+                // E <= 2^32: through 32 bits, the same rounding
+                const float Ef = E >> 32 ? 4294967296.0f : __uint2float_rn((uint32_t)E);
+                const float p = Ef * inv;
                 h += p * logf(p + 1e-9f);
             }
         }
@@ -976,14 +987,17 @@ __global__ void __launch_bounds__(NT) draft_cluster_kernel(const uint16_t *__res
         token[b] = V - 1;                      // a row without mass (flagged above)
     }
 
-    // the features: entropy from the slices' parts in slice order, the
-    // confidence max_v E_v / S as in the chunked path
+    // the features: entropy from the slices' parts (a fixed shuffle tree),
+    // the confidence max_v E_v / S as in the chunked path
     umma::cluster_sync();
-    if (r == 0 && threadIdx.x == 0) {
-        float ht = 0.0f;
-        for (int q = 0; q < C; ++q) ht += umma::ld_peer_f32(&part.h, (uint32_t)q);
-        entropy[b] = -ht;
-        confidence[b] = S ? (float)((double)fixed_weight(mrow, mrow) / (double)S) : 0.0f;
+    if (r == 0 && threadIdx.x < 32) {
+        float ht = lane < C ? umma::ld_peer_f32(&part.h, (uint32_t)lane) : 0.0f;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) ht += __shfl_xor_sync(0xffffffffu, ht, o);
+        if (lane == 0) {
+            entropy[b] = -ht;
+            confidence[b] = S ? (float)((double)fixed_weight(mrow, mrow) / (double)S) : 0.0f;
+        }
     }
     umma::cluster_sync();                      // every CTA's shared memory stays until CTA 0 has read it
 }
