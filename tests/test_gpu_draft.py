@@ -36,11 +36,14 @@ def compare(Q, seed, rnd, step, dev):
 
 # (320, 4096) and (310, 999): at least two rows per SM, one CTA per row;
 # V >= 2048 below that: a cluster of CTAs per row (2048 the smallest, 20001
-# with element-wise loads); shorter rows: rows split into chunks (2047 the
-# longest).  V = 1001, 999, 7: element-wise loads.
+# with element-wise loads, 303 rows the most, 196608 the longest row a
+# cluster of 16 holds in registers); shorter rows: rows split into chunks
+# (2047 the longest), as are longer ones (196616).  V = 1001, 999, 7:
+# element-wise loads.
 @pytest.mark.parametrize("B,V,seed", [(1, 1024, 0), (3, 1001, 1), (1, 128256, 2), (16, 128256, 3),
                                       (5, 7, 4), (320, 4096, 5), (310, 999, 6), (32, 152064, 7),
-                                      (2, 2048, 8), (2, 2047, 9), (7, 20001, 10)])
+                                      (2, 2048, 8), (2, 2047, 9), (7, 20001, 10), (303, 2048, 11),
+                                      (2, 196608, 12), (2, 196616, 13)])
 def test_draft_sample_matches_oracle(B, V, seed):
     dev = need_gpu()
     g = torch.Generator().manual_seed(seed)
