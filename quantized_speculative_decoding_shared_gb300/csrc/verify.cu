@@ -26,7 +26,7 @@
 //            with atomics), decisions + residual chunk sums (chunk x
 //            sequence), draw (per sequence)
 //   draft  : rows of at least kDraftClusterMinV logits and fewer than two
-//            rows per SM: one launch, a cluster of 16 (else 8) CTAs per row
+//            rows per SM: one launch, a cluster of 16 CTAs per row
 //            (each a slice of the row; the slices' maxima, weight sums and
 //            entropy parts exchanged through distributed shared memory, the
 //            draw in the slice that holds the threshold); otherwise the same
@@ -748,8 +748,8 @@ __global__ void draft_features_kernel(int B, int n_chunks, const uint32_t *__res
     confidence[b] = S ? (float)((double)fixed_weight(m, m) / (double)S) : 0.0f;
 }
 
-// One launch per draft position: a cluster of C CTAs of NT threads per row
-// (16 where the device schedules clusters of 16, else 8), CTA r over the
+// One launch per draft position: a cluster of C = 16 CTAs of NT threads per
+// row (where the device schedules clusters of 16), CTA r over the
 // slice [r span, (r + 1) span) of the row (span a multiple of 8).  Each
 // thread loads its pieces of the slice once (all loads in flight together)
 // and keeps them in registers: the maximum, then E_v, their sum, and E_v
@@ -1237,18 +1237,19 @@ extern "C" size_t qspec_draft_workspace_bytes(int B, int V) {
 }
 
 // 16 when clusters of 16 CTAs (a size above the portable 8) can be
-// scheduled for the draft kernel on this device, else 8; settled once per
-// device (both instances get the attribute), before any capture
+// scheduled for the draft kernel on this device, else 0 (the chunked path
+// then runs); settled once per device (both instances get the attribute),
+// before any capture
 static int draft_cluster_size() {
     static std::mutex mu;
     static int known[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     std::lock_guard<std::mutex> lock(mu);
     if (known[dev] == 0) {
         const void *k1 = reinterpret_cast<const void *>(draft_cluster_kernel<true, 16, kDraftThreads>);
         const void *k0 = reinterpret_cast<const void *>(draft_cluster_kernel<false, 16, kDraftThreads>);
-        int c = 8;
+        int c = -1;
         if (cudaFuncSetAttribute(k1, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
             cudaFuncSetAttribute(k0, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
             smem_limit_once(k1, kDraftCacheMax) == QSPEC_OK && smem_limit_once(k0, kDraftCacheMax) == QSPEC_OK) {
@@ -1271,7 +1272,7 @@ static int draft_cluster_size() {
         cudaGetLastError();                    // a refused size leaves no error behind
         known[dev] = c;
     }
-    return known[dev];
+    return known[dev] > 0 ? known[dev] : 0;
 }
 
 template <bool VEC>
@@ -1288,18 +1289,11 @@ static int launch_draft(const uint16_t *Q, int B, int V, uint64_t seed, uint64_t
     int rc;
     const int C = B < 2 * sm_count() && V >= kDraftClusterMinV ? draft_cluster_size() : 0;
     const int span = C ? ((V + C - 1) / C + 7) / 8 * 8 : 0;
-    if (C && (size_t)span * 8 <= (size_t)kDraftCacheMax && span <= kDraftIt * 8 * kDraftThreads) {
+    if (C == 16 && (size_t)span * 8 <= (size_t)kDraftCacheMax && span <= kDraftIt * 8 * kDraftThreads) {
         const uint32_t slot = (uint32_t)(QSPEC_MAX_GAMMA + step);
         const size_t smem = (size_t)span * 8;
-        if (C == 16)
-            return launch_pdl_cluster(w, draft_cluster_kernel<VEC, 16, kDraftThreads>, dim3(16, (unsigned)B),
-                                      dim3(kDraftThreads), smem, st, 16, Q, V, span, seed, round, slot, token,
-                                      confidence, entropy, dev_status);
-        rc = smem_limit_once(reinterpret_cast<const void *>(draft_cluster_kernel<VEC, 8, kDraftThreads>),
-                             kDraftCacheMax);
-        if (rc) return rc;
-        return launch_pdl_cluster(w, draft_cluster_kernel<VEC, 8, kDraftThreads>, dim3(8, (unsigned)B),
-                                  dim3(kDraftThreads), smem, st, 8, Q, V, span, seed, round, slot, token, confidence,
+        return launch_pdl_cluster(w, draft_cluster_kernel<VEC, 16, kDraftThreads>, dim3(16, (unsigned)B),
+                                  dim3(kDraftThreads), smem, st, 16, Q, V, span, seed, round, slot, token, confidence,
                                   entropy, dev_status);
     }
     if (B >= 2 * sm_count()) {
