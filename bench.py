@@ -97,7 +97,7 @@ def parse_args():
     ap.add_argument("--rounds", type=int, default=16, help="distinct captured rounds (RNG round ids)")
     ap.add_argument("--profile-case", choices=["w4a4_m1", "w4a16_m5", "w4a16_m80", "quant", "verify_sample",
                                                "verify_greedy", "kv", "fp8_m5", "w4a4_m4096", "w4a4_m32",
-                                              "w4a4_m16_down", "w4a4_m16", "draft_sample"],
+                                              "w4a4_m16_down", "w4a4_m16", "w4a4_m16_gateup", "draft_sample"],
                     help="run one kernel a few times on a single LM-head-sized case (for ncu)")
     ap.add_argument("--profile-reps", type=int, default=3)
     return ap.parse_args()
@@ -141,11 +141,13 @@ def profile_case(name, reps):
         xq, sx, qs = q.quant_act_int4(syn.activations(4096, 4096, 50, device=dev))
         for _ in range(reps):
             q.linear_w4a4(xq, sx, qs, packed, sz)
-    elif name in ("w4a4_m32", "w4a4_m16_down", "w4a4_m16"):
+    elif name in ("w4a4_m32", "w4a4_m16_down", "w4a4_m16", "w4a4_m16_gateup"):
         # the decode-batch W4A4 tensor-core kernel: the LM head at 32 tokens,
-        # or the 4096 x 14336 down projection at 16 (groups split over 4-CTA
-        # clusters); the tensor-memory GEMV on the LM head at 16 tokens
-        M, Nn, Kk = {"w4a4_m32": (32, N, K), "w4a4_m16_down": (16, 4096, 14336), "w4a4_m16": (16, N, K)}[name]
+        # the 4096 x 14336 down projection at 16 (groups split over 4-CTA
+        # clusters), or the 28672 x 4096 gate/up projection at 16 (one CTA per
+        # 128-channel tile); the tensor-memory GEMV on the LM head at 16 tokens
+        M, Nn, Kk = {"w4a4_m32": (32, N, K), "w4a4_m16_down": (16, 4096, 14336), "w4a4_m16": (16, N, K),
+                     "w4a4_m16_gateup": (16, 28672, 4096)}[name]
         codes, s, z = syn.weights(Nn, Kk, 41, device=dev)
         packed, sz = q.pack_weights(codes, s, z)
         del codes
